@@ -1,0 +1,176 @@
+"""KV-pool helpers of the oracle: widening, the INT8 codec, page tables, appends.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Paged KV with 64-token pages and an INT8 cache follow the v100llm article
+(sections 1-2: "Paged KV cache", INT4/INT8/FP16 storage).  The pages give no
+quantisation rule; the one written here is the workload's own statement:
+symmetric INT8 per (pool row, KV head) with an fp16 scale, x = q * s.
+Readings (the pages are silent on each):
+
+* ``s = fp16(min(amax / 127, 65504))`` where ``amax / 127`` is one correctly
+  rounded fp32 division and the fp16 conversion rounds to nearest even;
+* ``q = clamp(round_half_even(x / s), -127, 127)`` with ``x / s`` one correctly
+  rounded fp32 division; ``s == 0`` gives ``q = 0``;
+* dequantisation is ``float32(q) * float32(s)``, which is exact in fp32 (an
+  8-bit by 11-bit significand product), so bit-exact agreement is well defined;
+* scales are stored per 64-row page and KV head, 64 to a run:
+  ``scale[r // 64, g, r % 64]``.
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+import numpy as np
+
+PAGE = 64
+
+
+# ---------------------------------------------------------------------------
+# widening of the 16-bit storage formats
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> float64 (exact: bf16 is the top half of fp32)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def widen_f16(bits: np.ndarray) -> np.ndarray:
+    """IEEE half bit patterns -> float64 (exact)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def widen(bits: np.ndarray, fmt: str) -> np.ndarray:
+    if fmt == "bf16":
+        return widen_bf16(bits)
+    if fmt == "f16":
+        return widen_f16(bits)
+    raise ValueError(fmt)
+
+
+# ---------------------------------------------------------------------------
+# INT8 codec
+
+
+def quantize_int8(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Symmetric INT8 per (row, head) over the last axis.
+
+    x: values exactly representable in fp32 (widened fp16/bf16), shape [N, H, D].
+    Returns (q int8 [N, H, D], s float16 [N, H]).
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)                       # exact
+    ratio = amax / np.float32(127.0)                          # fp32, correctly rounded
+    s16 = np.minimum(ratio, np.float32(65504.0)).astype(np.float16)   # nearest-even into fp16
+    s32 = s16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        quot = x32 / s32                                      # fp32, correctly rounded
+    qv = np.clip(np.rint(quot), -127, 127)                    # rint: ties to even
+    qv = np.where(s32 == 0, 0, qv)
+    return qv.astype(np.int8), s16
+
+
+def dequantize_int8(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """float32(q) * float32(s), per (row, head) scale broadcast over the last axis."""
+    return np.asarray(q, dtype=np.float32) * np.asarray(s, dtype=np.float16).astype(np.float32)[..., None]
+
+
+def pack_scales(s: np.ndarray) -> np.ndarray:
+    """Per-(row, head) scales [R, H] -> the stored layout [R/64, H, 64]."""
+    R, H = s.shape
+    assert R % PAGE == 0
+    return np.ascontiguousarray(s.reshape(R // PAGE, PAGE, H).transpose(0, 2, 1))
+
+
+def unpack_scales(sp: np.ndarray) -> np.ndarray:
+    """The stored layout [R/64, H, 64] -> per-(row, head) scales [R, H]."""
+    P, H, _ = sp.shape
+    return np.ascontiguousarray(sp.transpose(0, 2, 1).reshape(P * PAGE, H))
+
+
+# ---------------------------------------------------------------------------
+# INT4 codec (paged INT4 KV, v100llm article section 2)
+
+
+def quantize_int4(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Symmetric INT4 per (row, head): levels -7..7, fp16 scale, two codes per byte.
+
+    Readings (the pages name INT4 KV but give no rule): same steps as INT8 with
+    127 replaced by 7; codes are stored as 4-bit two's complement, element
+    ``2t`` in the low nibble and ``2t+1`` in the high nibble of byte ``t``.
+    Returns (packed uint8 [N, H, D/2], s float16 [N, H]).
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    ratio = amax / np.float32(7.0)
+    s16 = np.minimum(ratio, np.float32(65504.0)).astype(np.float16)
+    s32 = s16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        quot = x32 / s32
+    qv = np.clip(np.rint(quot), -7, 7)
+    qv = np.where(s32 == 0, 0, qv).astype(np.int64)
+    nib = (qv & 0xF).astype(np.uint8)
+    packed = nib[..., 0::2] | (nib[..., 1::2] << np.uint8(4))
+    return packed.astype(np.uint8), s16
+
+
+def dequantize_int4(packed: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Unpack two's-complement nibbles and multiply by the fp16 scale (exact in fp32)."""
+    p = np.asarray(packed, dtype=np.uint8).astype(np.int64)
+    lo = p & 0xF
+    hi = (p >> 4) & 0xF
+    codes = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.int64)
+    codes[..., 0::2] = lo
+    codes[..., 1::2] = hi
+    codes = np.where(codes >= 8, codes - 16, codes)
+    return codes.astype(np.float32) * np.asarray(s, dtype=np.float16).astype(np.float32)[..., None]
+
+
+# ---------------------------------------------------------------------------
+# page tables
+
+
+def page_table_to_rows(page_table: np.ndarray, seq_len: np.ndarray, list_len: int, page: int = PAGE) -> np.ndarray:
+    """Expand per-sequence page tables into row lists.
+
+    Position ``j`` of sequence ``s`` lives in page ``page_table[s, j // page]``
+    at offset ``j % page``, so its pool row is ``page_id * page + j % page``;
+    positions at or beyond ``seq_len[s]`` (and up to ``list_len``) are padding,
+    written as -1.
+    """
+    S = page_table.shape[0]
+    out = np.full((S, list_len), -1, dtype=np.int32)
+    for s in range(S):
+        for j in range(min(int(seq_len[s]), list_len)):
+            page_id = int(page_table[s, j // page])
+            out[s, j] = page_id * page + (j % page)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# appending new rows to the pool
+
+
+def append_rows(pool: np.ndarray, new: np.ndarray, dst_rows: np.ndarray,
+                pool_scales: Optional[np.ndarray] = None, fmt: str = "copy"):
+    """Write ``new[i]`` into pool row ``dst_rows[i]`` (negative = skip).
+
+    fmt 'copy': ``pool`` holds raw 16-bit patterns [R, H, D] and is written as is.
+    fmt 'int8': ``new`` holds fp32-exact values; each row is quantised with
+    ``quantize_int8`` into ``pool`` (int8 [R, H, D]) and ``pool_scales`` (the
+    stored layout [R/64, H, 64], fp16).
+    Returns the updated (pool, pool_scales) copies.
+    """
+    pool = pool.copy()
+    sc = None if pool_scales is None else pool_scales.copy()
+    if fmt == "int8":
+        qv, s = quantize_int8(new)
+    for i, r in enumerate(np.asarray(dst_rows).tolist()):
+        if r < 0:
+            continue
+        if fmt == "copy":
+            pool[r] = new[i]
+        else:
+            pool[r] = qv[i]
+            sc[r // PAGE, :, r % PAGE] = s[i]
+    return pool, sc
