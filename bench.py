@@ -1,0 +1,454 @@
+"""Benchmark of row-indexed attention over a unified KV pool on GB300.
+
+Default workload: decode, bf16, 4 sequences x 16,384 rows in a 65,536-row
+shuffled pool, 32 query / 8 KV heads, head_dim 128, one query token per
+sequence (lists sorted ascending).  Metric: gathered-KV GB/s = listed rows x
+(K + V bytes) per KV head, per second; padding, indices, Q and O excluded.
+
+``--workload prefill_bf16`` measures the prefill chunk (4 x 2,048 query rows
+over 99,936-row lists in a 400,000-row pool, causal) in tensor TFLOP/s with
+4*D FLOPs per visible (query, key, head) triple.
+
+One JSON line on stdout (rank 0).  Under torchrun each rank runs an
+independent replica of the workload (the path shards by sequence with no
+exchange), timing is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle legs run one BLAS thread per worker process
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "row-indexed attention: decode gathered-KV GB/s, prefill TFLOP/s (vs GB300 roofline)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "decode": ["row_indexed_flash_gb300/csrc/decode.cuh", "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
+    "prefill": ["row_indexed_flash_gb300/csrc/prefill.cu", "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
+}
+PROFILE_FILES = {
+    "decode_bf16": "profiles/decode_bf16_4x16384_ncu.txt",
+    "prefill_bf16": "profiles/prefill_bf16_4x2048x99936_ncu.txt",
+}
+
+
+# ---------------------------------------------------------------------------
+# workload accounting
+
+
+def decode_bytes(p) -> int:
+    """Algorithmic bytes: each listed row is read once per KV head (K and V)."""
+    per = 2 * p.D * (1 if p.kv_int8 else 2) + (4 if p.kv_int8 else 0)
+    return p.n_valid() * p.Hkv * per
+
+
+def prefill_flops(p) -> int:
+    """4*D per visible (query, key, head): QK^T and PV, 2*D each."""
+    n = p.L
+    vis = 0
+    for i in range(p.Nq):
+        vis += max(0, min(n, n - p.Nq + i + 1))
+    return 4 * p.D * p.Hq * p.S * vis
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        out = dict(FALLBACK_PEAKS)
+        for k in out:
+            for cand in (k, k.replace("_gbs", "_GBs")):
+                if isinstance(d.get(cand), (int, float)):
+                    out[k] = float(d[cand])
+        return out, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, kind: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, PROFILE_FILES.get(workload, ""))
+    if not os.path.isfile(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.strip().split("=", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha") != source_sha(kind):
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs (fork pool, created before any CUDA call)
+
+_P = None
+
+
+def _oracle_unit(args):
+    import oracle
+    s, g = args
+    p = _P
+    G = p.Hq // p.Hkv
+    q = oracle.widen(p.q[s:s + 1, :, g * G:(g + 1) * G], p.dtype)
+    oracle.attend_rows(q, p.k[:, g:g + 1], p.v[:, g:g + 1], p.kv_rows[s:s + 1], p.scale, causal=p.causal,
+                       kv_len=None if p.kv_len is None else p.kv_len[s:s + 1], kv_format=p.dtype)
+    return s, g
+
+
+def oracle_rate(p, units, passes: int, procs: int):
+    """Gathered-KV GB/s of the oracle over ``units`` (slice, KV head) pairs."""
+    global _P
+    _P = p
+    per_unit_bytes = {}
+    rb = 2 * p.D * 2
+    for s, g in units:
+        per_unit_bytes[(s, g)] = int((p.kv_rows[s] >= 0).sum()) * rb
+    ctx = mp.get_context("fork")
+    with ctx.Pool(procs) as pool:
+        t0 = time.perf_counter()
+        for _ in range(passes):
+            pool.map(_oracle_unit, units, chunksize=1)
+        dt = time.perf_counter() - t0
+    total = passes * sum(per_unit_bytes[u] for u in units)
+    return total / dt / 1e9, dt
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.out:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+
+def build_problem(workload: str):
+    if workload == "decode_bf16":
+        return synth.decode_bf16_large()
+    if workload == "prefill_bf16":
+        return synth.prefill_bf16()
+    raise SystemExit(f"unknown workload {workload}")
+
+
+def run_gpu(args, rank, world, p, cpu_baseline):
+    import torch
+    import torch.distributed as dist
+
+    import row_indexed_flash_gb300 as far
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    tdt = torch.bfloat16 if p.dtype == "bf16" else torch.float16
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt).to(dev)
+
+    is_prefill = args.workload.startswith("prefill")
+    q = to_dev(p.q)
+    rows = torch.from_numpy(p.kv_rows).to(dev)
+    k0, v0 = to_dev(p.k), to_dev(p.v)
+    pool_bytes = 2 * k0.numel() * k0.element_size()
+    # rotate over enough pool copies that each step reads data not left in L2
+    n_copies = max(1, min(3, int(math.ceil(3 * 129e6 / pool_bytes)) + 1)) if not is_prefill else 1
+    pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(n_copies - 1)]
+    out = torch.empty((p.S, p.Nq, p.Hq, p.D), dtype=torch.float32, device=dev)
+    a_list = []
+    for (k, v) in pools:
+        a, _, _ = far.make_args(q, k, v, rows, p.scale, causal=p.causal, out=out)
+        a_list.append(a)
+    entry = far.lib().fa_rows_prefill if is_prefill else far.lib().fa_rows_decode
+    need = far.fa_rows_workspace_size(a_list[0], is_prefill)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    sh = stream.cuda_stream
+    import ctypes
+
+    def step(i):
+        st = entry(ctypes.byref(a_list[i % len(a_list)]), ws.data_ptr(), ws.numel(), sh)
+        if st != 0:
+            raise far.FaRowsError(st, far.fa_last_error())
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_launch_ms = sum(launch_ms) / len(launch_ms)
+
+    # end to end through the public API: pinned host inputs copied in every step,
+    # the output read back every step
+    hq = torch.from_numpy(np.ascontiguousarray(p.q).view(np.int16)).view(tdt).pin_memory()
+    hk = torch.from_numpy(np.ascontiguousarray(p.k).view(np.int16)).view(tdt).pin_memory()
+    hv = torch.from_numpy(np.ascontiguousarray(p.v).view(np.int16)).view(tdt).pin_memory()
+    hr = torch.from_numpy(p.kv_rows).pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv, dr = torch.empty_like(q), torch.empty_like(k0), torch.empty_like(v0), torch.empty_like(rows)
+    a_e2e, _, _ = far.make_args(dq, dk, dv, dr, p.scale, causal=p.causal, out=out)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hr))
+    d2h = hout.numel() * hout.element_size()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dr.copy_(hr, non_blocking=True)
+        st = entry(ctypes.byref(a_e2e), ws.data_ptr(), ws.numel(), sh)
+        if st != 0:
+            raise far.FaRowsError(st, far.fa_last_error())
+        hout.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    step_ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms, e2e_ms, mean_launch_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms, mean_launch_ms = t.tolist()
+    if rank != 0:
+        return None
+
+    pk, pk_src = peaks()
+    kind = "prefill" if is_prefill else "decode"
+    if is_prefill:
+        work = prefill_flops(p)
+        unit, scale_ = "TFLOP/s", 1e12
+        peak = pk["bf16_tflops_sustained" if args.steps * step_ms > 2000 else "bf16_tflops"]
+        bound = "tensor"
+    else:
+        work = decode_bytes(p)
+        unit, scale_ = "GB/s", 1e9
+        peak = pk["hbm_gbs"]
+        bound = "hbm"
+    value = world * work / (step_ms * 1e-3) / scale_
+    achieved = work / (mean_launch_ms * 1e-3) / scale_
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": unit,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": p.dtype,
+        "data": "synthetic (seeded N(0,1) values, generator shapes of the pages' workloads)",
+        "config": {
+            "workload": p.name,
+            "kv_rows": f"[{p.S}, {p.L}] int32",
+            "n_valid_rows": p.n_valid(),
+            "l2": (f"inputs larger than L2: {len(pools)} pool copies of {pool_bytes / 1e6:.0f} MB rotated"
+                   if not is_prefill else f"pool {pool_bytes / 1e9:.2f} GB > L2"),
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": bound,
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_source": pk_src,
+            "unit": unit,
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(args.workload, kind),
+            "kernel": "fa_rows_prefill_kernel" if is_prefill else "fa_rows_decode_kernel",
+            "kernel_ms": round(mean_launch_ms, 5),
+            "work_per_launch": work,
+        },
+        "e2e": {
+            "value": round(world * work / (e2e_ms * 1e-3) / scale_, 2),
+            "unit": unit,
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms, 4),
+        },
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu_baseline,
+    }
+    return res
+
+
+# ---------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="decode_bf16", choices=["decode_bf16", "prefill_bf16"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    procs = os.cpu_count() or 1
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        p = build_problem(args.workload)
+        if args.workload.startswith("prefill"):
+            print(json.dumps({"impl": "reference", "unavailable": "the fp64 oracle arm is timed for decode only"}))
+            return
+        units = [(s, g) for s in range(p.S) for g in range(p.Hkv)][:procs]
+        for _ in range(args.warmup):
+            oracle_rate(p, units[:1], 1, 1)
+        t0 = time.perf_counter()
+        moved = 0
+        for _ in range(args.steps):
+            r, dt = oracle_rate(p, units, 1, procs)
+            moved += r * dt * 1e9
+        dt = time.perf_counter() - t0
+        v = moved / dt / 1e9
+        sample = f"{len(units)} of {p.S * p.Hkv} (slice, KV head) units per step, fp64 oracle, {procs} processes"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": p.name},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": procs, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    p = build_problem(args.workload)
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload.startswith("prefill"):
+        units = [(s, g) for s in range(p.S) for g in range(p.Hkv)]
+        passes = 3
+        v, dt = oracle_rate(p, units, passes, procs)
+        cpu_baseline = {"value": round(v, 4), "unit": "GB/s", "cores": procs, "kind": "oracle",
+                        "sample": f"whole workload ({len(units)} (slice, KV head) units) x {passes} passes, "
+                                  f"{dt:.1f} s wall"}
+    res = run_gpu(args, rank, world, p, cpu_baseline)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

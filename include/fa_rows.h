@@ -1,0 +1,185 @@
+/*
+ * fa_rows.h — row-indexed flash attention over a unified KV pool (C ABI).
+ *
+ * The operation ("llama.cpp 0.9.0 inference boundaries", section 1, the
+ * ggml_flash_attn_ext_rows paragraph): every sequence's K/V rows share one
+ * storage pool; each query slice carries its own integer kv_rows list naming
+ * the pool rows it attends to; a negative row index is padding whose mask is
+ * minus infinity.  The next paragraph of that section fixes that the result is
+ * exact attention over the listed rows, not a lossy summary.
+ *
+ * Paged KV with 64-token pages and an INT8 cache: the v100llm article,
+ * sections 1-2 ("FlashAttention 1.5 SM70 kernels", "Paged KV cache").
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers, row-major and contiguous, owned
+ *    by the caller.  The library never allocates device memory, never
+ *    synchronises, and enqueues all work on the given stream.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    returned as a status; nothing is thrown across this boundary.  A failed
+ *    launch returns FA_ERR_CUDA; fa_last_error() then names the CUDA error.
+ *  - Row indices are NOT range-checked by the attention calls (that would cost
+ *    a pass over the lists); fa_rows_validate() checks them on the device and
+ *    reports through a status word, without trapping.
+ */
+#ifndef FA_ROWS_H
+#define FA_ROWS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, inconsistent shape        */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but outside the shapes/dtypes built here   */
+  FA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required        */
+  FA_ERR_INDEX_OOB = 4,    /* reported by fa_rows_validate through its status   */
+  FA_ERR_CUDA = 5          /* a CUDA launch or runtime call failed              */
+} fa_status;
+
+typedef enum fa_dtype { FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2, FA_I8 = 3, FA_I4 = 4 } fa_dtype;
+
+typedef enum fa_mask_kind {
+  FA_MASK_NONE = 0,
+  /* additive fp32 mask [S, Nq, L], aligned with list POSITION j (not pool row);
+   * minus infinity removes an entry.  Section 1's "corresponding mask". */
+  FA_MASK_DENSE = 1,
+  /* bottom-right causal: the slice's Nq queries are the last Nq positions of
+   * its n_s list entries, so query i sees list positions j <= n_s - Nq + i. */
+  FA_MASK_CAUSAL = 2
+} fa_mask_kind;
+
+/*
+ * Arguments of one row-indexed attention call.
+ *
+ *   q        [S, Nq, Hq, D]     FA_F16 or FA_BF16
+ *   k, v     [R, Hkv, D]        the unified pool: FA_F16/FA_BF16 (same as q),
+ *                               or FA_I8 (int8 codes, then k_scale/v_scale)
+ *   k_scale, v_scale            FA_I8 only: fp16 bit patterns laid out
+ *                               [R/64, Hkv, 64], i.e. the scale of (row r,
+ *                               head g) sits at ((r/64)*Hkv + g)*64 + r%64;
+ *                               value = code * scale (R must be a multiple of 64)
+ *   kv_rows  [S, L] int32       pool row of list entry j of slice s; negative =
+ *                               padding.  Duplicates count once per occurrence.
+ *   kv_len   [S] int32 or NULL  n_s: entries at positions >= kv_len[s] are
+ *                               padding (NULL: n_s = L)
+ *   mask     [S, Nq, L] fp32    FA_MASK_DENSE only
+ *   out      [S, Nq, Hq, D]     FA_F32, FA_BF16 or FA_F16
+ *   lse      [S, Nq, Hq] fp32   optional natural-log log-sum-exp of the logits
+ *
+ * Query head h reads KV head h / (Hq/Hkv).  Logit of entry j for query i:
+ * scale * <q, K[row]> (+ mask[s,i,j]).  A query with no visible entry gets
+ * out = 0 and lse = -inf.
+ *
+ * n_valid_hint: optional host-side count of listed entries summed over all
+ * slices (0 = unknown); it only steers how the list is split across SMs.
+ */
+typedef struct fa_rows_args {
+  const void* q;
+  fa_dtype q_dtype;
+  const void* k;
+  const void* v;
+  fa_dtype kv_dtype;
+  const uint16_t* k_scale;
+  const uint16_t* v_scale;
+  int64_t n_pool_rows;
+  const int32_t* kv_rows;
+  int32_t list_len;
+  const int32_t* kv_len;
+  fa_mask_kind mask_kind;
+  const float* mask;
+  float scale;
+  void* out;
+  fa_dtype out_dtype;
+  float* lse;
+  int32_t S, Nq, Hq, Hkv, D;
+  int64_t n_valid_hint;
+} fa_rows_args;
+
+/*
+ * Bytes of scratch that fa_rows_decode / fa_rows_prefill need for these
+ * arguments (0 when none).  The decode scratch holds per-split partial results
+ * and one arrival counter per (slice, KV head); it must be ZERO-FILLED once
+ * after allocation (fa_rows_workspace_init) — every call leaves the counters
+ * at zero again.  One workspace must not be used by two calls that can run at
+ * the same time.  Returns 0 and sets fa_last_error() on invalid arguments.
+ */
+size_t fa_rows_workspace_size(const fa_rows_args* a, int is_prefill);
+fa_status fa_rows_workspace_init(void* ws, size_t ws_bytes, fa_stream_t stream);
+
+/*
+ * Decode: few query rows per slice (Nq * Hq/Hkv <= 32).  Split-KV over the
+ * list, online softmax per split, cross-split merge inside the same launch.
+ * D in {64, 128, 256}; Hq/Hkv a power of two up to 32 (times Nq).
+ */
+fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_stream_t stream);
+
+/*
+ * Prefill: many query rows per slice.  QK^T and PV on the tensor cores
+ * (tcgen05, accumulators in tensor memory), K/V tiles gathered by row index.
+ * D = 128, FA_BF16 or FA_F16 for q and the pool; Nq >= 1.
+ */
+fa_status fa_rows_prefill(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_stream_t stream);
+
+/*
+ * Range check of the lists (section 1: negative = padding; anything else must
+ * name a pool row).  d_status is a device int64[2] that this call overwrites:
+ * [0] = number of entries with kv_rows >= n_pool_rows (within kv_len),
+ * [1] = flat index s*L + j of the first such entry, or -1.
+ * Returns FA_OK once the check is enqueued; the caller reads d_status.
+ */
+fa_status fa_rows_validate(const fa_rows_args* a, int64_t* d_status, fa_stream_t stream);
+
+/*
+ * Page tables -> row lists (v100llm article, section 2: 64-token pages).
+ * page_table [n_seq, max_pages] int32 page ids; seq_len [n_seq] int32 (device).
+ * kv_rows [n_seq, list_len] is written as page_id*page_size + j%page_size for
+ * j < seq_len[s] and -1 elsewhere.  seq_len values above max_pages*page_size
+ * are clamped to it.
+ */
+fa_status fa_kv_page_table_to_rows(const int32_t* page_table, int32_t max_pages, const int32_t* seq_len,
+                                   int32_t n_seq, int32_t page_size, int32_t* kv_rows, int32_t list_len,
+                                   fa_stream_t stream);
+
+/*
+ * INT8 KV quantisation, per (row, KV head) with an fp16 scale (value = q*s):
+ * s = fp16_rne(min(amax/127, 65504)) with amax/127 one fp32 division;
+ * q = clamp(rint_half_even(x/s), -127, 127) with x/s one fp32 division;
+ * s = 0 gives q = 0.
+ *   x        [n_rows, Hkv, D] FA_F16 or FA_BF16 (x_dtype)
+ *   dst_rows [n_rows] int32 pool rows to write, negative = skip; NULL = row i
+ *   q        [R, Hkv, D] int8 pool; scale the fp16 layout of fa_rows_args.
+ * This is also the KV append of a ubatch into an INT8 pool.
+ */
+fa_status fa_kv_quantize_int8(const void* x, fa_dtype x_dtype, int64_t n_rows, int32_t Hkv, int32_t D,
+                              const int32_t* dst_rows, int8_t* q, uint16_t* scale, int64_t n_pool_rows,
+                              fa_stream_t stream);
+
+/* out[r, g, d] = float(q[r, g, d]) * float(scale of (r, g)), exact in fp32. */
+fa_status fa_kv_dequantize_int8(const int8_t* q, const uint16_t* scale, int64_t n_rows, int32_t Hkv, int32_t D,
+                                float* out, fa_stream_t stream);
+
+/*
+ * KV append for 16-bit pools: pool[dst_rows[i]] = x[i] for i < n_rows
+ * (negative dst = skip).  x and pool are [*, Hkv, D] of the same 16-bit dtype.
+ */
+fa_status fa_kv_append(const void* x, fa_dtype dtype, int64_t n_rows, int32_t Hkv, int32_t D,
+                       const int32_t* dst_rows, void* pool, int64_t n_pool_rows, fa_stream_t stream);
+
+const char* fa_status_string(fa_status s);
+/* Text of the last error seen by the calling thread ("" if none). */
+const char* fa_last_error(void);
+/* Library build tag, e.g. "fa_rows sm_103a". */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_ROWS_H */

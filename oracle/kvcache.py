@@ -136,14 +136,18 @@ def page_table_to_rows(page_table: np.ndarray, seq_len: np.ndarray, list_len: in
     Position ``j`` of sequence ``s`` lives in page ``page_table[s, j // page]``
     at offset ``j % page``, so its pool row is ``page_id * page + j % page``;
     positions at or beyond ``seq_len[s]`` (and up to ``list_len``) are padding,
-    written as -1.
+    written as -1.  Reading (the pages are silent): a negative page id marks an
+    unused page-table slot, so its positions are padding (-1) as well, and
+    ``seq_len`` is clamped to the table's ``max_pages * page`` positions.
     """
     S = page_table.shape[0]
     out = np.full((S, list_len), -1, dtype=np.int32)
+    max_pos = page_table.shape[1] * page
     for s in range(S):
-        for j in range(min(int(seq_len[s]), list_len)):
+        for j in range(min(int(seq_len[s]), list_len, max_pos)):
             page_id = int(page_table[s, j // page])
-            out[s, j] = page_id * page + (j % page)
+            if page_id >= 0:
+                out[s, j] = page_id * page + (j % page)
     return out
 
 

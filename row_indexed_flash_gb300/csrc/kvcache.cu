@@ -1,0 +1,195 @@
+// KV-pool kernels: page-table expansion, INT8 quantise / dequantise, 16-bit
+// row appends and the row-list range check.
+//
+// Paged KV with 64-token pages and INT8 storage: v100llm article, sections
+// 1-2.  Negative row = padding: "llama.cpp 0.9.0 inference boundaries",
+// section 1.
+#include <limits.h>
+
+#include "fa_internal.cuh"
+
+namespace far {
+
+// kv_rows[s, j] = page_table[s, j/page]*page + j%page for j < seq_len[s], else -1.
+// One thread writes four consecutive positions.
+__global__ void page_table_to_rows_kernel(const int32_t* __restrict__ pt, int max_pages,
+                                          const int32_t* __restrict__ seq_len, int n_seq, int page,
+                                          int32_t* __restrict__ rows, int list_len) {
+  const long long quads = (long long)n_seq * ((list_len + 3) / 4);
+  const int qpr = (list_len + 3) / 4;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < quads;
+       t += (long long)gridDim.x * blockDim.x) {
+    const int s = (int)(t / qpr);
+    const int j0 = (int)(t % qpr) * 4;
+    int len = seq_len[s];
+    len = min(max(len, 0), max_pages * page);
+    int out[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      int r = -1;
+      if (j < len) {
+        const int pid = __ldg(pt + (size_t)s * max_pages + j / page);
+        r = pid >= 0 ? pid * page + j % page : -1;
+      }
+      out[u] = r;
+    }
+    int32_t* dst = rows + (size_t)s * list_len + j0;
+    if ((list_len & 3) == 0) {
+      *reinterpret_cast<int4*>(dst) = make_int4(out[0], out[1], out[2], out[3]);
+    } else {
+      for (int u = 0; u < 4 && j0 + u < list_len; ++u) dst[u] = out[u];
+    }
+  }
+}
+
+cudaError_t launch_page_table_to_rows(const int32_t* pt, int max_pages, const int32_t* seq_len, int n_seq, int page,
+                                      int32_t* rows, int list_len, cudaStream_t st) {
+  const long long quads = (long long)n_seq * ((list_len + 3) / 4);
+  if (quads == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (quads + threads - 1) / threads;
+  page_table_to_rows_kernel<<<(unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0, st>>>(
+      pt, max_pages, seq_len, n_seq, page, rows, list_len);
+  return cudaGetLastError();
+}
+
+// One warp per (source row, head): amax over D, fp16 scale, int8 codes.
+__global__ void quantize_int8_kernel(const uint16_t* __restrict__ x, int x_bf16, long long n_rows, int Hkv, int D,
+                                     const int32_t* __restrict__ dst_rows, int8_t* __restrict__ q,
+                                     uint16_t* __restrict__ scale, long long R) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+  for (long long w = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5); w < n_rows * Hkv; w += warps) {
+    const long long i = w / Hkv;
+    const int g = (int)(w % Hkv);
+    const long long dst = dst_rows ? (long long)dst_rows[i] : i;
+    if (dst < 0 || dst >= R) continue;
+    const uint16_t* src = x + (size_t)w * D;
+    float vals[8];   // D <= 256
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int d = lane + 32 * u;
+      float f = 0.f;
+      if (d < D) {
+        const uint32_t b = src[d];
+        f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
+      }
+      vals[u] = f;
+      amax = fmaxf(amax, fabsf(f));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const __half sh = __float2half_rn(fminf(__fdiv_rn(amax, 127.0f), 65504.0f));
+    const float sf = __half2float(sh);
+    int8_t* qd = q + ((size_t)dst * Hkv + g) * D;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int d = lane + 32 * u;
+      if (d < D) {
+        int c = 0;
+        if (sf != 0.f) c = min(max(__float2int_rn(__fdiv_rn(vals[u], sf)), -127), 127);
+        qd[d] = (int8_t)c;
+      }
+    }
+    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = __half_as_ushort(sh);
+  }
+}
+
+cudaError_t launch_quantize_int8(const void* x, int x_bf16, long long n_rows, int Hkv, int D, const int32_t* dst,
+                                 int8_t* q, uint16_t* scale, long long R, cudaStream_t st) {
+  const long long warps = n_rows * Hkv;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (warps + 7) / 8;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  quantize_int8_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint16_t*>(x), x_bf16, n_rows, Hkv, D,
+                                                             dst, q, scale, R);
+  return cudaGetLastError();
+}
+
+// out = float(code) * float(scale): both factors are exact in fp32 and the
+// product of an 8-bit and an 11-bit significand is exact too.
+__global__ void dequantize_int8_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ scale,
+                                       long long n_rows, int Hkv, int D, float* __restrict__ out) {
+  const long long n = n_rows * Hkv * D;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n; t += (long long)gridDim.x * blockDim.x) {
+    const long long rh = t / D;
+    const long long r = rh / Hkv;
+    const int g = (int)(rh % Hkv);
+    const float s = __half2float(__ushort_as_half(scale[((size_t)(r / kPage) * Hkv + g) * kPage + (r % kPage)]));
+    out[t] = __fmul_rn((float)q[t], s);
+  }
+}
+
+cudaError_t launch_dequantize_int8(const int8_t* q, const uint16_t* scale, long long n_rows, int Hkv, int D,
+                                   float* out, cudaStream_t st) {
+  const long long n = n_rows * Hkv * D;
+  if (n == 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  dequantize_int8_kernel<<<(unsigned)blocks, 256, 0, st>>>(q, scale, n_rows, Hkv, D, out);
+  return cudaGetLastError();
+}
+
+// pool[dst_rows[i]] = x[i]; one CTA per source row, 16-byte copies.
+__global__ void kv_append_kernel(const uint4* __restrict__ x, long long n_rows, int row_vec,
+                                 const int32_t* __restrict__ dst_rows, uint4* __restrict__ pool, long long R) {
+  for (long long i = blockIdx.x; i < n_rows; i += gridDim.x) {
+    const long long dst = dst_rows[i];
+    if (dst < 0 || dst >= R) continue;
+    for (int c = threadIdx.x; c < row_vec; c += blockDim.x) pool[(size_t)dst * row_vec + c] = x[(size_t)i * row_vec + c];
+  }
+}
+
+cudaError_t launch_kv_append(const void* x, long long n_rows, int row_bytes, const int32_t* dst, void* pool,
+                             long long R, cudaStream_t st) {
+  if (n_rows == 0) return cudaSuccess;
+  const long long blocks = n_rows < 152 * 32 ? n_rows : 152 * 32;
+  kv_append_kernel<<<(unsigned)blocks, 128, 0, st>>>(static_cast<const uint4*>(x), n_rows, row_bytes / 16, dst,
+                                                     static_cast<uint4*>(pool), R);
+  return cudaGetLastError();
+}
+
+// status[0] += number of entries >= R (within kv_len); status[1] = min flat index
+// of such an entry, kept as unsigned so that the initial all-ones reads as -1.
+__global__ void validate_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ kv_len, int S, int L,
+                                long long R, unsigned long long* status) {
+  const long long n = (long long)S * L;
+  unsigned long long bad = 0, first = ~0ull;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n; t += (long long)gridDim.x * blockDim.x) {
+    const int s = (int)(t / L), j = (int)(t % L);
+    const int len = kv_len ? min(max(kv_len[s], 0), L) : L;
+    if (j < len && (long long)rows[t] >= R) {
+      ++bad;
+      if ((unsigned long long)t < first) first = (unsigned long long)t;
+    }
+  }
+  for (int o = 16; o >= 1; o >>= 1) {
+    bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    const unsigned long long f2 = __shfl_xor_sync(0xffffffffu, first, o);
+    first = f2 < first ? f2 : first;
+  }
+  if ((threadIdx.x & 31) == 0 && bad) {
+    atomicAdd(status, bad);
+    atomicMin(status + 1, first);
+  }
+}
+
+cudaError_t launch_validate(const int32_t* rows, const int32_t* kv_len, int S, int L, long long R, long long* status,
+                            cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(long long), st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(status + 1, 0xff, sizeof(long long), st);
+  if (e != cudaSuccess) return e;
+  const long long n = (long long)S * L;
+  if (n == 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  validate_kernel<<<(unsigned)blocks, 256, 0, st>>>(rows, kv_len, S, L, R,
+                                                    reinterpret_cast<unsigned long long*>(status));
+  return cudaGetLastError();
+}
+
+}  // namespace far

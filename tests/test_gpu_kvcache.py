@@ -1,0 +1,123 @@
+"""KV-pool kernels against the oracle: bit-exact page expansion, INT8 codes,
+scales and dequantisation, row appends; and INT8 paged decode parity."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import row_indexed_flash_gb300 as far
+import synth
+from helpers import assert_lse, assert_parity, dev_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def test_page_table_expansion_is_bit_exact():
+    p = synth.paged_int8(n_seq=9, lo=1, hi=5000)
+    pt = torch.from_numpy(p.page_table).cuda()
+    sl = torch.from_numpy(p.seq_len).cuda()
+    for L in (p.L, p.L + 3, p.L - 1):
+        got = far.fa_kv_page_table_to_rows(pt, sl, L)
+        want = oracle.page_table_to_rows(p.page_table, p.seq_len, L)
+        assert np.array_equal(got.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 128), ("bf16", 256), ("bf16", 64), ("f16", 96)])
+def test_int8_quantise_and_dequantise_are_bit_exact(dtype, D):
+    g = synth.rng(77)
+    R, H = 640, 4
+    bits = synth.normal_bits(g, (R, H, D), dtype)
+    bits[3, 1] = 0                                   # an all-zero (row, head): scale 0
+    x = dev_bits(bits, dtype)
+    q, s = far.fa_kv_quantize_int8(x, R)
+    qo, so = oracle.quantize_int8(oracle.widen(bits, dtype).astype(np.float32))
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), oracle.pack_scales(so).view(np.uint16))
+    deq = far.fa_kv_dequantize_int8(q, s).cpu().numpy()
+    assert np.array_equal(deq.view(np.uint32), oracle.dequantize_int8(qo, so).view(np.uint32))
+
+
+def test_int8_append_scatters_into_named_rows():
+    g = synth.rng(78)
+    R, H, D, n = 256, 2, 128, 40
+    bits = synth.normal_bits(g, (n, H, D), "bf16")
+    dst = g.permutation(R)[:n].astype(np.int32)
+    dst[7] = -1
+    q, s = far.fa_kv_quantize_int8(dev_bits(bits, "bf16"), R, dst_rows=torch.from_numpy(dst).cuda())
+    pool0 = np.zeros((R, H, D), np.int8)
+    sc0 = np.zeros((R // 64, H, 64), np.float16)
+    qo, so = oracle.append_rows(pool0, oracle.widen_bf16(bits).astype(np.float32), dst, sc0, fmt="int8")
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), so.view(np.uint16))
+
+
+def test_append_16bit_rows():
+    g = synth.rng(79)
+    R, H, D, n = 300, 8, 128, 50
+    pool_bits = synth.normal_bits(g, (R, H, D), "bf16")
+    new_bits = synth.normal_bits(g, (n, H, D), "bf16")
+    dst = g.permutation(R)[:n].astype(np.int32)
+    dst[::9] = -3
+    pool = dev_bits(pool_bits, "bf16")
+    far.fa_kv_append(dev_bits(new_bits, "bf16"), torch.from_numpy(dst).cuda(), pool)
+    want, _ = oracle.append_rows(pool_bits, new_bits, dst)
+    assert np.array_equal(pool.cpu().view(torch.int16).numpy().view(np.uint16), want)
+
+
+def _int8_problem_on_device(p, slices=None):
+    """Quantise the bf16 pool on the device and, independently, in the oracle."""
+    k = dev_bits(p.k, "bf16")
+    v = dev_bits(p.v, "bf16")
+    kq, ks = far.fa_kv_quantize_int8(k, p.R)
+    vq, vs = far.fa_kv_quantize_int8(v, p.R)
+    del k, v
+    return kq, ks, vq, vs
+
+
+def _oracle_int8(p, rows, slices):
+    """Oracle attention over dequantised INT8 rows; quantises only the rows used."""
+    used = np.unique(rows[slices][rows[slices] >= 0])
+    kq, ks = oracle.quantize_int8(oracle.widen_bf16(p.k[used]).astype(np.float32))
+    vq, vs = oracle.quantize_int8(oracle.widen_bf16(p.v[used]).astype(np.float32))
+    kd = oracle.dequantize_int8(kq, ks).astype(np.float64)
+    vd = oracle.dequantize_int8(vq, vs).astype(np.float64)
+    remap = np.full(p.R, -1, np.int64)
+    remap[used] = np.arange(used.size)
+    r2 = np.where(rows[slices] >= 0, remap[np.maximum(rows[slices], 0)], -1).astype(np.int32)
+    q = oracle.widen_bf16(p.q[slices])
+    return oracle.attend_rows(q, kd, vd, r2, p.scale), (kq, ks, vq, vs, used)
+
+
+def test_paged_int8_decode_small():
+    p = synth.paged_int8(n_seq=6, lo=100, hi=9000)
+    rows_np = oracle.page_table_to_rows(p.page_table, p.seq_len, p.L)
+    kq, ks, vq, vs = _int8_problem_on_device(p)
+    rows = far.fa_kv_page_table_to_rows(torch.from_numpy(p.page_table).cuda(), torch.from_numpy(p.seq_len).cuda(), p.L)
+    assert np.array_equal(rows.cpu().numpy(), rows_np)
+    q = dev_bits(p.q, "bf16")
+    out, lse = far.fa_rows_decode(q, kq, vq, rows, p.scale, k_scale=ks, v_scale=vs, want_lse=True,
+                                  kv_len=torch.from_numpy(p.seq_len).cuda(), n_valid_hint=int(p.seq_len.sum()))
+    (ref, ref_lse), (okq, oks, _, _, used) = _oracle_int8(p, rows_np, slice(None))
+    assert np.array_equal(kq.cpu().numpy()[used], okq)
+    assert_parity(out, ref, "paged int8 small")
+    assert_lse(lse, ref_lse)
+
+
+@pytest.mark.slow
+def test_workload_paged_int8_full_size_sampled_slices():
+    p = synth.paged_int8()
+    rows_np = oracle.page_table_to_rows(p.page_table, p.seq_len, p.L)
+    kq, ks, vq, vs = _int8_problem_on_device(p)
+    rows = far.fa_kv_page_table_to_rows(torch.from_numpy(p.page_table).cuda(), torch.from_numpy(p.seq_len).cuda(), p.L)
+    assert np.array_equal(rows.cpu().numpy(), rows_np)
+    q = dev_bits(p.q, "bf16")
+    out, lse = far.fa_rows_decode(q, kq, vq, rows, p.scale, k_scale=ks, v_scale=vs, want_lse=True,
+                                  kv_len=torch.from_numpy(p.seq_len).cuda(), n_valid_hint=int(p.seq_len.sum()))
+    torch.cuda.synchronize()
+    # the oracle on a sample of slices: the longest, the shortest and four random ones
+    order = np.argsort(p.seq_len)
+    pick = sorted({int(order[0]), int(order[-1])} | set(synth.rng(5).choice(p.S, 4, replace=False).tolist()))
+    (ref, ref_lse), (okq, oks, ovq, ovs, used) = _oracle_int8(p, rows_np, pick)
+    assert np.array_equal(kq.cpu().numpy()[used], okq) and np.array_equal(vq.cpu().numpy()[used], ovq)
+    assert_parity(out[pick], ref, "paged int8 full")
+    assert_lse(lse[pick], ref_lse)

@@ -152,6 +152,15 @@ def test_page_table_expansion_hand_worked():
     assert rows[1].tolist() == want1
 
 
+def test_negative_page_ids_and_overlong_lengths_are_padding():
+    pt = np.array([[3, -1, 1]], dtype=np.int32)
+    rows = oracle.page_table_to_rows(pt, np.array([500]), 200, page=64)
+    assert rows[0, :64].tolist() == list(range(192, 256))
+    assert np.all(rows[0, 64:128] == -1)
+    assert rows[0, 128:192].tolist() == list(range(64, 128))
+    assert np.all(rows[0, 192:] == -1)          # beyond max_pages * page
+
+
 def test_identity_page_table_gives_contiguous_rows():
     pt = np.arange(8, dtype=np.int32)[None]
     rows = oracle.page_table_to_rows(pt, np.array([500]), 512)
