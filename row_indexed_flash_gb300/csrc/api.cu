@@ -94,6 +94,10 @@ struct DecodePlan {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The prefill workspace holds one error word: non-zero after a call whose
+// pipeline waits expired (its output is then invalid).
+constexpr size_t kPrefillWorkspace = 256;
+
 // Chooses how the list is cut into per-CTA chunks.  Cost model in units of
 // rows streamed by one CTA: waves * (chunk + fixed cost) + merge cost, where
 // ragged lists (n_valid_hint given) are costed by their mean length and the
@@ -189,7 +193,7 @@ const char* fa_version(void) { return "fa_rows 0.1 sm_103a"; }
 size_t fa_rows_workspace_size(const fa_rows_args* a, int is_prefill) {
   g_err[0] = 0;
   if (check_common(a) != FA_OK) return 0;
-  if (is_prefill) return 0;
+  if (is_prefill) return kPrefillWorkspace;
   DecodePlan pl;
   if (plan_decode(a, &pl) != FA_OK) return 0;
   return pl.ws;
@@ -256,13 +260,18 @@ fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_st
 }
 
 fa_status fa_rows_prefill(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   g_err[0] = 0;
   fa_status st = check_common(a);
   if (st != FA_OK) return st;
   if (!far::prefill_supported(a->D, kv_kind(a->kv_dtype)))
     return fail(FA_ERR_UNSUPPORTED, "prefill is built for D=128 with a bf16 or f16 pool");
+  if (a->mask_kind == FA_MASK_DENSE) return fail(FA_ERR_UNSUPPORTED, "prefill takes FA_MASK_NONE or FA_MASK_CAUSAL");
+  if (a->Hq / a->Hkv > 128) return fail(FA_ERR_UNSUPPORTED, "prefill packs at most 128 query heads per KV head");
+  if (!aligned(a->q, 16)) return fail(FA_ERR_INVALID_ARG, "prefill needs 16-byte aligned q");
+  if ((a->out_dtype == FA_F32 && !aligned(a->out, 16)) || !aligned(a->out, 8))
+    return fail(FA_ERR_INVALID_ARG, "prefill needs a 16-byte aligned out");
+  if (ws && (ws_bytes < kPrefillWorkspace || !aligned(ws, 16)))
+    return fail(FA_ERR_WORKSPACE, "prefill workspace must be NULL or %zu bytes", kPrefillWorkspace);
   if ((long long)a->S * a->Nq == 0) return FA_OK;
   far::PrefillParams p;
   memset(&p, 0, sizeof(p));
@@ -285,6 +294,7 @@ fa_status fa_rows_prefill(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_s
   p.mask_kind = a->mask_kind;
   p.is_bf16 = a->q_dtype == FA_BF16;
   p.qscale = a->scale * far::kLog2e;
+  p.err = static_cast<unsigned int*>(ws);
   cudaError_t e = far::prefill_launch(p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "prefill launch");
 }

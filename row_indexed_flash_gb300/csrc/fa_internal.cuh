@@ -78,7 +78,8 @@ struct PrefillParams {
   int out_dtype;
   int mask_kind;
   int is_bf16;
-  float qscale;  // scale * log2(e)
+  float qscale;         // scale * log2(e)
+  unsigned int* err;    // set non-zero if a pipeline wait expired (may be NULL)
 };
 cudaError_t prefill_launch(const PrefillParams& p, cudaStream_t st);
 bool prefill_supported(int D, int kind);

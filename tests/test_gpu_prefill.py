@@ -1,0 +1,98 @@
+"""Prefill parity: the tcgen05 kernel through the C ABI against the fp64
+oracle.  Contiguous runs exercise the TMA path, shuffled pools and padding the
+cp.async gather path; the full-size chunk is checked on sampled query rows."""
+import numpy as np
+import pytest
+import torch
+
+import row_indexed_flash_gb300 as far
+import synth
+from helpers import assert_lse, assert_parity, dev_bits, oracle_for
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(p, out_dtype=torch.float32):
+    q, k, v = dev_bits(p.q, p.dtype), dev_bits(p.k, p.dtype), dev_bits(p.v, p.dtype)
+    rows = torch.from_numpy(p.kv_rows).cuda()
+    extra = {}
+    if p.kv_len is not None:
+        extra["kv_len"] = torch.from_numpy(p.kv_len).cuda()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    out, lse = far.fa_rows_prefill(q, k, v, rows, p.scale, causal=p.causal, out_dtype=out_dtype, want_lse=True,
+                                   workspace=ws, **extra)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0, "prefill pipeline wait expired"
+    return out, lse
+
+
+CASES = {
+    "runs_tma_causal": lambda: synth.prefill_bf16(seed=11, n_seq=2, seq_rows=1500, pool_rows=4096, n_query=300,
+                                                  run=256, Hq=8, Hkv=2),
+    "runs_tma_g1": lambda: synth.prefill_bf16(seed=12, n_seq=2, seq_rows=700, pool_rows=2048, n_query=130,
+                                              run=128, Hq=4, Hkv=4),
+    "runs_tma_g8": lambda: synth.prefill_bf16(seed=13, n_seq=1, seq_rows=1200, pool_rows=2048, n_query=200,
+                                              run=384, Hq=16, Hkv=2),
+    "shuffled_gather": lambda: synth.prefill_bf16(seed=14, n_seq=3, seq_rows=900, pool_rows=3000, n_query=150,
+                                                  Hq=8, Hkv=2, shuffled=True),
+    "random_padding": lambda: synth.random_problem(15, S=2, Nq=100, Hq=8, Hkv=2, D=128, R=2000, L=700,
+                                                   causal=True, pad_frac=0.15),
+    "noncausal_kvlen": lambda: synth.random_problem(16, S=3, Nq=70, Hq=8, Hkv=2, D=128, R=2000, L=900,
+                                                    kv_len=True, pad_frac=0.05),
+    "f16": lambda: synth.random_problem(17, S=2, Nq=64, Hq=4, Hkv=1, D=128, R=1000, L=513, dtype="f16",
+                                        causal=True, pad_frac=0.0),
+    "one_query": lambda: synth.random_problem(18, S=2, Nq=1, Hq=8, Hkv=2, D=128, R=600, L=300, causal=True),
+    "g16_partial_tiles": lambda: synth.random_problem(19, S=1, Nq=45, Hq=32, Hkv=2, D=128, R=1000, L=400,
+                                                      causal=True),
+    "g6_nonpow2": lambda: synth.random_problem(20, S=2, Nq=50, Hq=12, Hkv=2, D=128, R=1000, L=333, causal=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_prefill_matches_oracle(name):
+    p = CASES[name]()
+    out, lse = run_prefill(p)
+    ref, ref_lse = oracle_for(p)
+    assert_parity(out, ref, name)
+    assert_lse(lse, ref_lse, name)
+
+
+@pytest.mark.parametrize("odt", [torch.bfloat16, torch.float16])
+def test_prefill_low_precision_outputs(odt):
+    p = CASES["runs_tma_causal"]()
+    out, _ = run_prefill(p, out_dtype=odt)
+    ref, _ = oracle_for(p)
+    assert_parity(out, ref, str(odt), out_dtype=odt)
+
+
+def test_prefill_empty_slice_and_poisoned_unlisted_rows():
+    p = synth.prefill_bf16(seed=21, n_seq=2, seq_rows=600, pool_rows=2048, n_query=100, run=128, Hq=8, Hkv=2)
+    used = np.zeros(p.R, bool)
+    used[p.kv_rows[p.kv_rows >= 0]] = True
+    p.k[~used] = 0x7FC0
+    p.v[~used] = 0x7FC0
+    out, lse = run_prefill(p)
+    ref, ref_lse = oracle_for(p)
+    assert_parity(out, ref, "poisoned")
+    p.kv_rows[1] = -1
+    out, lse = run_prefill(p)
+    assert torch.all(out[1] == 0) and torch.all(torch.isinf(lse[1]))
+
+
+def test_prefill_agrees_with_decode_on_small_query_counts():
+    p = synth.random_problem(22, S=3, Nq=2, Hq=8, Hkv=2, D=128, R=3000, L=2500, causal=True)
+    a, _ = run_prefill(p)
+    q, k, v = dev_bits(p.q, "bf16"), dev_bits(p.k, "bf16"), dev_bits(p.v, "bf16")
+    b, _ = far.fa_rows_decode(q, k, v, torch.from_numpy(p.kv_rows).cuda(), p.scale, causal=True)
+    assert_parity(a, b.double().cpu().numpy(), "prefill vs decode")
+
+
+@pytest.mark.slow
+def test_workload_prefill_full_size_sampled_rows():
+    p = synth.prefill_bf16()
+    out, lse = run_prefill(p)
+    rows = [0, 1, 31, 32, 1000, 2046, 2047]
+    for sl in ([0], [3]):
+        ref, ref_lse = oracle_for(p, query_rows=rows, slices=sl)
+        assert_parity(out[sl][:, rows], ref, f"prefill full slice {sl}")
+        assert_lse(lse[sl][:, rows], ref_lse, f"prefill full slice {sl}")
