@@ -28,9 +28,19 @@ namespace far {
 
 template <int D, int QVP, int KIND>
 struct DecodeShape {
-  static constexpr int RT = 32 / QVP;                      // rows per warp tile
-  static constexpr int E = D / 32;                         // dimensions per lane
   static constexpr int ES = (KIND == KV_I8) ? 1 : 2;       // bytes per element
+  // dimensions per lane of one row: at least D/32, and 16 (or 64/QVP) so that
+  // a row spans few lanes and the cross-lane reduction stays short
+  static constexpr int EPL_A = D / 32;
+  static constexpr int EPL_B = (64 / QVP) > 16 ? 16 : (64 / QVP);
+  static constexpr int EPL = EPL_A > EPL_B ? EPL_A : EPL_B;
+  static constexpr int LG = D / EPL;                       // lanes per row
+  static constexpr int NG = 32 / LG;                       // rows per warp step
+  static constexpr int RT = 8;                             // rows per warp tile
+  static constexpr int STEPS = RT / NG;
+  static constexpr int LB = EPL * ES;                      // bytes of one row held by a lane
+  static constexpr int CH = LB >= 16 ? LB / 16 : 1;        // 16-byte pieces per lane and row
+  static constexpr int PB = LB >= 16 ? 16 : LB;            // bytes per piece
   static constexpr int KB = D * ES;                        // bytes of one (row, head)
   static constexpr int CPR = KB / 16;                      // 16-byte chunks per (row, head)
   static constexpr int TILE_CH = RT * CPR;                 // chunks per tile for K (and for V)
@@ -43,72 +53,112 @@ struct DecodeShape {
   static constexpr int RING = NW * NSTAGE * SLOT;
   static constexpr int MERGE = NW * QVP * (D + 2) * 4;
   static constexpr int BODY = RING > MERGE ? RING : MERGE;
-  static constexpr int PBUF = NW * 64 * 4;
+  static constexpr int PBUF = NW * (RT * QVP + QVP) * 4;   // per warp: p[RT][QVP], alpha[QVP]
   static constexpr int SMEM = IDX_BYTES + BODY + PBUF + 2 * QVP * 4;
+  static_assert(LG >= 1 && LG <= 32 && NG * LG == 32 && STEPS * NG == RT, "bad decode shape");
+  static_assert(QVP <= LG, "query vectors must fit in one row group");
 };
 
-// Loads this lane's E consecutive elements of one (row, head) from shared
-// memory and widens them to fp32 (INT8: the raw code, scaled later).
-template <int E, int KIND>
-__device__ __forceinline__ void load_lane(const unsigned char* p, float (&x)[E]) {
-  if constexpr (KIND == KV_I8) {
-    if constexpr (E == 2) {
-      uint32_t w = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) ^ 0x8080u;
-      x[0] = i8_to_f(w, 0);
-      x[1] = i8_to_f(w, 1);
+// Element e (0..EPL-1) of a lane with in-row index k covers dimension:
+template <int D, int QVP, int KIND>
+__device__ __forceinline__ int lane_dim(int k, int e) {
+  using Sh = DecodeShape<D, QVP, KIND>;
+  constexpr int PE = Sh::PB / Sh::ES;  // elements per piece
+  if constexpr (Sh::LB >= 16) {
+    return (k + Sh::LG * (e / PE)) * PE + (e % PE);
+  } else {
+    return k * Sh::EPL + e;
+  }
+}
+
+// Loads this lane's EPL elements of one (row, head) from shared memory as
+// fp32 pairs (INT8: the raw codes, scaled later).  Pieces are interleaved
+// across the lanes of a row so that each quarter warp reads contiguous bytes.
+template <int D, int QVP, int KIND>
+__device__ __forceinline__ void load_row(const unsigned char* row, int k,
+                                         float2 (&x)[DecodeShape<D, QVP, KIND>::EPL / 2]) {
+  using Sh = DecodeShape<D, QVP, KIND>;
+  constexpr int PE = Sh::PB / Sh::ES;
+#pragma unroll
+  for (int u = 0; u < Sh::CH; ++u) {
+    const unsigned char* src = row + (Sh::LB >= 16 ? (k + Sh::LG * u) * 16 : k * Sh::LB);
+    uint32_t w[4];
+    if constexpr (Sh::PB == 16) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src);
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (Sh::PB == 8) {
+      const uint2 v = *reinterpret_cast<const uint2*>(src);
+      w[0] = v.x; w[1] = v.y;
+    } else if constexpr (Sh::PB == 4) {
+      w[0] = *reinterpret_cast<const uint32_t*>(src);
+    } else {
+      w[0] = *reinterpret_cast<const uint16_t*>(src);
+    }
+    if constexpr (KIND == KV_I8) {
+#pragma unroll
+      for (int c = 0; c < (PE + 3) / 4; ++c) {
+        const uint32_t xw = w[c] ^ 0x80808080u;
+        const float2 bias = make_float2(8388736.0f, 8388736.0f);
+        if (4 * c + 1 < PE)
+          x[(u * PE + 4 * c) / 2] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7650u)),
+                                                           __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7651u))),
+                                               make_float2(-bias.x, -bias.y));
+        if (4 * c + 3 < PE)
+          x[(u * PE + 4 * c) / 2 + 1] =
+              __fadd2_rn(make_float2(__uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7652u)),
+                                     __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7653u))),
+                         make_float2(-bias.x, -bias.y));
+      }
     } else {
 #pragma unroll
-      for (int c = 0; c < E / 4; ++c) {
-        uint32_t w = reinterpret_cast<const uint32_t*>(p)[c] ^ 0x80808080u;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) x[4 * c + b] = i8_to_f(w, b);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < E / 2; ++c) {
-      uint32_t w = reinterpret_cast<const uint32_t*>(p)[c];
-      if constexpr (KIND == KV_BF16) {
-        x[2 * c] = bf16_lo(w);
-        x[2 * c + 1] = bf16_hi(w);
-      } else {
-        float2 f = f16x2_to_f2(w);
-        x[2 * c] = f.x;
-        x[2 * c + 1] = f.y;
+      for (int c = 0; c < PE / 2; ++c) {
+        if constexpr (KIND == KV_BF16) {
+          x[(u * PE) / 2 + c] = make_float2(bf16_lo(w[c]), bf16_hi(w[c]));
+        } else {
+          x[(u * PE) / 2 + c] = f16x2_to_f2(w[c]);
+        }
       }
     }
   }
 }
 
-// Sum of 32 per-lane values across the warp, transposed: on return lane l
-// holds the warp-wide sum of value index l.
-__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+// Sum across the LG lanes of a row group of QVP per-lane values, transposed:
+// afterwards lane k of the group holds the group sum of value k / (LG / QVP).
+template <int QVP, int LG>
+__device__ __forceinline__ float group_reduce(float (&v)[QVP], int lane) {
+  int w = LG / 2;
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
+  for (int n = QVP; n > 1; n >>= 1, w >>= 1) {
     const bool up = (lane & w) != 0;
 #pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float send = up ? v[i] : v[i + w];
-      const float keep = up ? v[i + w] : v[i];
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? v[i] : v[i + n / 2];
+      const float keep = up ? v[i + n / 2] : v[i];
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
     }
   }
+#pragma unroll
+  for (; w >= 1; w >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], w);
   return v[0];
 }
 
 template <int D, int QVP, int KIND>
 __global__ void __launch_bounds__(kDecodeWarps * 32) fa_rows_decode_kernel(const DecodeParams p) {
   using Sh = DecodeShape<D, QVP, KIND>;
-  constexpr int RT = Sh::RT, E = Sh::E, KB = Sh::KB, CPR = Sh::CPR, NW = Sh::NW, NSTAGE = Sh::NSTAGE;
+  constexpr int RT = Sh::RT, EPL = Sh::EPL, LG = Sh::LG, NG = Sh::NG, STEPS = Sh::STEPS;
+  constexpr int KB = Sh::KB, CPR = Sh::CPR, NW = Sh::NW, NSTAGE = Sh::NSTAGE;
+  constexpr int QSTRIDE = LG / QVP;   // lanes of a group holding the same query vector
   const float NEG_INF = __int_as_float(0xff800000);
 
   extern __shared__ __align__(128) unsigned char smem[];
   int32_t* idx_s = reinterpret_cast<int32_t*>(smem);
   unsigned char* body = smem + Sh::IDX_BYTES;
-  float* pbuf = reinterpret_cast<float*>(body + Sh::BODY);   // [NW][32] p, [NW][32] alpha
-  float* fin = pbuf + NW * 64;                                // [QVP] merged max, [QVP] merged sum
+  float* pbuf_all = reinterpret_cast<float*>(body + Sh::BODY);
+  float* fin = pbuf_all + NW * (RT * QVP + QVP);              // [QVP] merged max, [QVP] merged sum
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = lane / LG, k = lane % LG;
+  const int my_qv = k / QSTRIDE;
   const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int G = p.G;
   int n_s = p.L;
@@ -123,39 +173,42 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) fa_rows_decode_kernel(const
     idx_s[t] = (r >= 0 && (long long)r < p.R) ? r : -1;
   }
 
-  // ---- this lane's slice of every query vector, pre-scaled by scale*log2(e)
-  float qr[QVP][E];
+  // ---- this lane's dimensions of every query vector, pre-scaled by scale*log2(e)
+  float2 qr[QVP][EPL / 2];
 #pragma unroll
   for (int qv = 0; qv < QVP; ++qv) {
-    if (qv < p.QV && cnt > 0) {
-      const int i = qv / G, h = g * G + qv % G;
-      const size_t base = (((size_t)s * p.Nq + i) * p.Hq + h) * D + lane * E;
-      const uint16_t* qp = static_cast<const uint16_t*>(p.q) + base;
+    const bool live = qv < p.QV && cnt > 0;
+    const int i = qv / G, h = g * G + qv % G;
+    const uint16_t* qp = static_cast<const uint16_t*>(p.q) + (((size_t)s * p.Nq + i) * p.Hq + h) * D;
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const uint32_t b = qp[e];
-        const float f = p.q_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
-        qr[qv][e] = f * p.qscale;
+    for (int e2 = 0; e2 < EPL / 2; ++e2) {
+      float f[2] = {0.f, 0.f};
+      if (live) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t b = qp[lane_dim<D, QVP, KIND>(k, 2 * e2 + t)];
+          f[t] = (p.q_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b))) * p.qscale;
+        }
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) qr[qv][e] = 0.f;
+      qr[qv][e2] = make_float2(f[0], f[1]);
     }
   }
   __syncthreads();
 
-  float m = NEG_INF, l = 0.f;
-  float o[QVP][E];
+  float m_used = NEG_INF, l_part = 0.f;   // per query vector my_qv; l over this lane's rows
+  float2 o[QVP][EPL / 2];
 #pragma unroll
   for (int qv = 0; qv < QVP; ++qv)
 #pragma unroll
-    for (int e = 0; e < E; ++e) o[qv][e] = 0.f;
+    for (int e2 = 0; e2 < EPL / 2; ++e2) o[qv][e2] = make_float2(0.f, 0.f);
 
   const int ntiles = (cnt + RT - 1) / RT;
   const int nk = ntiles > warp ? (ntiles - warp + NW - 1) / NW : 0;
   unsigned char* wring = body + warp * NSTAGE * Sh::SLOT;
+  float* pbuf = pbuf_all + warp * (RT * QVP + QVP);
   const char* kbase = static_cast<const char*>(p.k);
   const char* vbase = static_cast<const char*>(p.v);
+  const int qi = my_qv / G;
 
   auto issue = [&](int kk) {
     if (kk < nk) {
@@ -196,94 +249,133 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) fa_rows_decode_kernel(const
     const unsigned char* slot = wring + (kk % NSTAGE) * Sh::SLOT;
     const int t = warp + kk * NW;
 
-    // QK^T partial sums: value index r*QVP + qv
-    float part[32];
+    // ---- logits of this lane's rows (one per step) for query vector my_qv
+    float lg[STEPS];
+    float vsc[STEPS];
 #pragma unroll
-    for (int r = 0; r < RT; ++r) {
-      float kf[E];
-      load_lane<E, KIND>(slot + r * KB + lane * E * Sh::ES, kf);
+    for (int st = 0; st < STEPS; ++st) {
+      const int r = st * NG + grp;
+      float2 kf[EPL / 2];
+      load_row<D, QVP, KIND>(slot + r * KB, k, kf);
+      float part[QVP];
 #pragma unroll
       for (int qv = 0; qv < QVP; ++qv) {
-        float acc = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(qr[qv][e], kf[e], acc);
-        part[r * QVP + qv] = acc;
+        for (int e2 = 0; e2 < EPL / 2; ++e2) acc = __ffma2_rn(qr[qv][e2], kf[e2], acc);
+        part[qv] = acc.x + acc.y;
+      }
+      float x = group_reduce<QVP, LG>(part, lane);
+      const int pos = t * RT + r;
+      const int row = pos < cnt ? idx_s[pos] : -1;
+      bool ok = row >= 0 && my_qv < p.QV;
+      vsc[st] = 1.f;
+      if constexpr (KIND == KV_I8) {
+        const uint32_t kw = reinterpret_cast<const uint32_t*>(slot + 2 * RT * KB)[r];
+        const uint32_t vw = reinterpret_cast<const uint32_t*>(slot + 2 * RT * KB)[RT + r];
+        const int hi = row & 1;
+        x *= __half2float(__ushort_as_half((unsigned short)(hi ? (kw >> 16) : (kw & 0xffffu))));
+        vsc[st] = __half2float(__ushort_as_half((unsigned short)(hi ? (vw >> 16) : (vw & 0xffffu))));
+      }
+      const int jpos = j0 + pos;
+      if (p.mask_kind == FA_MASK_CAUSAL) ok = ok && (jpos <= n_s - p.Nq + qi);
+      if (ok && p.mask_kind == FA_MASK_DENSE) x += __ldg(p.mask + ((size_t)s * p.Nq + qi) * p.L + jpos) * kLog2e;
+      lg[st] = ok ? x : NEG_INF;
+    }
+
+    // ---- online softmax; the reference max only moves when it grows by > 2^8
+    float tmax = lg[0];
+#pragma unroll
+    for (int st = 1; st < STEPS; ++st) tmax = fmaxf(tmax, lg[st]);
+#pragma unroll
+    for (int w = LG; w < 32; w <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, w));
+    const float m_new = fmaxf(m_used, tmax);
+    const bool need = m_new > m_used + 8.f;
+    if (__any_sync(0xffffffffu, need)) {
+      const float alpha = need ? fast_ex2(m_used - m_new) : 1.f;
+      if (need) {
+        l_part *= alpha;
+        m_used = m_new;
+      }
+      if (lane < LG && (lane % QSTRIDE) == 0) pbuf[RT * QVP + my_qv] = alpha;
+      __syncwarp();
+#pragma unroll
+      for (int qv = 0; qv < QVP; ++qv) {
+        const float a = pbuf[RT * QVP + qv];
+        const float2 a2 = make_float2(a, a);
+#pragma unroll
+        for (int e2 = 0; e2 < EPL / 2; ++e2) o[qv][e2] = __fmul2_rn(o[qv][e2], a2);
       }
     }
-    float logit = transpose_reduce32(part, lane);
-    const int my_r = lane / QVP, my_qv = lane % QVP;
-    const int pos = t * RT + my_r;
-    const int row = pos < cnt ? idx_s[pos] : -1;
-    bool ok = row >= 0 && my_qv < p.QV;
-    float vsc = 1.f;
-    if constexpr (KIND == KV_I8) {
-      const uint32_t kw = reinterpret_cast<const uint32_t*>(slot + 2 * RT * KB)[my_r];
-      const uint32_t vw = reinterpret_cast<const uint32_t*>(slot + 2 * RT * KB)[RT + my_r];
-      const int hi = row & 1;
-      logit *= __half2float(__ushort_as_half((unsigned short)(hi ? (kw >> 16) : (kw & 0xffffu))));
-      vsc = __half2float(__ushort_as_half((unsigned short)(hi ? (vw >> 16) : (vw & 0xffffu))));
+    const float mu = (m_used == NEG_INF) ? 0.f : m_used;
+#pragma unroll
+    for (int st = 0; st < STEPS; ++st) {
+      const float pr = fast_ex2(lg[st] - mu);
+      l_part += pr;
+      if ((k % QSTRIDE) == 0) pbuf[(st * NG + grp) * QVP + my_qv] = pr * vsc[st];
     }
-    const int qi = my_qv / G;
-    const int jpos = j0 + pos;
-    if (p.mask_kind == FA_MASK_CAUSAL) ok = ok && (jpos <= n_s - p.Nq + qi);
-    if (ok && p.mask_kind == FA_MASK_DENSE)
-      logit += __ldg(p.mask + ((size_t)s * p.Nq + qi) * p.L + jpos) * kLog2e;
-    if (!ok) logit = NEG_INF;
-
-    // online softmax over the RT lanes holding the same query vector
-    float tmax = logit;
-#pragma unroll
-    for (int w = QVP; w < 32; w <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, w));
-    const float mnew = fmaxf(m, tmax);
-    const float muse = (mnew == NEG_INF) ? 0.f : mnew;
-    const float pr = fast_ex2(logit - muse);
-    const float alpha = fast_ex2(m - muse);
-    float ps = pr;
-#pragma unroll
-    for (int w = QVP; w < 32; w <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, w);
-    l = l * alpha + ps;
-    m = mnew;
-
-    float* wp = pbuf + warp * 64;
-    wp[lane] = pr * vsc;
-    if (lane < QVP) wp[32 + lane] = alpha;
     __syncwarp();
+
+    // ---- PV for this lane's rows
 #pragma unroll
-    for (int qv = 0; qv < QVP; ++qv) {
-      const float a = wp[32 + qv];
+    for (int st = 0; st < STEPS; ++st) {
+      const int r = st * NG + grp;
+      float2 vf[EPL / 2];
+      load_row<D, QVP, KIND>(slot + RT * KB + r * KB, k, vf);
+      float pp[QVP];
+      if constexpr (QVP % 4 == 0) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) o[qv][e] *= a;
-    }
+        for (int q4 = 0; q4 < QVP / 4; ++q4) {
+          const float4 v4 = reinterpret_cast<const float4*>(pbuf + r * QVP)[q4];
+          pp[4 * q4] = v4.x; pp[4 * q4 + 1] = v4.y; pp[4 * q4 + 2] = v4.z; pp[4 * q4 + 3] = v4.w;
+        }
+      } else {
 #pragma unroll
-    for (int r = 0; r < RT; ++r) {
-      float vf[E];
-      load_lane<E, KIND>(slot + RT * KB + r * KB + lane * E * Sh::ES, vf);
+        for (int qv = 0; qv < QVP; ++qv) pp[qv] = pbuf[r * QVP + qv];
+      }
 #pragma unroll
       for (int qv = 0; qv < QVP; ++qv) {
-        const float pp = wp[r * QVP + qv];
+        const float2 p2 = make_float2(pp[qv], pp[qv]);
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[qv][e] = fmaf(pp, vf[e], o[qv][e]);
+        for (int e2 = 0; e2 < EPL / 2; ++e2) o[qv][e2] = __ffma2_rn(p2, vf[e2], o[qv][e2]);
       }
     }
     __syncwarp();
   }
   cp_async_wait<0>();
+
+  // ---- fold the row groups of the warp: O and l over groups (m is shared)
+#pragma unroll
+  for (int w = LG; w < 32; w <<= 1) {
+    l_part += __shfl_xor_sync(0xffffffffu, l_part, w);
+#pragma unroll
+    for (int qv = 0; qv < QVP; ++qv)
+#pragma unroll
+      for (int e2 = 0; e2 < EPL / 2; ++e2) {
+        o[qv][e2].x += __shfl_xor_sync(0xffffffffu, o[qv][e2].x, w);
+        o[qv][e2].y += __shfl_xor_sync(0xffffffffu, o[qv][e2].y, w);
+      }
+  }
   __syncthreads();
 
   // ---- merge the warps of this CTA (the ring is free now)
   float* wo = reinterpret_cast<float*>(body);   // [NW][QVP][D]
   float* wm = wo + NW * QVP * D;                // [NW][QVP]
   float* wl = wm + NW * QVP;                    // [NW][QVP]
+  if (grp == 0) {
 #pragma unroll
-  for (int qv = 0; qv < QVP; ++qv)
+    for (int qv = 0; qv < QVP; ++qv)
 #pragma unroll
-    for (int e = 0; e < E; ++e) wo[(warp * QVP + qv) * D + lane * E + e] = o[qv][e];
-  if (lane < QVP) {
-    wm[warp * QVP + lane] = m;
-    wl[warp * QVP + lane] = l;
+      for (int e2 = 0; e2 < EPL / 2; ++e2) {
+        wo[(warp * QVP + qv) * D + lane_dim<D, QVP, KIND>(k, 2 * e2)] = o[qv][e2].x;
+        wo[(warp * QVP + qv) * D + lane_dim<D, QVP, KIND>(k, 2 * e2 + 1)] = o[qv][e2].y;
+      }
+    if ((k % QSTRIDE) == 0) {
+      wm[warp * QVP + my_qv] = m_used;
+      wl[warp * QVP + my_qv] = l_part;
+    }
   }
   __syncthreads();
-
   const size_t unit = (size_t)s * p.Hkv + g;
   for (int t = threadIdx.x; t < QVP * D; t += NW * 32) {
     const int qv = t / D, d = t % D;

@@ -86,7 +86,29 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* b, uint32_t parity) {
   }
 }
 
-__global__ void __maxnreg__(200)
+// Visibility of column k of KV tile j for this thread's row: a valid entry
+// (bit k of the tile's validity mask) within the causal limit.
+__device__ __forceinline__ bool col_visible(int k, unsigned vb0, unsigned vb1, unsigned vb2, unsigned vb3, int jbase,
+                                            int lim) {
+  const unsigned vb = k < 32 ? vb0 : k < 64 ? vb1 : k < 96 ? vb2 : vb3;
+  return ((vb >> (k & 31)) & 1u) && (jbase + k <= lim);
+}
+
+// 32 columns of this thread's S row starting at column c0, scaled into log2
+// units, masked columns -inf.
+__device__ __forceinline__ void load_s32(float (&x)[32], uint32_t tS, int c0, float c, bool need_mask, unsigned vb0,
+                                         unsigned vb1, unsigned vb2, unsigned vb3, int jbase, int lim) {
+  const float NEG_INF = __int_as_float(0xff800000);
+  uint32_t r[32];
+  tmem_ld32(tS + c0, r);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    x[k] = __uint_as_float(r[k]) * c;
+    if (need_mask && !col_visible(c0 + k, vb0, vb1, vb2, vb3, jbase, lim)) x[k] = NEG_INF;
+  }
+}
+
+__global__ void __launch_bounds__(pf::NWARP * 32, 1)
     fa_rows_prefill_kernel(const PrefillKernelParams kp, const __grid_constant__ CUtensorMap tq,
                            const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
   using namespace pf;
@@ -313,28 +335,15 @@ __global__ void __maxnreg__(200)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + qt, j & 1, abort_flag)))) break;
       tc_fence_after();
       const bool need_mask = !all_valid || j * BN + BN - 1 > lim;
-      // S row of this thread, scaled into log2 units, masked
-      auto load_x = [&](float (&x)[128]) {
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t r[32];
-          tmem_ld32(tS + c4 * 32, r);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) x[c4 * 32 + k] = __uint_as_float(r[k]) * c;
-        }
-        if (need_mask) {
-#pragma unroll
-          for (int k = 0; k < 128; ++k) {
-            const bool vis = ((vbits[k >> 5] >> (k & 31)) & 1u) && (j * BN + k <= lim);
-            if (!vis) x[k] = NEG_INF;
-          }
-        }
-      };
-      float x[128];
-      load_x(x);
+      // pass 1: the row maximum, 32 columns at a time
       float mx = NEG_INF;
 #pragma unroll
-      for (int k = 0; k < 128; ++k) mx = fmaxf(mx, x[k]);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float x[32];
+        load_s32(x, tS, c4 * 32, c, need_mask, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, x[k]);
+      }
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + 8.f;
       if (__any_sync(0xffffffffu, need)) {
@@ -355,19 +364,25 @@ __global__ void __maxnreg__(200)
             tmem_st32(tO + c4 * 32, r);
           }
         }
-        load_x(x);
       }
+      // pass 2: P = exp2(x - m) as 16-bit pairs; half h of P (32 columns)
+      // overwrites S columns 32h..32h+31, which pass 2 has already read
       const float mu = (m_used == NEG_INF) ? 0.f : m_used;
       float sum = 0.f;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float p0 = fast_ex2(x[hh * 64 + 2 * k] - mu);
-          const float p1 = fast_ex2(x[hh * 64 + 2 * k + 1] - mu);
-          sum += p0 + p1;
-          pk[k] = pack2(p0, p1, bf16);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          float x[32];
+          load_s32(x, tS, hh * 64 + c2 * 32, c, need_mask, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float p0 = fast_ex2(x[2 * k] - mu);
+            const float p1 = fast_ex2(x[2 * k + 1] - mu);
+            sum += p0 + p1;
+            pk[c2 * 16 + k] = pack2(p0, p1, bf16);
+          }
         }
         tmem_st32(tS + hh * 32, pk);
       }
