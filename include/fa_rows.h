@@ -121,6 +121,24 @@ fa_status fa_rows_workspace_init(void* ws, size_t ws_bytes, fa_stream_t stream);
 fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_stream_t stream);
 
 /*
+ * Decode for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call; it exists for hosts that may not call cudaMalloc
+ * (or any allocating routine) where they run attention: code inside a custom
+ * device allocator or its callbacks, plugins whose framework owns every device
+ * allocation, and latency-critical paths that cannot afford an allocation or
+ * its failure.  Same arguments and results as fa_rows_decode, but the
+ * split-merge scratch comes from a static device array of 16 MiB inside this
+ * library (held on every GPU that loads it, until the process exits).
+ * Arguments whose scratch would exceed 16 MiB are rejected with
+ * FA_ERR_WORKSPACE before anything is launched.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress), so make that
+ * first call before any stream capture.  Each call zero-fills the part of the
+ * array it uses; all calls share the array, so calls that overlap on the GPU
+ * (other streams or threads) race and must be serialised by the caller.
+ */
+fa_status fa_rows_decode_static(const fa_rows_args* a, fa_stream_t stream);
+
+/*
  * Prefill: many query rows per slice.  QK^T and PV on the tensor cores
  * (tcgen05, accumulators in tensor memory), K/V tiles gathered by row index.
  * D = 128, FA_BF16 or FA_F16 for q and the pool; Nq >= 1.

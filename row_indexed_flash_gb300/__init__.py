@@ -68,6 +68,7 @@ _SIGS = {
     "fa_rows_workspace_init": (ctypes.c_int, [_P, ctypes.c_size_t, _P]),
     "fa_rows_decode": (ctypes.c_int, [ctypes.POINTER(fa_rows_args), _P, ctypes.c_size_t, _P]),
     "fa_rows_prefill": (ctypes.c_int, [ctypes.POINTER(fa_rows_args), _P, ctypes.c_size_t, _P]),
+    "fa_rows_decode_static": (ctypes.c_int, [ctypes.POINTER(fa_rows_args), _P]),
     "fa_rows_validate": (ctypes.c_int, [ctypes.POINTER(fa_rows_args), _P, _P]),
     "fa_kv_page_table_to_rows": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_int32, _P,
                                                 ctypes.c_int32, _P]),

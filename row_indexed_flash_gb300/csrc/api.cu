@@ -172,6 +172,10 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
 
 }  // namespace
 
+namespace far {
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+}  // namespace far
+
 extern "C" {
 
 const char* fa_status_string(fa_status s) {
