@@ -43,12 +43,16 @@ import synth  # noqa: E402
 METRIC = "row-indexed attention: decode gathered-KV GB/s, prefill TFLOP/s (vs GB300 roofline)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
-    "decode": ["row_indexed_flash_gb300/csrc/decode.cuh", "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
-    "prefill": ["row_indexed_flash_gb300/csrc/prefill.cu", "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
+    "decode": ["row_indexed_flash_gb300/csrc/decode_tc.cu", "row_indexed_flash_gb300/csrc/tc.cuh",
+               "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
+    "prefill": ["row_indexed_flash_gb300/csrc/prefill.cu", "row_indexed_flash_gb300/csrc/tc.cuh",
+                "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
 }
+KERNEL_NAMES = {"decode": "fa_rows_decode_tc_kernel<128>", "prefill": "fa_rows_prefill_kernel"}
 PROFILE_FILES = {
     "decode_bf16": "profiles/decode_bf16_4x16384_ncu.txt",
     "prefill_bf16": "profiles/prefill_bf16_4x2048x99936_ncu.txt",
+    "prefill_bf16_small": "profiles/prefill_bf16_4x2048x16384_ncu.txt",
 }
 
 
@@ -213,6 +217,9 @@ def build_problem(workload: str):
         return synth.decode_bf16_large()
     if workload == "prefill_bf16":
         return synth.prefill_bf16()
+    if workload == "prefill_bf16_small":
+        # profiling size: 4 x 16,384-row lists in a 65,536-row pool (268 MB of K/V, above L2)
+        return synth.prefill_bf16(n_seq=4, seq_rows=16384, pool_rows=65536)
     raise SystemExit(f"unknown workload {workload}")
 
 
@@ -363,7 +370,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             "unit": unit,
             "frac": round(achieved / peak, 4),
             "traffic": profiled_traffic(args.workload, kind),
-            "kernel": "fa_rows_prefill_kernel" if is_prefill else "fa_rows_decode_kernel",
+            "kernel": KERNEL_NAMES[kind],
             "kernel_ms": round(mean_launch_ms, 5),
             "work_per_launch": work,
         },
@@ -390,7 +397,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="decode_bf16", choices=["decode_bf16", "prefill_bf16"])
+    ap.add_argument("--workload", default="decode_bf16", choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -87,9 +87,10 @@ fa_status check_common(const fa_rows_args* a) {
 }
 
 struct DecodePlan {
-  int qvp = 0, chunk = 0, nsplit = 0;
-  size_t ws = 0;  // workspace bytes
-  size_t off_ml = 0, off_o = 0;
+  bool tc = false;   // tensor-core kernel
+  int qvp = 0, rows = 0, chunk = 0, nsplit = 0;
+  size_t ws = 0;     // workspace bytes
+  size_t off_err = 0, off_ml = 0, off_o = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -98,23 +99,37 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // pipeline waits expired (its output is then invalid).
 constexpr size_t kPrefillWorkspace = 256;
 
-// Chooses how the list is cut into per-CTA chunks.  Cost model in units of
-// rows streamed by one CTA: waves * (chunk + fixed cost) + merge cost, where
-// ragged lists (n_valid_hint given) are costed by their mean length and the
-// all-padding CTAs they leave add a small per-CTA cost.
+// Chooses the kernel and how the list is cut into per-CTA chunks.  Cost model
+// in units of rows streamed by one CTA: waves * (chunk + fixed cost) + merge
+// cost, where ragged lists (n_valid_hint given) are costed by their mean
+// length and the all-padding CTAs they leave add a small per-CTA cost.
 fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   const int G = a->Hq / a->Hkv;
   const long long qv = (long long)a->Nq * G;
   if (qv > 32) return fail(FA_ERR_UNSUPPORTED, "decode packs Nq*Hq/Hkv <= 32 query vectors per KV head (got %lld)", qv);
   const int qvp = next_pow2((int)(qv < 1 ? 1 : qv));
-  far::DecodeConfig cfg;
-  bool built = false;
   const int kind = kv_kind(a->kv_dtype);
-  if (kind == far::KV_BF16) built = far::decode_config_bf16(a->D, qvp, &cfg);
-  if (kind == far::KV_F16) built = far::decode_config_f16(a->D, qvp, &cfg);
-  if (kind == far::KV_I8) built = far::decode_config_i8(a->D, qvp, &cfg);
-  if (!built) return fail(FA_ERR_UNSUPPORTED, "decode is built for D in {64,128,256} with (Nq*G padded) * D <= 2048; got D=%d, %d query vectors", a->D, qvp);
+  pl->tc = far::decode_tc_supported(a->D, kind, (int)(qv < 1 ? 1 : qv), a->mask_kind) && aligned(a->q, 16) &&
+           a->n_pool_rows * a->Hkv < 0x7fffffffLL;  // gather rows are int32 coordinates r * Hkv + g
   pl->qvp = qvp;
+  pl->rows = pl->tc ? (int)qv : qvp;
+  int align = 0, chunk_max = 0;
+  if (pl->tc) {
+    align = far::decode_tc_tile();
+    chunk_max = 1 << 30;
+  } else {
+    far::DecodeConfig cfg;
+    bool built = false;
+    if (kind == far::KV_BF16) built = far::decode_config_bf16(a->D, qvp, &cfg);
+    if (kind == far::KV_F16) built = far::decode_config_f16(a->D, qvp, &cfg);
+    if (kind == far::KV_I8) built = far::decode_config_i8(a->D, qvp, &cfg);
+    if (!built)
+      return fail(FA_ERR_UNSUPPORTED,
+                  "decode is built for D in {64,128,256} with (Nq*G padded) * D <= 2048; got D=%d, %d query vectors",
+                  a->D, qvp);
+    align = cfg.rt * far::kDecodeWarps;
+    chunk_max = far::kDecodeChunkMax;
+  }
   const int L = a->list_len;
   if ((long long)a->S * a->Nq == 0 || L == 0) {
     pl->chunk = 0;
@@ -122,23 +137,24 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
     return FA_OK;
   }
   int occ = 0;
-  if (kind == far::KV_BF16) occ = far::decode_occupancy_bf16(a->D, qvp);
-  if (kind == far::KV_F16) occ = far::decode_occupancy_f16(a->D, qvp);
-  if (kind == far::KV_I8) occ = far::decode_occupancy_i8(a->D, qvp);
+  if (pl->tc) occ = far::decode_tc_occupancy(a->D);
+  else if (kind == far::KV_BF16) occ = far::decode_occupancy_bf16(a->D, qvp);
+  else if (kind == far::KV_F16) occ = far::decode_occupancy_f16(a->D, qvp);
+  else if (kind == far::KV_I8) occ = far::decode_occupancy_i8(a->D, qvp);
   if (occ <= 0) return fail(FA_ERR_CUDA, "decode kernel cannot be resident (no device, or shared memory too small)");
   const long long slots = (long long)sm_count() * occ;
   const long long units = (long long)a->S * a->Hkv;
-  const int align = cfg.rt * far::kDecodeWarps;
   const bool ragged = a->n_valid_hint > 0;
   const double lavg = ragged ? (double)a->n_valid_hint / a->S : (double)L;
-  const double c_cta = 64.0, c_split = 2.0, c_empty = 16.0;
-  const int ns_lo = (L + far::kDecodeChunkMax - 1) / far::kDecodeChunkMax;
+  // fixed cost of a CTA (start-up, pipeline fill, merge), in streamed rows
+  const double c_cta = pl->tc ? 256.0 : 64.0, c_split = 2.0, c_empty = 16.0;
+  const int ns_lo = (int)((L + chunk_max - 1) / chunk_max);
   const int ns_hi = (L + align - 1) / align;
   double best = 1e300;
   int best_ns = ns_lo;
   for (int ns = ns_lo; ns <= ns_hi && ns <= 4096; ++ns) {
     const long long chunk = round_up((L + ns - 1) / ns, align);
-    if (chunk > far::kDecodeChunkMax) continue;
+    if (chunk > chunk_max) continue;
     const long long ns_eff = (L + chunk - 1) / chunk;
     double cost;
     if (!ragged) {
@@ -148,8 +164,7 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
       const double per_unit = ceil(lavg / (double)chunk);
       const long long busy = (long long)(units * per_unit);
       const long long waves = (busy + slots - 1) / slots;
-      cost = waves * (chunk + c_cta) + c_empty * (double)(units * ns_eff - busy) / slots +
-             c_split * per_unit;
+      cost = waves * (chunk + c_cta) + c_empty * (double)(units * ns_eff - busy) / slots + c_split * per_unit;
     }
     if (cost < best - 1e-9) {
       best = cost;
@@ -158,14 +173,18 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   }
   pl->chunk = (int)round_up((L + best_ns - 1) / best_ns, align);
   pl->nsplit = (L + pl->chunk - 1) / pl->chunk;
+  const size_t nunit = (size_t)units;
+  const size_t cnt_bytes = round_up(nunit * sizeof(unsigned int), 256);
+  pl->off_err = cnt_bytes;
+  const size_t err_bytes = pl->tc ? 256 : 0;
   if (pl->nsplit > 1) {
-    const size_t nunit = (size_t)units;
-    const size_t cnt_bytes = round_up(nunit * sizeof(unsigned int), 256);
-    const size_t ml_bytes = round_up(nunit * pl->nsplit * qvp * 2 * sizeof(float), 256);
-    const size_t o_bytes = nunit * pl->nsplit * qvp * (size_t)a->D * sizeof(float);
-    pl->off_ml = cnt_bytes;
-    pl->off_o = cnt_bytes + ml_bytes;
-    pl->ws = cnt_bytes + ml_bytes + o_bytes;
+    const size_t ml_bytes = round_up(nunit * pl->nsplit * pl->rows * 2 * sizeof(float), 256);
+    const size_t o_bytes = nunit * pl->nsplit * pl->rows * (size_t)a->D * sizeof(float);
+    pl->off_ml = cnt_bytes + err_bytes;
+    pl->off_o = pl->off_ml + ml_bytes;
+    pl->ws = pl->off_o + o_bytes;
+  } else if (pl->tc) {
+    pl->ws = cnt_bytes + err_bytes;
   }
   return FA_OK;
 }
@@ -257,9 +276,16 @@ fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_st
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;
   const int kind = kv_kind(a->kv_dtype);
-  if (kind == far::KV_BF16) e = far::decode_launch_bf16(p, a->D, pl.qvp, s);
-  if (kind == far::KV_F16) e = far::decode_launch_f16(p, a->D, pl.qvp, s);
-  if (kind == far::KV_I8) e = far::decode_launch_i8(p, a->D, pl.qvp, s);
+  if (pl.tc) {
+    unsigned int* err = pl.ws > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + pl.off_err) : nullptr;
+    e = far::decode_tc_launch(p, a->D, err, s);
+  } else if (kind == far::KV_BF16) {
+    e = far::decode_launch_bf16(p, a->D, pl.qvp, s);
+  } else if (kind == far::KV_F16) {
+    e = far::decode_launch_f16(p, a->D, pl.qvp, s);
+  } else if (kind == far::KV_I8) {
+    e = far::decode_launch_i8(p, a->D, pl.qvp, s);
+  }
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "decode launch");
 }
 

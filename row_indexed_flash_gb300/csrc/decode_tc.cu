@@ -1,0 +1,614 @@
+// Split-KV decode over row-indexed lists on the 5th-generation tensor cores.
+//
+// The operation ("llama.cpp 0.9.0 inference boundaries", section 1): each
+// query slice attends exactly to the pool rows its kv_rows list names;
+// negative entries are padding (mask -inf).
+//
+// Decode is bound by the HBM bytes of the gathered K/V rows.  On GB300 the
+// CUDA cores cannot form the dot products at that rate without becoming the
+// bottleneck (a widening conversion and a fused multiply-add per element for
+// every query vector), while the tensor pipe is idle.  So the Nq*G query
+// vectors that share a KV head (at most 32) are placed in the rows of a
+// 128-row MMA tile; the other rows carry whatever lies in shared memory after
+// the query rows and only ever produce rows of S, P and O that are never read
+// (an MMA row depends on its own A row only).
+//
+// One CTA handles one (slice, KV head, split) item, 64 list entries per tile:
+//   producers      4 warps: cp.async gathers of the listed rows into the
+//                  128-byte-swizzled layout (padding rows zero-filled), or one
+//                  TMA tile load per 64-column atom when the 64 listed rows are
+//                  one contiguous pool run; 3 stages.
+//   MMA warp       S_b = Q K^T (M=128, N=64, both operands in shared memory),
+//                  then O += P_b V (P from tensor memory, V MN-major), S
+//                  double-buffered so the next QK overlaps the softmax.
+//   softmax warp   one lane per query vector: masks, keeps a reference max that
+//                  only moves when it grows by more than 2^8 (then rescales O in
+//                  place), writes P over S as 16-bit pairs, and at the end
+//                  writes the split's (max, sum, O) or the final output.
+// The last CTA to finish a (slice, KV head) merges the splits (an arrival
+// counter in the workspace, reset by that CTA; nothing waits on it).
+// Every pipeline wait is bounded in time and reported through an error word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "tc.cuh"
+
+namespace far {
+
+namespace dk {
+constexpr int BN = 64;       // list entries per tile
+constexpr int QROWS = 32;    // query-vector rows kept in shared memory
+constexpr int NST = 3;       // K/V stages
+constexpr int NPROD = 4;     // producer warps (each gathers BN / NPROD rows of every tile)
+constexpr int NWARP = 2 + NPROD;   // softmax, producers, MMA
+constexpr int MMA_WARP = 1 + NPROD;
+}  // namespace dk
+
+template <int D>
+struct DkShape {
+  static constexpr int KT = D / 64;                  // 128-byte K atoms per row
+  static constexpr int QATOM = dk::QROWS * 128;      // bytes of one atom column of the Q tile
+  static constexpr int Q_BYTES = KT * QATOM;
+  static constexpr int KV_ATOM = dk::BN * 128;       // bytes of one atom column of a K or V tile
+  static constexpr int TILE = KT * KV_ATOM;          // one K (or V) tile
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = ((Q_BYTES + 1023) / 1024) * 1024;
+  static constexpr int OFF_V = OFF_K + dk::NST * TILE;
+  static constexpr int OFF_BAR = OFF_V + dk::NST * TILE;
+  // q_full, kv_full[NST], kv_empty[NST], s_full[2], p_full[2], o_ready, drain
+  static constexpr int NBAR = 1 + 2 * dk::NST + 2 + 2 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_IDX = OFF_MISC + 16;
+  static constexpr int OFF_FIN = OFF_IDX + dk::BN * 4;
+  static constexpr int SMEM_USED = OFF_FIN + 2 * dk::QROWS * 4;
+  static constexpr int SMEM = SMEM_USED + 1024;
+  static constexpr uint32_t TMEM_COLS = (2 * dk::BN + D) <= 256 ? 256 : 512;
+  static constexpr uint32_t COL_S = 0;               // S0, S1: 64 columns each
+  static constexpr uint32_t COL_O = 2 * dk::BN;      // O: D columns
+};
+
+struct DecodeTcParams {
+  DecodeParams a;   // QV query vectors per KV head; partials laid out [unit][split][QV][D]
+  unsigned int* err;
+  int tma_kv;
+};
+
+namespace {
+
+__device__ __forceinline__ uint32_t pack2h(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void wait_drain(uint64_t* b, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(b, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(dk::NWARP * 32, 1)
+    fa_rows_decode_tc_kernel(const DecodeTcParams kp, const __grid_constant__ CUtensorMap tk,
+                             const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap gk,
+                             const __grid_constant__ CUtensorMap gv) {
+  using Sh = DkShape<D>;
+  using namespace dk;
+  const DecodeParams& p = kp.a;
+  const float NEG_INF = __int_as_float(0xff800000);
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + NST;
+  uint64_t* s_full = kv_empty + NST;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_ready = p_full + 2;
+  uint64_t* drain = o_ready + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Sh::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::OFF_MISC + 4);
+  int* am_last = reinterpret_cast<int*>(sm + Sh::OFF_MISC + 8);
+  float* fin = reinterpret_cast<float*>(sm + Sh::OFF_FIN);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int G = p.G, QV = p.QV;
+  const bool bf16 = p.q_bf16 != 0;
+  int n_s = p.L;
+  if (p.kv_len) n_s = min(max(__ldg(p.kv_len + s), 0), p.L);
+  const int j0 = split * p.chunk;
+  const int cnt = max(min(j0 + p.chunk, n_s) - j0, 0);
+  const int T = (cnt + BN - 1) / BN;
+  const int32_t* rows_g = p.kv_rows + (size_t)s * p.L + j0;
+  const size_t unit = (size_t)s * p.Hkv + g;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(kv_full + i, NPROD);   // one arrival per producer warp (warp 0's may carry TMA bytes)
+      mbar_init(kv_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(p_full + i, 1);
+    }
+    mbar_init(o_ready, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_holder, Sh::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp >= 1 && warp <= NPROD) {
+    // ------------------------------------------------------------ producers
+    // Gathered rows are fetched with cp.async by NPROD warps (the load/store
+    // path sustains far more independent row requests than one warp or the
+    // TMA gather unit); each warp publishes its part of a tile NST - 1 tiles
+    // after issuing it, once its copies have landed.  A tile whose 64 listed
+    // rows form one contiguous pool run is loaded by TMA tile loads instead.
+    const int pw = warp - 1;
+    constexpr int CPR = D / 8;                  // 16-byte chunks per (row, head)
+    constexpr int ROWS = BN / NPROD;            // rows per producer warp
+    const char* kb = static_cast<const char*>(p.k);
+    const char* vb = static_cast<const char*>(p.v);
+    if (pw == 0 && T > 0) {
+      // query vectors -> rows 0..QV-1 of the swizzled Q tile
+      const uint16_t* qg = static_cast<const uint16_t*>(p.q);
+      for (int f = lane; f < QV * CPR; f += 32) {
+        const int r = f / CPR, c = f % CPR;
+        const int i = r / G, h = g * G + r % G;
+        const char* src = reinterpret_cast<const char*>(qg + (((size_t)s * p.Nq + i) * p.Hq + h) * D) + c * 16;
+        cp_async16(sm + Sh::OFF_Q + (c >> 3) * Sh::QATOM + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, true);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+    }
+    static_assert(NST == 3, "the producers track three stages in scalars");
+    unsigned gathered = 0;   // bit t % 32: this warp gathered its rows of tile t (arrival due at publish)
+    unsigned tma_pend = 0;   // bit st: a TMA load into stage st may still be in flight (warp 0)
+    int use0 = 0, use1 = 0, use2 = 0;
+    int nrow0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // next tile's rows, one tile ahead
+    int nrow1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
+    int published = 0;
+    auto publish = [&](int t) {
+      if ((gathered >> (t & 31)) & 1u) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kv_full + t % NST);
+      }
+    };
+    for (int j = 0; j < T; ++j) {
+      const int st = j % NST, u = j / NST;
+      // publish tile j - (NST - 1) before waiting for stage st: the MMA needs
+      // it before it can free that stage
+      if (j >= NST - 1) {
+        cp_async_wait<NST - 2>();
+        publish(j - (NST - 1));
+        published = j - (NST - 1) + 1;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
+      int rows[2] = {nrow0, nrow1};
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (rows[t] < 0 || (long long)rows[t] >= p.R) rows[t] = -1;
+      {
+        const int pos = (j + 1) * BN + lane;
+        nrow0 = pos < cnt ? __ldg(rows_g + pos) : -1;
+        nrow1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
+      }
+      const int r0 = __shfl_sync(0xffffffffu, rows[0], 0);
+      bool contig = rows[0] >= 0 && rows[0] == r0 + lane && rows[1] >= 0 && rows[1] == r0 + lane + 32;
+      contig = __all_sync(0xffffffffu, contig) && kp.tma_kv;
+      unsigned char* Ks = sm + Sh::OFF_K + st * Sh::TILE;
+      unsigned char* Vs = sm + Sh::OFF_V + st * Sh::TILE;
+      if (contig) {
+        if (pw == 0) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(kv_full + st, 2 * Sh::TILE);
+#pragma unroll
+            for (int a = 0; a < Sh::KT; ++a) {
+              tma_load_3d(Ks + a * Sh::KV_ATOM, &tk, a * 64, g, r0, kv_full + st);
+              tma_load_3d(Vs + a * Sh::KV_ATOM, &tv, a * 64, g, r0, kv_full + st);
+            }
+          }
+          tma_pend |= 1u << st;
+          if (st == 0) use0 = u;
+          else if (st == 1) use1 = u;
+          else use2 = u;
+        } else if (lane == 0) {
+          mbar_arrive(kv_full + st);   // this warp has no part in a TMA tile
+        }
+        gathered &= ~(1u << (j & 31));
+      } else {
+        // this warp's rows pw*ROWS .. pw*ROWS+ROWS-1: 16 lanes cover one row
+#pragma unroll 4
+        for (int it = 0; it < ROWS * CPR / 32; ++it) {
+          const int f = it * 32 + lane;
+          const int e = pw * ROWS + f / CPR, c = f % CPR;
+          const int ra = __shfl_sync(0xffffffffu, rows[0], e & 31);
+          const int rb = __shfl_sync(0xffffffffu, rows[1], e & 31);
+          const int r = e < 32 ? ra : rb;
+          const bool okr = r >= 0;
+          const size_t go = ((size_t)(okr ? r : 0) * p.Hkv + g) * (D * 2) + c * 16;
+          const uint32_t so = (c >> 3) * Sh::KV_ATOM + e * 128 + (((c & 7) ^ (e & 7)) << 4);
+          cp_async16(Ks + so, kb + go, okr);
+          cp_async16(Vs + so, vb + go, okr);
+        }
+        gathered |= 1u << (j & 31);
+      }
+      cp_async_commit();   // one group per tile (empty for TMA tiles)
+    }
+    cp_async_wait<0>();
+    if (!*abort_flag)
+      for (int t = published; t < T; ++t) publish(t);
+    if (pw == 0 && lane == 0 && *abort_flag) {
+      if (tma_pend & 1u) wait_drain(kv_full + 0, use0 & 1);
+      if (tma_pend & 2u) wait_drain(kv_full + 1, use1 & 1);
+      if (tma_pend & 4u) wait_drain(kv_full + 2, use2 & 1);
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      const uint32_t id_qk = make_idesc_f16(128, BN, bf16, false);
+      const uint32_t id_pv = make_idesc_f16(128, D, bf16, true);
+      const uint32_t sQ = smem_u32(sm + Sh::OFF_Q), sK = smem_u32(sm + Sh::OFF_K), sV = smem_u32(sm + Sh::OFF_V);
+      const uint32_t tO = tbase + Sh::COL_O;
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      tc_fence_after();
+      // Event-driven issue: QK of the next tile as soon as its K/V have landed
+      // (and its S buffer is free: at most one tile ahead of the PVs), PV of
+      // the oldest tile as soon as its P is written.  Neither waits for the
+      // other, so a late tile never holds back the release of earlier stages.
+      int nqk = 0, npv = 0;
+      unsigned long long t_idle = 0;
+      while (ok && npv < T) {
+        bool progressed = false;
+        if (nqk < T && nqk < npv + 2 && mbar_test_wait(kv_full + nqk % NST, (nqk / NST) & 1)) {
+          const int st = nqk % NST, b = nqk & 1;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t a_off = (kk >> 2) * Sh::QATOM + (kk & 3) * 32;
+            const uint32_t b_off = (kk >> 2) * Sh::KV_ATOM + (kk & 3) * 32;
+            mma_ss(tbase + Sh::COL_S + b * BN, sdesc_sw128(sQ + a_off, 16, 1024),
+                   sdesc_sw128(sK + st * Sh::TILE + b_off, 16, 1024), id_qk, kk > 0);
+          }
+          tc_commit(s_full + b);
+          ++nqk;
+          progressed = true;
+        }
+        if (npv < nqk && mbar_test_wait(p_full + (npv & 1), (npv >> 1) & 1)) {
+          const int pst = npv % NST, pb = npv & 1;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tO, tbase + Sh::COL_S + pb * BN + kk * 8,
+                   sdesc_sw128(sV + pst * Sh::TILE + kk * 2048, Sh::KV_ATOM, 1024), id_pv, npv > 0 || kk > 0);
+          tc_commit(kv_empty + pst);
+          tc_commit(o_ready);
+          ++npv;
+          progressed = true;
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else if (t_idle == 0) {
+          t_idle = globaltimer();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (globaltimer() - t_idle > kWaitLimitNs) {
+          *abort_flag = 1;
+          ok = false;
+        }
+      }
+      tc_commit(drain);
+      wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (warp 0)
+    const int r = lane;
+    const bool row_ok = r < QV;
+    const int qi = r / G;
+    const int lim = (p.mask_kind == FA_MASK_CAUSAL) ? n_s - p.Nq + qi : n_s - 1;
+    const float c = p.qscale;
+    const bool cpos = c >= 0.f;
+    const float fill = cpos ? NEG_INF : -NEG_INF;
+    const uint32_t tO = tbase + Sh::COL_O;
+    float m_used = NEG_INF, l = 0.f;
+    bool ok = true;
+    // list entries of the next tile, loaded one tile ahead
+    int nxt0 = lane < cnt ? __ldg(rows_g + lane) : -1;
+    int nxt1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
+    for (int j = 0; j < T; ++j) {
+      const int b = j & 1;
+      unsigned vb[2];
+      vb[0] = __ballot_sync(0xffffffffu, nxt0 >= 0 && (long long)nxt0 < p.R);
+      vb[1] = __ballot_sync(0xffffffffu, nxt1 >= 0 && (long long)nxt1 < p.R);
+      {
+        const int pos = (j + 1) * BN + lane;
+        nxt0 = pos < cnt ? __ldg(rows_g + pos) : -1;
+        nxt1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
+      }
+      const int jb = j0 + j * BN;   // list position of column 0
+      const bool need_mask = (vb[0] & vb[1]) != 0xffffffffu || jb + BN - 1 > lim;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag)))) break;
+      tc_fence_after();
+      uint32_t sr[2][32];
+      tmem_ld32_nowait(tbase + Sh::COL_S + b * BN, sr[0]);
+      tmem_ld32_nowait(tbase + Sh::COL_S + b * BN + 32, sr[1]);
+      tmem_wait_ld_tied(sr[0]);
+      tmem_wait_ld_tied(sr[1]);
+      float ext = fill;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          float x = __uint_as_float(sr[h2][k]);
+          if (need_mask && !(((vb[h2] >> k) & 1u) && (jb + 32 * h2 + k <= lim))) x = fill;
+          ext = cpos ? fmaxf(ext, x) : fminf(ext, x);
+        }
+      const float mx = (ext == fill) ? NEG_INF : ext * c;
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = row_ok && m_new > m_used + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? fast_ex2(m_used - m_new) : 1.f;
+        if (need) {
+          l *= alpha;
+          m_used = m_new;
+        }
+        if (j > 0) {
+          // O holds the PV of tiles < j once PV(j-1) has completed
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (j - 1) & 1, abort_flag)))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t o[32];
+            tmem_ld32(tO + c4 * 32, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(tO + c4 * 32, o);
+          }
+        }
+      }
+      const float nmu = (m_used == NEG_INF) ? 0.f : -m_used;
+      const float2 c2 = make_float2(c, c), nmu2 = make_float2(nmu, nmu);
+      float2 sum2 = make_float2(0.f, 0.f);
+      uint32_t pk[32];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(sr[h2][2 * k]), __uint_as_float(sr[h2][2 * k + 1])),
+                                       c2, nmu2);
+          float2 pr = make_float2(fast_ex2(t2.x), fast_ex2(t2.y));
+          if (need_mask) {
+            const int k0 = 32 * h2 + 2 * k;
+            if (!(((vb[h2] >> (2 * k)) & 1u) && (jb + k0 <= lim))) pr.x = 0.f;
+            if (!(((vb[h2] >> (2 * k + 1)) & 1u) && (jb + k0 + 1 <= lim))) pr.y = 0.f;
+          }
+          sum2 = __fadd2_rn(sum2, pr);
+          pk[h2 * 16 + k] = pack2h(pr.x, pr.y, bf16);
+        }
+      l += sum2.x + sum2.y;
+      tmem_st32(tbase + Sh::COL_S + b * BN, pk);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full + b);
+    }
+    // ---- this split's result
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (T - 1) & 1, abort_flag));
+    tc_fence_after();
+    if (ok) {
+      const int i = r / G, h = g * G + r % G;
+      const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
+      const size_t pi = (unit * p.nsplit + split) * QV + r;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t o[32];
+        if (T > 0) {
+          tmem_ld32(tO + c4 * 32, o);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = 0u;
+        }
+        if (!row_ok) continue;
+        if (p.nsplit == 1) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) store_out(p.out, oi * D + c4 * 32 + k, __uint_as_float(o[k]) * inv, p.out_dtype);
+        } else if (m_used != NEG_INF) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + pi * D + c4 * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]), __uint_as_float(o[4 * k + 2]),
+                                 __uint_as_float(o[4 * k + 3]));
+        }
+      }
+      if (row_ok) {
+        if (p.nsplit == 1) {
+          if (p.lse) p.lse[oi] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : NEG_INF;
+        } else {
+          p.part_ml[pi * 2] = m_used;
+          p.part_ml[pi * 2 + 1] = l;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, Sh::TMEM_COLS);
+  }
+  if (*abort_flag) {
+    if (threadIdx.x == 0 && kp.err) atomicOr(kp.err, 1u);
+    return;
+  }
+  if (p.nsplit == 1) return;
+
+  // ---- cross-split merge by the last CTA of this (slice, KV head)
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *am_last = (atomicAdd(p.counters + unit, 1u) == (unsigned)(p.nsplit - 1));
+  __syncthreads();
+  if (!*am_last) return;
+  __threadfence();
+  const size_t pbase = unit * p.nsplit;
+  for (int qv = warp; qv < QV; qv += NWARP) {
+    float M = NEG_INF;
+    for (int k = lane; k < p.nsplit; k += 32) M = fmaxf(M, __ldcg(p.part_ml + ((pbase + k) * QV + qv) * 2));
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
+    const float Mu = (M == NEG_INF) ? 0.f : M;
+    float Ls = 0.f;
+    for (int k = lane; k < p.nsplit; k += 32) {
+      const float mk = __ldcg(p.part_ml + ((pbase + k) * QV + qv) * 2);
+      if (mk != NEG_INF) Ls = fmaf(__ldcg(p.part_ml + ((pbase + k) * QV + qv) * 2 + 1), fast_ex2(mk - Mu), Ls);
+    }
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, w);
+    if (lane == 0) {
+      fin[qv] = M;
+      fin[QROWS + qv] = Ls;
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < QV * D; t += NWARP * 32) {
+    const int qv = t / D, d = t % D;
+    const float M = fin[qv], Ls = fin[QROWS + qv];
+    const float Mu = (M == NEG_INF) ? 0.f : M;
+    float Os = 0.f;
+    for (int k = 0; k < p.nsplit; ++k) {
+      const float mk = __ldcg(p.part_ml + ((pbase + k) * QV + qv) * 2);
+      if (mk != NEG_INF) Os = fmaf(__ldcg(p.part_o + ((pbase + k) * QV + qv) * D + d), fast_ex2(mk - Mu), Os);
+    }
+    const int i = qv / G, h = g * G + qv % G;
+    const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
+    store_out(p.out, oi * D + d, Ls > 0.f ? Os / Ls : 0.f, p.out_dtype);
+    if (p.lse && d == 0) p.lse[oi] = Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : NEG_INF;
+  }
+  if (threadIdx.x == 0) p.counters[unit] = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 dk_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool dk_map(CUtensorMap* m, const void* base, bool bf16, int D, int Hkv, long long R) {
+  auto enc = dk_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)R};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * Hkv * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)dk::BN};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D view of a pool [R][Hkv][D] as [R * Hkv] rows of D, box 64 columns x one
+// row (the shape tile::gather4 takes).
+bool dk_gather_map(CUtensorMap* m, const void* base, bool bf16, int D, int Hkv, long long R) {
+  auto enc = dk_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)R * (cuuint64_t)Hkv};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int dk_occupancy() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] > 0) return cached[dev];
+  auto kern = fa_rows_decode_tc_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkShape<D>::SMEM) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, dk::NWARP * 32, DkShape<D>::SMEM) != cudaSuccess) return 0;
+  // tensor memory also bounds residency: 512 columns per SM
+  const int by_tmem = 512 / (int)DkShape<D>::TMEM_COLS;
+  n = n < by_tmem ? n : by_tmem;
+  cached[dev] = n;
+  return n;
+}
+
+template <int D>
+cudaError_t dk_launch(const DecodeParams& a, unsigned int* err, cudaStream_t st) {
+  if (dk_occupancy<D>() <= 0) return cudaErrorInvalidConfiguration;
+  DecodeTcParams kp;
+  kp.a = a;
+  kp.err = err;
+  kp.tma_kv = a.R >= dk::BN;
+  const bool bf16 = a.q_bf16 != 0;
+  CUtensorMap tk, tv, gk, gv;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  if (kp.tma_kv) {
+    if (!dk_map(&tk, a.k, bf16, D, a.Hkv, a.R) || !dk_map(&tv, a.v, bf16, D, a.Hkv, a.R)) return cudaErrorInvalidValue;
+  }
+  if (!dk_gather_map(&gk, a.k, bf16, D, a.Hkv, a.R) || !dk_gather_map(&gv, a.v, bf16, D, a.Hkv, a.R))
+    return cudaErrorInvalidValue;
+  dim3 grid(a.nsplit, a.Hkv, a.S);
+  fa_rows_decode_tc_kernel<D><<<grid, dk::NWARP * 32, DkShape<D>::SMEM, st>>>(kp, tk, tv, gk, gv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc_supported(int D, int kind, int qv, int mask_kind) {
+  return (D == 128 || D == 256) && (kind == KV_BF16 || kind == KV_F16) && qv >= 1 && qv <= dk::QROWS &&
+         mask_kind != FA_MASK_DENSE;
+}
+
+int decode_tc_occupancy(int D) { return D == 128 ? dk_occupancy<128>() : D == 256 ? dk_occupancy<256>() : 0; }
+
+int decode_tc_tile() { return dk::BN; }
+
+cudaError_t decode_tc_launch(const DecodeParams& a, int D, unsigned int* err, cudaStream_t st) {
+  if (D == 128) return dk_launch<128>(a, err, st);
+  if (D == 256) return dk_launch<256>(a, err, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace far

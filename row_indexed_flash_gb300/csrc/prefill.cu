@@ -94,18 +94,13 @@ __device__ __forceinline__ bool col_visible(int k, unsigned vb0, unsigned vb1, u
   return ((vb >> (k & 31)) & 1u) && (jbase + k <= lim);
 }
 
-// 32 columns of this thread's S row starting at column c0, scaled into log2
-// units, masked columns -inf.
-__device__ __forceinline__ void load_s32(float (&x)[32], uint32_t tS, int c0, float c, bool need_mask, unsigned vb0,
-                                         unsigned vb1, unsigned vb2, unsigned vb3, int jbase, int lim) {
-  const float NEG_INF = __int_as_float(0xff800000);
-  uint32_t r[32];
-  tmem_ld32(tS + c0, r);
-#pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    x[k] = __uint_as_float(r[k]) * c;
-    if (need_mask && !col_visible(c0 + k, vb0, vb1, vb2, vb3, jbase, lim)) x[k] = NEG_INF;
-  }
+// 64 raw fp32 columns of this thread's S row starting at column c0, two loads
+// in flight per wait.
+__device__ __forceinline__ void load_s64(uint32_t (&a)[32], uint32_t (&b)[32], uint32_t tS, int c0) {
+  tmem_ld32_nowait(tS + c0, a);
+  tmem_ld32_nowait(tS + c0 + 32, b);
+  tmem_wait_ld_tied(a);
+  tmem_wait_ld_tied(b);
 }
 
 __global__ void __launch_bounds__(pf::NWARP * 32, 1)
@@ -278,6 +273,9 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       };
       bool ok = mbar_wait(q_full, 0, abort_flag);
       tc_fence_after();
+      // Issue order per KV tile j: [PV_0(j-1), QK_0(j)], [PV_1(j-1), QK_1(j)],
+      // so each tile's QK follows the PV that read its S buffer (the tensor
+      // pipe runs one thread's MMAs in order).
       for (int j = 0; ok && j < T; ++j) {
         const int st = j % NST, u = j / NST;
         if (!(ok = mbar_wait(k_full + st, u & 1, abort_flag))) break;
@@ -322,28 +320,48 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
     const float c = p.qscale;
     float m_used = NEG_INF, l = 0.f;
     bool ok = true;
+    // list entries of the next tile, loaded one tile ahead of their use
+    int nxt[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) nxt[t] = lane + 32 * t < n_s ? __ldg(rows_g + lane + 32 * t) : -1;
     for (int j = 0; j < T; ++j) {
       unsigned vbits[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int pos = j * BN + lane + 32 * t;
-        const int r = pos < n_s ? __ldg(rows_g + pos) : -1;
-        vbits[t] = __ballot_sync(0xffffffffu, r >= 0 && (long long)r < p.R);
+        vbits[t] = __ballot_sync(0xffffffffu, nxt[t] >= 0 && (long long)nxt[t] < p.R);
+        const int pos = (j + 1) * BN + lane + 32 * t;
+        nxt[t] = pos < n_s ? __ldg(rows_g + pos) : -1;
       }
       const bool all_valid = (vbits[0] & vbits[1] & vbits[2] & vbits[3]) == 0xffffffffu;
       // warp-uniform: the tcgen05 loads below need every lane of the warp
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + qt, j & 1, abort_flag)))) break;
       tc_fence_after();
       const bool need_mask = !all_valid || j * BN + BN - 1 > lim;
-      // pass 1: the row maximum, 32 columns at a time
-      float mx = NEG_INF;
+      // pass 1: the row maximum of the logits S*c (c = scale*log2e), taken on
+      // raw S: max(S*c) = c*max(S) for c >= 0 and c*min(S) for c < 0
+      const bool cpos = c >= 0.f;
+      const float fill = cpos ? NEG_INF : -NEG_INF;
+      float ext = fill;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float x[32];
-        load_s32(x, tS, c4 * 32, c, need_mask, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim);
+      for (int c8 = 0; c8 < 2; ++c8) {
+        uint32_t ra[32], rb[32];
+        load_s64(ra, rb, tS, c8 * 64);
+        if (need_mask) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, x[k]);
+          for (int k = 0; k < 64; ++k) {
+            float x = __uint_as_float(k < 32 ? ra[k] : rb[k - 32]);
+            if (!col_visible(c8 * 64 + k, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) x = fill;
+            ext = cpos ? fmaxf(ext, x) : fminf(ext, x);
+          }
+        } else if (cpos) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) ext = fmaxf(ext, __uint_as_float(k < 32 ? ra[k] : rb[k - 32]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) ext = fminf(ext, __uint_as_float(k < 32 ? ra[k] : rb[k - 32]));
+        }
       }
+      const float mx = (ext == fill) ? NEG_INF : ext * c;
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + 8.f;
       if (__any_sync(0xffffffffu, need)) {
@@ -365,27 +383,45 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
           }
         }
       }
-      // pass 2: P = exp2(x - m) as 16-bit pairs; half h of P (32 columns)
-      // overwrites S columns 32h..32h+31, which pass 2 has already read
-      const float mu = (m_used == NEG_INF) ? 0.f : m_used;
-      float sum = 0.f;
+      // pass 2: P = exp2(S*c - m) as 16-bit pairs, invisible columns 0; half h
+      // of P (32 columns) overwrites S columns 32h..32h+31, already read here
+      const float nmu = (m_used == NEG_INF) ? 0.f : -m_used;
+      const float2 c2v = make_float2(c, c), nmu2 = make_float2(nmu, nmu);
+      float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
+        uint32_t ra[32], rb[32];
+        load_s64(ra, rb, tS, hh * 64);
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c0 = hh * 64 + cc * 32;
           float x[32];
-          load_s32(x, tS, hh * 64 + c2 * 32, c, need_mask, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float p0 = fast_ex2(x[2 * k] - mu);
-            const float p1 = fast_ex2(x[2 * k + 1] - mu);
-            sum += p0 + p1;
-            pk[c2 * 16 + k] = pack2(p0, p1, bf16);
+          for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(cc == 0 ? ra[k] : rb[k]);
+          if (need_mask) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), c2v, nmu2);
+              float2 pr = make_float2(fast_ex2(t.x), fast_ex2(t.y));
+              if (!col_visible(c0 + 2 * k, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) pr.x = 0.f;
+              if (!col_visible(c0 + 2 * k + 1, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) pr.y = 0.f;
+              sum2 = __fadd2_rn(sum2, pr);
+              pk[cc * 16 + k] = pack2(pr.x, pr.y, bf16);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), c2v, nmu2);
+              const float2 pr = make_float2(fast_ex2(t.x), fast_ex2(t.y));
+              sum2 = __fadd2_rn(sum2, pr);
+              pk[cc * 16 + k] = pack2(pr.x, pr.y, bf16);
+            }
           }
         }
         tmem_st32(tS + hh * 32, pk);
       }
+      const float sum = sum2.x + sum2.y;
       l += sum;
       tc_fence_before();
       mbar_arrive(p_full + qt);

@@ -79,7 +79,7 @@ def _args(**kw):
     (dict(mask_kind=far.FA_MASK_DENSE), far.FaRowsError),  # dense mask without a pointer
     (dict(kv_dtype=far.FA_I8), far.FaRowsError),           # int8 without scales
     (dict(k=4096 + 8), far.FaRowsError),                   # misaligned pool
-    (dict(Nq=8, Hq=32, Hkv=8), far.FaRowsError),           # decode packs at most 32 query vectors
+    (dict(Nq=9, Hq=32, Hkv=8), far.FaRowsError),           # decode packs at most 32 query vectors
 ])
 def test_bad_arguments_are_rejected_on_the_host(lib, kw, status):
     a = _args(**kw)

@@ -57,6 +57,16 @@ def test_prefill_matches_oracle(name):
     assert_lse(lse, ref_lse, name)
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.08838834764831845, 0.05])
+def test_prefill_scale_edge_cases_with_masks(scale):
+    p = synth.random_problem(23, S=2, Nq=40, Hq=8, Hkv=2, D=128, R=1500, L=600, causal=True, pad_frac=0.2)
+    p.scale = scale
+    out, lse = run_prefill(p)
+    ref, ref_lse = oracle_for(p)
+    assert_parity(out, ref, f"scale {scale}")
+    assert_lse(lse, ref_lse, f"scale {scale}")
+
+
 @pytest.mark.parametrize("odt", [torch.bfloat16, torch.float16])
 def test_prefill_low_precision_outputs(odt):
     p = CASES["runs_tma_causal"]()

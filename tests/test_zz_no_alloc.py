@@ -40,7 +40,9 @@ def test_static_scratch_decode_matches_workspace_decode_on_two_calls():
 
 
 def test_static_scratch_decode_rejects_plans_larger_than_the_array():
-    p = synth.random_problem(4243, S=64, Nq=1, Hq=32, Hkv=8, D=128, R=70000, L=65536, pad_frac=0.0)
+    # D 64 lists of 131,072 entries: at most 2,048 entries per CTA, so at least
+    # 64 splits of 4 query vectors for each of 512 (slice, KV head) pairs
+    p = synth.random_problem(4243, S=64, Nq=1, Hq=32, Hkv=8, D=64, R=131072, L=131072, pad_frac=0.0)
     q, k, v, rows = _device_problem(p)
     a, out, _ = far.make_args(q, k, v, rows, p.scale)
     need = far.fa_rows_workspace_size(a)
