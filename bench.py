@@ -44,11 +44,12 @@ METRIC = "row-indexed attention: decode gathered-KV GB/s, prefill TFLOP/s (vs GB
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "decode": ["row_indexed_flash_gb300/csrc/decode_tc.cu", "row_indexed_flash_gb300/csrc/tc.cuh",
-               "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
+               "row_indexed_flash_gb300/csrc/merge.cuh", "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
     "prefill": ["row_indexed_flash_gb300/csrc/prefill.cu", "row_indexed_flash_gb300/csrc/tc.cuh",
                 "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
 }
-KERNEL_NAMES = {"decode": "fa_rows_decode_tc_kernel<128>", "prefill": "fa_rows_prefill_kernel"}
+KERNEL_NAMES = {"decode": "fa_rows_decode_tc_kernel", "prefill": "fa_rows_prefill_kernel",
+                "decode_cc": "fa_rows_decode_kernel"}
 PROFILE_FILES = {
     "decode_bf16": "profiles/decode_bf16_4x16384_ncu.txt",
     "prefill_bf16": "profiles/prefill_bf16_4x2048x99936_ncu.txt",
@@ -217,6 +218,12 @@ def build_problem(workload: str):
         return synth.decode_bf16_large()
     if workload == "prefill_bf16":
         return synth.prefill_bf16()
+    if workload == "paged_int8":
+        return synth.paged_int8()
+    if workload == "sparse_bf16":
+        return synth.sparse_bf16()
+    if workload == "decode_f16_small":
+        return synth.decode_fp16_small()
     if workload == "prefill_bf16_small":
         # profiling size: 4 x 16,384-row lists in a 65,536-row pool (268 MB of K/V, above L2)
         return synth.prefill_bf16(n_seq=4, seq_rows=16384, pool_rows=65536)
@@ -238,9 +245,22 @@ def run_gpu(args, rank, world, p, cpu_baseline):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt).to(dev)
 
     is_prefill = args.workload.startswith("prefill")
+    paged = p.kv_int8
     q = to_dev(p.q)
-    rows = torch.from_numpy(p.kv_rows).to(dev)
     k0, v0 = to_dev(p.k), to_dev(p.v)
+    scales = None
+    if paged:
+        # write path (not timed): quantise the bf16 pool into INT8 codes + fp16 scales
+        kq, ks = far.fa_kv_quantize_int8(k0, p.R)
+        vq, vs = far.fa_kv_quantize_int8(v0, p.R)
+        del k0, v0
+        torch.cuda.synchronize(dev)
+        k0, v0, scales = kq, vq, (ks, vs)
+        pt = torch.from_numpy(p.page_table).to(dev)
+        sl = torch.from_numpy(p.seq_len).to(dev)
+        rows = torch.empty((p.S, p.L), dtype=torch.int32, device=dev)
+    else:
+        rows = torch.from_numpy(p.kv_rows).to(dev)
     pool_bytes = 2 * k0.numel() * k0.element_size()
     # rotate over enough pool copies that each step reads data not left in L2
     n_copies = max(1, min(3, int(math.ceil(3 * 129e6 / pool_bytes)) + 1)) if not is_prefill else 1
@@ -248,7 +268,10 @@ def run_gpu(args, rank, world, p, cpu_baseline):
     out = torch.empty((p.S, p.Nq, p.Hq, p.D), dtype=torch.float32, device=dev)
     a_list = []
     for (k, v) in pools:
-        a, _, _ = far.make_args(q, k, v, rows, p.scale, causal=p.causal, out=out)
+        kw = {}
+        if paged:
+            kw = dict(k_scale=scales[0], v_scale=scales[1], kv_len=sl, n_valid_hint=p.n_valid())
+        a, _, _ = far.make_args(q, k, v, rows, p.scale, causal=p.causal, out=out, **kw)
         a_list.append(a)
     entry = far.lib().fa_rows_prefill if is_prefill else far.lib().fa_rows_decode
     need = far.fa_rows_workspace_size(a_list[0], is_prefill)
@@ -256,7 +279,14 @@ def run_gpu(args, rank, world, p, cpu_baseline):
     sh = stream.cuda_stream
     import ctypes
 
+    lib = far.lib()
+
     def step(i):
+        if paged:   # page tables -> row lists, then the decode (both kernels of the step)
+            st = lib.fa_kv_page_table_to_rows(pt.data_ptr(), pt.shape[1], sl.data_ptr(), p.S, p.page_size,
+                                              rows.data_ptr(), p.L, sh)
+            if st != 0:
+                raise far.FaRowsError(st, far.fa_last_error())
         st = entry(ctypes.byref(a_list[i % len(a_list)]), ws.data_ptr(), ws.numel(), sh)
         if st != 0:
             raise far.FaRowsError(st, far.fa_last_error())
@@ -288,12 +318,15 @@ def run_gpu(args, rank, world, p, cpu_baseline):
     # end to end through the public API: pinned host inputs copied in every step,
     # the output read back every step
     hq = torch.from_numpy(np.ascontiguousarray(p.q).view(np.int16)).view(tdt).pin_memory()
-    hk = torch.from_numpy(np.ascontiguousarray(p.k).view(np.int16)).view(tdt).pin_memory()
-    hv = torch.from_numpy(np.ascontiguousarray(p.v).view(np.int16)).view(tdt).pin_memory()
-    hr = torch.from_numpy(p.kv_rows).pin_memory()
+    hk = k0.cpu().pin_memory()
+    hv = v0.cpu().pin_memory()
+    hr = rows.cpu().pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     dq, dk, dv, dr = torch.empty_like(q), torch.empty_like(k0), torch.empty_like(v0), torch.empty_like(rows)
-    a_e2e, _, _ = far.make_args(dq, dk, dv, dr, p.scale, causal=p.causal, out=out)
+    kw = {}
+    if paged:
+        kw = dict(k_scale=scales[0], v_scale=scales[1], kv_len=sl, n_valid_hint=p.n_valid())
+    a_e2e, _, _ = far.make_args(dq, dk, dv, dr, p.scale, causal=p.causal, out=out, **kw)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hr))
     d2h = hout.numel() * hout.element_size()
     e2e_steps = max(3, min(args.steps, 20))
@@ -370,7 +403,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             "unit": unit,
             "frac": round(achieved / peak, 4),
             "traffic": profiled_traffic(args.workload, kind),
-            "kernel": KERNEL_NAMES[kind],
+            "kernel": KERNEL_NAMES["decode_cc" if paged else kind],
             "kernel_ms": round(mean_launch_ms, 5),
             "work_per_launch": work,
         },
@@ -381,7 +414,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4),
         },
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if paged else 1),
         "clocks": clk.summary(),
         "cpu_baseline": cpu_baseline,
     }
@@ -397,7 +430,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="decode_bf16", choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small"])
+    ap.add_argument("--workload", default="decode_bf16", choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8",
+                                                             "sparse_bf16", "decode_f16_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -442,7 +476,8 @@ def main():
 
     p = build_problem(args.workload)
     cpu_baseline = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload.startswith("prefill"):
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload.startswith("prefill")
+            and p.kv_rows is not None):
         units = [(s, g) for s in range(p.S) for g in range(p.Hkv)]
         passes = 3
         v, dt = oracle_rate(p, units, passes, procs)

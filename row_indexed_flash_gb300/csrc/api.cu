@@ -95,6 +95,8 @@ struct DecodePlan {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int kMaxSplits = far::kDecodeMaxSplits;
+
 // The prefill workspace holds one error word: non-zero after a call whose
 // pipeline waits expired (its output is then invalid).
 constexpr size_t kPrefillWorkspace = 256;
@@ -137,7 +139,7 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
     return FA_OK;
   }
   int occ = 0;
-  if (pl->tc) occ = far::decode_tc_occupancy(a->D);
+  if (pl->tc) occ = far::decode_tc_occupancy(a->D, (int)(qv < 1 ? 1 : qv));
   else if (kind == far::KV_BF16) occ = far::decode_occupancy_bf16(a->D, qvp);
   else if (kind == far::KV_F16) occ = far::decode_occupancy_f16(a->D, qvp);
   else if (kind == far::KV_I8) occ = far::decode_occupancy_i8(a->D, qvp);
@@ -149,10 +151,12 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   // fixed cost of a CTA (start-up, pipeline fill, merge), in streamed rows
   const double c_cta = pl->tc ? 256.0 : 64.0, c_split = 2.0, c_empty = 16.0;
   const int ns_lo = (int)((L + chunk_max - 1) / chunk_max);
+  if (ns_lo > kMaxSplits)
+    return fail(FA_ERR_UNSUPPORTED, "list length %d needs more than %d splits of %d entries", L, kMaxSplits, chunk_max);
   const int ns_hi = (L + align - 1) / align;
   double best = 1e300;
   int best_ns = ns_lo;
-  for (int ns = ns_lo; ns <= ns_hi && ns <= 4096; ++ns) {
+  for (int ns = ns_lo; ns <= ns_hi && ns <= kMaxSplits; ++ns) {
     const long long chunk = round_up((L + ns - 1) / ns, align);
     if (chunk > chunk_max) continue;
     const long long ns_eff = (L + chunk - 1) / chunk;

@@ -23,6 +23,7 @@
 #pragma once
 
 #include "fa_internal.cuh"
+#include "merge.cuh"
 
 namespace far {
 
@@ -51,8 +52,10 @@ struct DecodeShape {
   static constexpr int NW = kDecodeWarps;
   static constexpr int IDX_BYTES = kDecodeChunkMax * 4;
   static constexpr int RING = NW * NSTAGE * SLOT;
-  static constexpr int MERGE = NW * QVP * (D + 2) * 4;
-  static constexpr int BODY = RING > MERGE ? RING : MERGE;
+  static constexpr int MERGE = NW * QVP * (D + 2) * 4;                      // warp merge
+  static constexpr int SPLITS = (2 * kDecodeMaxSplits + 2) * QVP * 4;        // split merge
+  static constexpr int BODY_A = RING > MERGE ? RING : MERGE;
+  static constexpr int BODY = BODY_A > SPLITS ? BODY_A : SPLITS;
   static constexpr int PBUF = NW * (RT * QVP + QVP) * 4;   // per warp: p[RT][QVP], alpha[QVP]
   static constexpr int SMEM = IDX_BYTES + BODY + PBUF + 2 * QVP * 4;
   static_assert(LG >= 1 && LG <= 32 && NG * LG == 32 && STEPS * NG == RT, "bad decode shape");
@@ -417,41 +420,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) fa_rows_decode_kernel(const
   if (!am_last) return;
   __threadfence();
 
-  const size_t pbase = unit * p.nsplit;
-  for (int qv = warp; qv < QVP; qv += NW) {
-    float M = NEG_INF;
-    for (int k = lane; k < p.nsplit; k += 32) M = fmaxf(M, __ldcg(p.part_ml + ((pbase + k) * QVP + qv) * 2));
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
-    const float Mu = (M == NEG_INF) ? 0.f : M;
-    float Ls = 0.f;
-    for (int k = lane; k < p.nsplit; k += 32) {
-      const float mk = __ldcg(p.part_ml + ((pbase + k) * QVP + qv) * 2);
-      if (mk != NEG_INF) Ls = fmaf(__ldcg(p.part_ml + ((pbase + k) * QVP + qv) * 2 + 1), fast_ex2(mk - Mu), Ls);
-    }
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, w);
-    if (lane == 0) {
-      fin[qv] = M;
-      fin[QVP + qv] = Ls;
-    }
-  }
-  __syncthreads();
-  for (int t = threadIdx.x; t < QVP * D; t += NW * 32) {
-    const int qv = t / D, d = t % D;
-    if (qv >= p.QV) continue;
-    const float M = fin[qv], Ls = fin[QVP + qv];
-    const float Mu = (M == NEG_INF) ? 0.f : M;
-    float Os = 0.f;
-    for (int k = 0; k < p.nsplit; ++k) {
-      const float mk = __ldcg(p.part_ml + ((pbase + k) * QVP + qv) * 2);
-      if (mk != NEG_INF) Os = fmaf(__ldcg(p.part_o + ((pbase + k) * QVP + qv) * D + d), fast_ex2(mk - Mu), Os);
-    }
-    const int i = qv / G, h = g * G + qv % G;
-    const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
-    store_out(p.out, oi * D + d, Ls > 0.f ? Os / Ls : 0.f, p.out_dtype);
-    if (p.lse && d == 0) p.lse[oi] = Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : NEG_INF;
-  }
+  merge_splits<D>(p, unit, QVP, p.QV, s, g, reinterpret_cast<float*>(body));
   if (threadIdx.x == 0) p.counters[unit] = 0u;
 }
 

@@ -34,6 +34,7 @@
 
 #include <mutex>
 
+#include "merge.cuh"
 #include "tc.cuh"
 
 namespace far {
@@ -47,7 +48,7 @@ constexpr int NWARP = 2 + NPROD;   // softmax, producers, MMA
 constexpr int MMA_WARP = 1 + NPROD;
 }  // namespace dk
 
-template <int D>
+template <int D, int QVP>
 struct DkShape {
   static constexpr int KT = D / 64;                  // 128-byte K atoms per row
   static constexpr int QATOM = dk::QROWS * 128;      // bytes of one atom column of the Q tile
@@ -61,13 +62,18 @@ struct DkShape {
   // q_full, kv_full[NST], kv_empty[NST], s_full[2], p_full[2], o_ready, drain
   static constexpr int NBAR = 1 + 2 * dk::NST + 2 + 2 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_IDX = OFF_MISC + 16;
-  static constexpr int OFF_FIN = OFF_IDX + dk::BN * 4;
-  static constexpr int SMEM_USED = OFF_FIN + 2 * dk::QROWS * 4;
+  static constexpr int OFF_SS = ((OFF_MISC + 16 + 127) / 128) * 128;   // S rows of the real query vectors, fp32
+  static constexpr int OFF_SP = OFF_SS + QVP * dk::BN * 4;             // P rows, packed 16-bit pairs
+  static constexpr int SMEM_USED = OFF_SP + QVP * dk::BN * 2;
   static constexpr int SMEM = SMEM_USED + 1024;
   static constexpr uint32_t TMEM_COLS = (2 * dk::BN + D) <= 256 ? 256 : 512;
   static constexpr uint32_t COL_S = 0;               // S0, S1: 64 columns each
   static constexpr uint32_t COL_O = 2 * dk::BN;      // O: D columns
+  // vector (16-byte) accesses: Q/K/V tiles (1024-byte swizzle atoms), S and P rows
+  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && TILE % 1024 == 0, "tiles must be 1024-byte aligned");
+  static_assert(OFF_SS % 16 == 0 && OFF_SP % 16 == 0 && (dk::BN * 4) % 16 == 0 && (dk::BN * 2) % 16 == 0,
+                "S/P rows must be 16-byte aligned");
+  static_assert(OFF_BAR % 8 == 0, "mbarriers must be 8-byte aligned");
 };
 
 struct DecodeTcParams {
@@ -96,12 +102,189 @@ __device__ __forceinline__ void wait_drain(uint64_t* b, uint32_t parity) {
 
 }  // namespace
 
-template <int D>
-__global__ void __launch_bounds__(dk::NWARP * 32, 1)
+// The softmax role (warp 0) of fa_rows_decode_tc_kernel for QVP = the query
+// vector count rounded up to a power of two.
+template <int D, int QVP>
+__device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char* sm, uint64_t* s_full, uint64_t* p_full,
+                                           uint64_t* o_ready, volatile int* abort_flag, uint32_t tbase, int T, int cnt,
+                                           int j0, int n_s, const int32_t* rows_g, size_t unit, int split, int s,
+                                           int g) {
+  using Sh = DkShape<D, QVP>;
+  using namespace dk;
+  const float NEG_INF = __int_as_float(0xff800000);
+  const int lane = threadIdx.x & 31;
+  const int G = p.G, QV = p.QV;
+  const bool bf16 = p.q_bf16 != 0;
+    // Only rows 0..QV-1 of S are real.  After the tensor-memory load (one row
+    // per lane), the real rows are spread over all 32 lanes through shared
+    // memory: LPR = 32/QVP lanes per row, CPL = BN/LPR columns per lane, so
+    // the exponentials and reductions use the whole warp.  P goes back the
+    // same way and is stored over S by the lanes that own its rows.
+    float* sS = reinterpret_cast<float*>(sm + Sh::OFF_SS);
+    uint32_t* sP = reinterpret_cast<uint32_t*>(sm + Sh::OFF_SP);
+    constexpr int qvp = QVP;
+    constexpr int LPR = 32 / QVP, CPL = BN / LPR;   // lanes per row, columns per lane
+    const int row = lane / LPR, part = lane % LPR;
+    const bool row_ok = row < QV;               // this lane's share is of a real row
+    const int lim = (p.mask_kind == FA_MASK_CAUSAL) ? n_s - p.Nq + row / G : n_s - 1;
+    const float c = p.qscale;
+    const uint32_t tO = tbase + Sh::COL_O;
+    float m_used = NEG_INF, l = 0.f;            // state of row `row`, held by its LPR lanes
+    bool ok = true;
+    int nxt0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // list entries of the next tile
+    int nxt1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
+    for (int j = 0; j < T; ++j) {
+      const int b = j & 1;
+      unsigned vb[2];
+      vb[0] = __ballot_sync(0xffffffffu, nxt0 >= 0 && (long long)nxt0 < p.R);
+      vb[1] = __ballot_sync(0xffffffffu, nxt1 >= 0 && (long long)nxt1 < p.R);
+      {
+        const int pos = (j + 1) * BN + lane;
+        nxt0 = pos < cnt ? __ldg(rows_g + pos) : -1;
+        nxt1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
+      }
+      const int jb = j0 + j * BN;   // list position of column 0
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag)))) break;
+      tc_fence_after();
+      {
+        uint32_t sr[2][32];
+        tmem_ld32_nowait(tbase + Sh::COL_S + b * BN, sr[0]);
+        tmem_ld32_nowait(tbase + Sh::COL_S + b * BN + 32, sr[1]);
+        tmem_wait_ld_tied(sr[0]);
+        tmem_wait_ld_tied(sr[1]);
+        if (lane < QV) {
+          float4* dst = reinterpret_cast<float4*>(sS + lane * BN);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(sr[0][4 * k]), __uint_as_float(sr[0][4 * k + 1]),
+                                 __uint_as_float(sr[0][4 * k + 2]), __uint_as_float(sr[0][4 * k + 3]));
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[8 + k] = make_float4(__uint_as_float(sr[1][4 * k]), __uint_as_float(sr[1][4 * k + 1]),
+                                     __uint_as_float(sr[1][4 * k + 2]), __uint_as_float(sr[1][4 * k + 3]));
+        }
+      }
+      __syncwarp();
+      // this lane's CPL columns of row `row`, scaled into log2 units, masked
+      const int c0 = part * CPL;
+      const unsigned long long vbits = ((unsigned long long)vb[1] << 32) | vb[0];
+      float x[CPL];
+      float mx = NEG_INF;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const int col = c0 + k;
+        float v = row_ok ? sS[row * BN + col] * c : NEG_INF;
+        if (!(((vbits >> col) & 1ull) && (jb + col <= lim))) v = NEG_INF;
+        x[k] = v;
+        mx = fmaxf(mx, v);
+      }
+#pragma unroll
+      for (int w = 1; w < LPR; w <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = row_ok && m_new > m_used + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? fast_ex2(m_used - m_new) : 1.f;
+        if (need) {
+          l *= alpha;
+          m_used = m_new;
+        }
+        if (j > 0) {
+          // O row r (tensor-memory lane r) is rescaled by the lane that owns it
+          const float a_r = __shfl_sync(0xffffffffu, alpha, (lane % qvp) * LPR);
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (j - 1) & 1, abort_flag)))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t o[32];
+            tmem_ld32(tO + c4 * 32, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * a_r);
+            tmem_st32(tO + c4 * 32, o);
+          }
+        }
+      }
+      const float mu = (m_used == NEG_INF) ? 0.f : m_used;
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < CPL; k += 2) {
+        const float p0 = fast_ex2(x[k] - mu), p1 = fast_ex2(x[k + 1] - mu);
+        sum += p0 + p1;
+        if (row_ok) sP[row * (BN / 2) + (c0 + k) / 2] = pack2h(p0, p1, bf16);
+      }
+#pragma unroll
+      for (int w = 1; w < LPR; w <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
+      l += sum;
+      __syncwarp();
+      {
+        uint32_t pk[32];
+        if (lane < QV) {
+          const uint4* src = reinterpret_cast<const uint4*>(sP + lane * (BN / 2));
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 w4 = src[k];
+            pk[4 * k] = w4.x; pk[4 * k + 1] = w4.y; pk[4 * k + 2] = w4.z; pk[4 * k + 3] = w4.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) pk[k] = 0u;
+        }
+        tmem_st32(tbase + Sh::COL_S + b * BN, pk);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full + b);
+    }
+    // ---- this split's result: lane r < QV owns O row r; its (m, l) come from lane r*LPR
+    const float m_r = __shfl_sync(0xffffffffu, m_used, (lane % qvp) * LPR);
+    const float l_r = __shfl_sync(0xffffffffu, l, (lane % qvp) * LPR);
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (T - 1) & 1, abort_flag));
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (ok) {
+      const int r = lane;
+      const bool own = r < QV;
+      const int i = r / G, h = g * G + r % G;
+      const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
+      const size_t pi = (unit * p.nsplit + split) * QV + r;
+      const float inv = l_r > 0.f ? 1.f / l_r : 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t o[32];
+        if (T > 0) {
+          tmem_ld32(tO + c4 * 32, o);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = 0u;
+        }
+        if (!own) continue;
+        if (p.nsplit == 1) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) store_out(p.out, oi * D + c4 * 32 + k, __uint_as_float(o[k]) * inv, p.out_dtype);
+        } else if (m_r != NEG_INF) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + pi * D + c4 * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]), __uint_as_float(o[4 * k + 2]),
+                                 __uint_as_float(o[4 * k + 3]));
+        }
+      }
+      if (own) {
+        if (p.nsplit == 1) {
+          if (p.lse) p.lse[oi] = l_r > 0.f ? (m_r + __log2f(l_r)) * kLn2 : NEG_INF;
+        } else {
+          p.part_ml[pi * 2] = m_r;
+          p.part_ml[pi * 2 + 1] = l_r;
+        }
+      }
+    }
+}
+
+template <int D, int QVP>
+__global__ void __launch_bounds__(dk::NWARP * 32, 2)
     fa_rows_decode_tc_kernel(const DecodeTcParams kp, const __grid_constant__ CUtensorMap tk,
                              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap gk,
                              const __grid_constant__ CUtensorMap gv) {
-  using Sh = DkShape<D>;
+  using Sh = DkShape<D, QVP>;
   using namespace dk;
   const DecodeParams& p = kp.a;
   const float NEG_INF = __int_as_float(0xff800000);
@@ -118,7 +301,6 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Sh::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::OFF_MISC + 4);
   int* am_last = reinterpret_cast<int*>(sm + Sh::OFF_MISC + 8);
-  float* fin = reinterpret_cast<float*>(sm + Sh::OFF_FIN);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
@@ -325,133 +507,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax (warp 0)
-    const int r = lane;
-    const bool row_ok = r < QV;
-    const int qi = r / G;
-    const int lim = (p.mask_kind == FA_MASK_CAUSAL) ? n_s - p.Nq + qi : n_s - 1;
-    const float c = p.qscale;
-    const bool cpos = c >= 0.f;
-    const float fill = cpos ? NEG_INF : -NEG_INF;
-    const uint32_t tO = tbase + Sh::COL_O;
-    float m_used = NEG_INF, l = 0.f;
-    bool ok = true;
-    // list entries of the next tile, loaded one tile ahead
-    int nxt0 = lane < cnt ? __ldg(rows_g + lane) : -1;
-    int nxt1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
-    for (int j = 0; j < T; ++j) {
-      const int b = j & 1;
-      unsigned vb[2];
-      vb[0] = __ballot_sync(0xffffffffu, nxt0 >= 0 && (long long)nxt0 < p.R);
-      vb[1] = __ballot_sync(0xffffffffu, nxt1 >= 0 && (long long)nxt1 < p.R);
-      {
-        const int pos = (j + 1) * BN + lane;
-        nxt0 = pos < cnt ? __ldg(rows_g + pos) : -1;
-        nxt1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
-      }
-      const int jb = j0 + j * BN;   // list position of column 0
-      const bool need_mask = (vb[0] & vb[1]) != 0xffffffffu || jb + BN - 1 > lim;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag)))) break;
-      tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32_nowait(tbase + Sh::COL_S + b * BN, sr[0]);
-      tmem_ld32_nowait(tbase + Sh::COL_S + b * BN + 32, sr[1]);
-      tmem_wait_ld_tied(sr[0]);
-      tmem_wait_ld_tied(sr[1]);
-      float ext = fill;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          float x = __uint_as_float(sr[h2][k]);
-          if (need_mask && !(((vb[h2] >> k) & 1u) && (jb + 32 * h2 + k <= lim))) x = fill;
-          ext = cpos ? fmaxf(ext, x) : fminf(ext, x);
-        }
-      const float mx = (ext == fill) ? NEG_INF : ext * c;
-      const float m_new = fmaxf(m_used, mx);
-      const bool need = row_ok && m_new > m_used + 8.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? fast_ex2(m_used - m_new) : 1.f;
-        if (need) {
-          l *= alpha;
-          m_used = m_new;
-        }
-        if (j > 0) {
-          // O holds the PV of tiles < j once PV(j-1) has completed
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (j - 1) & 1, abort_flag)))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t o[32];
-            tmem_ld32(tO + c4 * 32, o);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(tO + c4 * 32, o);
-          }
-        }
-      }
-      const float nmu = (m_used == NEG_INF) ? 0.f : -m_used;
-      const float2 c2 = make_float2(c, c), nmu2 = make_float2(nmu, nmu);
-      float2 sum2 = make_float2(0.f, 0.f);
-      uint32_t pk[32];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(sr[h2][2 * k]), __uint_as_float(sr[h2][2 * k + 1])),
-                                       c2, nmu2);
-          float2 pr = make_float2(fast_ex2(t2.x), fast_ex2(t2.y));
-          if (need_mask) {
-            const int k0 = 32 * h2 + 2 * k;
-            if (!(((vb[h2] >> (2 * k)) & 1u) && (jb + k0 <= lim))) pr.x = 0.f;
-            if (!(((vb[h2] >> (2 * k + 1)) & 1u) && (jb + k0 + 1 <= lim))) pr.y = 0.f;
-          }
-          sum2 = __fadd2_rn(sum2, pr);
-          pk[h2 * 16 + k] = pack2h(pr.x, pr.y, bf16);
-        }
-      l += sum2.x + sum2.y;
-      tmem_st32(tbase + Sh::COL_S + b * BN, pk);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full + b);
-    }
-    // ---- this split's result
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (T - 1) & 1, abort_flag));
-    tc_fence_after();
-    if (ok) {
-      const int i = r / G, h = g * G + r % G;
-      const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
-      const size_t pi = (unit * p.nsplit + split) * QV + r;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        uint32_t o[32];
-        if (T > 0) {
-          tmem_ld32(tO + c4 * 32, o);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = 0u;
-        }
-        if (!row_ok) continue;
-        if (p.nsplit == 1) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) store_out(p.out, oi * D + c4 * 32 + k, __uint_as_float(o[k]) * inv, p.out_dtype);
-        } else if (m_used != NEG_INF) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + pi * D + c4 * 32);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]), __uint_as_float(o[4 * k + 2]),
-                                 __uint_as_float(o[4 * k + 3]));
-        }
-      }
-      if (row_ok) {
-        if (p.nsplit == 1) {
-          if (p.lse) p.lse[oi] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : NEG_INF;
-        } else {
-          p.part_ml[pi * 2] = m_used;
-          p.part_ml[pi * 2 + 1] = l;
-        }
-      }
-    }
+    dk_softmax<D, QVP>(p, sm, s_full, p_full, o_ready, abort_flag, tbase, T, cnt, j0, n_s, rows_g, unit, split, s, g);
   }
 
   tc_fence_before();
@@ -474,40 +530,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 1)
   __syncthreads();
   if (!*am_last) return;
   __threadfence();
-  const size_t pbase = unit * p.nsplit;
-  for (int qv = warp; qv < QV; qv += NWARP) {
-    float M = NEG_INF;
-    for (int k = lane; k < p.nsplit; k += 32) M = fmaxf(M, __ldcg(p.part_ml + ((pbase + k) * QV + qv) * 2));
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
-    const float Mu = (M == NEG_INF) ? 0.f : M;
-    float Ls = 0.f;
-    for (int k = lane; k < p.nsplit; k += 32) {
-      const float mk = __ldcg(p.part_ml + ((pbase + k) * QV + qv) * 2);
-      if (mk != NEG_INF) Ls = fmaf(__ldcg(p.part_ml + ((pbase + k) * QV + qv) * 2 + 1), fast_ex2(mk - Mu), Ls);
-    }
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, w);
-    if (lane == 0) {
-      fin[qv] = M;
-      fin[QROWS + qv] = Ls;
-    }
-  }
-  __syncthreads();
-  for (int t = threadIdx.x; t < QV * D; t += NWARP * 32) {
-    const int qv = t / D, d = t % D;
-    const float M = fin[qv], Ls = fin[QROWS + qv];
-    const float Mu = (M == NEG_INF) ? 0.f : M;
-    float Os = 0.f;
-    for (int k = 0; k < p.nsplit; ++k) {
-      const float mk = __ldcg(p.part_ml + ((pbase + k) * QV + qv) * 2);
-      if (mk != NEG_INF) Os = fmaf(__ldcg(p.part_o + ((pbase + k) * QV + qv) * D + d), fast_ex2(mk - Mu), Os);
-    }
-    const int i = qv / G, h = g * G + qv % G;
-    const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
-    store_out(p.out, oi * D + d, Ls > 0.f ? Os / Ls : 0.f, p.out_dtype);
-    if (p.lse && d == 0) p.lse[oi] = Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : NEG_INF;
-  }
+  merge_splits<D>(p, unit, QV, QV, s, g, reinterpret_cast<float*>(sm + Sh::OFF_K));
   if (threadIdx.x == 0) p.counters[unit] = 0u;
 }
 
@@ -555,27 +578,27 @@ bool dk_gather_map(CUtensorMap* m, const void* base, bool bf16, int D, int Hkv, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int QVP>
 int dk_occupancy() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (cached[dev] > 0) return cached[dev];
-  auto kern = fa_rows_decode_tc_kernel<D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkShape<D>::SMEM) != cudaSuccess)
+  auto kern = fa_rows_decode_tc_kernel<D, QVP>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkShape<D, QVP>::SMEM) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, dk::NWARP * 32, DkShape<D>::SMEM) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, dk::NWARP * 32, DkShape<D, QVP>::SMEM) != cudaSuccess) return 0;
   // tensor memory also bounds residency: 512 columns per SM
-  const int by_tmem = 512 / (int)DkShape<D>::TMEM_COLS;
+  const int by_tmem = 512 / (int)DkShape<D, QVP>::TMEM_COLS;
   n = n < by_tmem ? n : by_tmem;
   cached[dev] = n;
   return n;
 }
 
-template <int D>
+template <int D, int QVP>
 cudaError_t dk_launch(const DecodeParams& a, unsigned int* err, cudaStream_t st) {
-  if (dk_occupancy<D>() <= 0) return cudaErrorInvalidConfiguration;
+  if (dk_occupancy<D, QVP>() <= 0) return cudaErrorInvalidConfiguration;
   DecodeTcParams kp;
   kp.a = a;
   kp.err = err;
@@ -590,7 +613,7 @@ cudaError_t dk_launch(const DecodeParams& a, unsigned int* err, cudaStream_t st)
   if (!dk_gather_map(&gk, a.k, bf16, D, a.Hkv, a.R) || !dk_gather_map(&gv, a.v, bf16, D, a.Hkv, a.R))
     return cudaErrorInvalidValue;
   dim3 grid(a.nsplit, a.Hkv, a.S);
-  fa_rows_decode_tc_kernel<D><<<grid, dk::NWARP * 32, DkShape<D>::SMEM, st>>>(kp, tk, tv, gk, gv);
+  fa_rows_decode_tc_kernel<D, QVP><<<grid, dk::NWARP * 32, DkShape<D, QVP>::SMEM, st>>>(kp, tk, tv, gk, gv);
   return cudaGetLastError();
 }
 
@@ -601,13 +624,47 @@ bool decode_tc_supported(int D, int kind, int qv, int mask_kind) {
          mask_kind != FA_MASK_DENSE;
 }
 
-int decode_tc_occupancy(int D) { return D == 128 ? dk_occupancy<128>() : D == 256 ? dk_occupancy<256>() : 0; }
+static int qv_pow2(int qv) {
+  int q = 1;
+  while (q < qv) q <<= 1;
+  return q;
+}
+
+template <int D>
+int dk_occupancy_d(int qvp) {
+  switch (qvp) {
+    case 1: return dk_occupancy<D, 1>();
+    case 2: return dk_occupancy<D, 2>();
+    case 4: return dk_occupancy<D, 4>();
+    case 8: return dk_occupancy<D, 8>();
+    case 16: return dk_occupancy<D, 16>();
+    default: return dk_occupancy<D, 32>();
+  }
+}
+
+template <int D>
+cudaError_t dk_launch_d(int qvp, const DecodeParams& a, unsigned int* err, cudaStream_t st) {
+  switch (qvp) {
+    case 1: return dk_launch<D, 1>(a, err, st);
+    case 2: return dk_launch<D, 2>(a, err, st);
+    case 4: return dk_launch<D, 4>(a, err, st);
+    case 8: return dk_launch<D, 8>(a, err, st);
+    case 16: return dk_launch<D, 16>(a, err, st);
+    default: return dk_launch<D, 32>(a, err, st);
+  }
+}
+
+int decode_tc_occupancy(int D, int qv) {
+  if (D == 128) return dk_occupancy_d<128>(qv_pow2(qv));
+  if (D == 256) return dk_occupancy_d<256>(qv_pow2(qv));
+  return 0;
+}
 
 int decode_tc_tile() { return dk::BN; }
 
 cudaError_t decode_tc_launch(const DecodeParams& a, int D, unsigned int* err, cudaStream_t st) {
-  if (D == 128) return dk_launch<128>(a, err, st);
-  if (D == 256) return dk_launch<256>(a, err, st);
+  if (D == 128) return dk_launch_d<128>(qv_pow2(a.QV), a, err, st);
+  if (D == 256) return dk_launch_d<256>(qv_pow2(a.QV), a, err, st);
   return cudaErrorInvalidValue;
 }
 

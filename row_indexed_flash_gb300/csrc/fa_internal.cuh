@@ -23,6 +23,9 @@ constexpr int kPage = 64;  // rows per page of the INT8 scale layout
 // Upper bound on list positions handled by one decode CTA (its index stage).
 constexpr int kDecodeChunkMax = 2048;
 constexpr int kDecodeWarps = 4;
+// Splits per (slice, KV head): the in-launch merge stages every split's
+// (max, sum) for up to 32 rows in shared memory (64 KB at this cap).
+constexpr int kDecodeMaxSplits = 256;
 
 struct DecodeParams {
   const void* q;
@@ -64,7 +67,7 @@ int decode_occupancy(int D, int qvp, int kind);
 // Tensor-core decode (16-bit pools, D 128/256, up to 32 query vectors per KV
 // head, no dense mask).  Partials are laid out [unit][split][QV][D].
 bool decode_tc_supported(int D, int kind, int qv, int mask_kind);
-int decode_tc_occupancy(int D);
+int decode_tc_occupancy(int D, int qv);
 int decode_tc_tile();
 cudaError_t decode_tc_launch(const DecodeParams& p, int D, unsigned int* err, cudaStream_t st);
 
