@@ -126,31 +126,56 @@ _P = None
 
 def _oracle_unit(args):
     import oracle
-    s, g = args
+    s, g, qrows = args
     p = _P
     G = p.Hq // p.Hkv
-    q = oracle.widen(p.q[s:s + 1, :, g * G:(g + 1) * G], p.dtype)
+    if qrows is None:
+        q = oracle.widen(p.q[s:s + 1, :, g * G:(g + 1) * G], p.dtype)
+        extra = {}
+    else:
+        q = oracle.widen(p.q[s:s + 1, list(qrows), g * G:(g + 1) * G], p.dtype)
+        extra = dict(query_rows=list(qrows), n_query=p.Nq)
     oracle.attend_rows(q, p.k[:, g:g + 1], p.v[:, g:g + 1], p.kv_rows[s:s + 1], p.scale, causal=p.causal,
-                       kv_len=None if p.kv_len is None else p.kv_len[s:s + 1], kv_format=p.dtype)
+                       kv_len=None if p.kv_len is None else p.kv_len[s:s + 1], kv_format=p.dtype, **extra)
     return s, g
 
 
-def oracle_rate(p, units, passes: int, procs: int):
-    """Gathered-KV GB/s of the oracle over ``units`` (slice, KV head) pairs."""
+def oracle_units(p, prefill: bool, q_sample: int = 4):
+    """(slice, KV head, query rows) units of the oracle legs and the work of
+    each: gathered K+V bytes for decode, 4*D FLOPs per visible (query, key,
+    head) for prefill, whose units take ``q_sample`` query rows spread over the
+    chunk."""
+    units, work = [], []
+    G = p.Hq // p.Hkv
+    for s in range(p.S):
+        for g in range(p.Hkv):
+            if prefill:
+                qrows = tuple(sorted({(p.Nq - 1) * t // max(1, q_sample - 1) for t in range(q_sample)}))
+                vis = sum(max(0, min(p.L, p.L - p.Nq + i + 1)) if p.causal else p.L for i in qrows)
+                units.append((s, g, qrows))
+                work.append(4 * p.D * G * vis)
+            else:
+                units.append((s, g, None))
+                work.append(int((p.kv_rows[s] >= 0).sum()) * 2 * p.D * 2)
+    return units, work
+
+
+def oracle_rate(p, units, work, procs: int, min_seconds: float = 0.0, max_passes: int = 1):
+    """Work per second of the oracle over ``units``: whole passes over them,
+    repeated until ``min_seconds`` have elapsed (at most ``max_passes``)."""
     global _P
     _P = p
-    per_unit_bytes = {}
-    rb = 2 * p.D * 2
-    for s, g in units:
-        per_unit_bytes[(s, g)] = int((p.kv_rows[s] >= 0).sum()) * rb
     ctx = mp.get_context("fork")
+    passes = 0
     with ctx.Pool(procs) as pool:
         t0 = time.perf_counter()
-        for _ in range(passes):
+        while True:
             pool.map(_oracle_unit, units, chunksize=1)
-        dt = time.perf_counter() - t0
-    total = passes * sum(per_unit_bytes[u] for u in units)
-    return total / dt / 1e9, dt
+            passes += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_seconds or passes >= max_passes:
+                break
+    return passes * sum(work) / dt, dt, passes
 
 
 # ---------------------------------------------------------------------------
@@ -445,28 +470,30 @@ def main():
         if rank != 0:
             return
         p = build_problem(args.workload)
-        if args.workload.startswith("prefill"):
-            print(json.dumps({"impl": "reference", "unavailable": "the fp64 oracle arm is timed for decode only"}))
-            return
-        units = [(s, g) for s in range(p.S) for g in range(p.Hkv)][:procs]
+        prefill = args.workload.startswith("prefill")
+        unit, div = ("TFLOP/s", 1e12) if prefill else ("GB/s", 1e9)
+        units, work = oracle_units(p, prefill)
+        units, work = units[:procs], work[:procs]
         for _ in range(args.warmup):
-            oracle_rate(p, units[:1], 1, 1)
+            oracle_rate(p, units[:1], work[:1], 1)
         t0 = time.perf_counter()
-        moved = 0
+        done = 0.0
         for _ in range(args.steps):
-            r, dt = oracle_rate(p, units, 1, procs)
-            moved += r * dt * 1e9
+            r, dt, _ = oracle_rate(p, units, work, procs)
+            done += r * dt
         dt = time.perf_counter() - t0
-        v = moved / dt / 1e9
-        sample = f"{len(units)} of {p.S * p.Hkv} (slice, KV head) units per step, fp64 oracle, {procs} processes"
+        v = done / dt / div
+        what = "query rows" if prefill else "rows"
+        sample = (f"{len(units)} of {p.S * p.Hkv} (slice, KV head) units per step"
+                  + (f", {len(units[0][2])} {what} each" if prefill else "") + f", fp64 oracle, {procs} processes")
         print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": p.name},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": procs, "kind": "oracle",
+            "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": procs, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return
 
@@ -476,14 +503,17 @@ def main():
 
     p = build_problem(args.workload)
     cpu_baseline = None
-    if (rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload.startswith("prefill")
-            and p.kv_rows is not None):
-        units = [(s, g) for s in range(p.S) for g in range(p.Hkv)]
-        passes = 3
-        v, dt = oracle_rate(p, units, passes, procs)
-        cpu_baseline = {"value": round(v, 4), "unit": "GB/s", "cores": procs, "kind": "oracle",
-                        "sample": f"whole workload ({len(units)} (slice, KV head) units) x {passes} passes, "
-                                  f"{dt:.1f} s wall"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and p.kv_rows is not None:
+        # bounded sample of the same workload: whole passes over its units
+        # (prefill: a few query rows per unit) for about 10 s of CPU work
+        prefill = args.workload.startswith("prefill")
+        units, work = oracle_units(p, prefill)
+        v, dt, passes = oracle_rate(p, units, work, procs, min_seconds=10.0, max_passes=1000)
+        unit, div = ("TFLOP/s", 1e12) if prefill else ("GB/s", 1e9)
+        cpu_baseline = {"value": round(v / div, 6), "unit": unit, "cores": procs, "kind": "oracle",
+                        "sample": f"{len(units)} (slice, KV head) units"
+                                  + (f" x {len(units[0][2])} query rows" if prefill else " (whole workload)")
+                                  + f" x {passes} passes, {dt:.1f} s wall"}
     res = run_gpu(args, rank, world, p, cpu_baseline)
     if world > 1:
         import torch.distributed as dist
