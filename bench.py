@@ -428,7 +428,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             "unit": unit,
             "frac": round(achieved / peak, 4),
             "traffic": profiled_traffic(args.workload, kind),
-            "kernel": KERNEL_NAMES["decode_cc" if paged else kind],
+            "kernel": KERNEL_NAMES[kind],
             "kernel_ms": round(mean_launch_ms, 5),
             "work_per_launch": work,
         },

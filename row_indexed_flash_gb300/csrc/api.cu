@@ -139,7 +139,7 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
     return FA_OK;
   }
   int occ = 0;
-  if (pl->tc) occ = far::decode_tc_occupancy(a->D, (int)(qv < 1 ? 1 : qv));
+  if (pl->tc) occ = far::decode_tc_occupancy(a->D, kind, (int)(qv < 1 ? 1 : qv));
   else if (kind == far::KV_BF16) occ = far::decode_occupancy_bf16(a->D, qvp);
   else if (kind == far::KV_F16) occ = far::decode_occupancy_f16(a->D, qvp);
   else if (kind == far::KV_I8) occ = far::decode_occupancy_i8(a->D, qvp);
@@ -282,7 +282,7 @@ fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_st
   const int kind = kv_kind(a->kv_dtype);
   if (pl.tc) {
     unsigned int* err = pl.ws > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + pl.off_err) : nullptr;
-    e = far::decode_tc_launch(p, a->D, err, s);
+    e = far::decode_tc_launch(p, a->D, kind, err, s);
   } else if (kind == far::KV_BF16) {
     e = far::decode_launch_bf16(p, a->D, pl.qvp, s);
   } else if (kind == far::KV_F16) {

@@ -25,6 +25,11 @@
 //                  only moves when it grows by more than 2^8 (then rescales O in
 //                  place), writes P over S as 16-bit pairs, and at the end
 //                  writes the split's (max, sum, O) or the final output.
+// INT8 pools (codes with one fp16 scale per (row, KV head)) take the same
+// pipeline: the producers gather the codes into the upper half of the stage's
+// tile, widen them in place to Q's 16-bit type (exact: |code| <= 127), and
+// store the rows' scales beside the tile; the softmax folds the K scale into
+// the logit and the V scale into P, so the MMAs see plain 16-bit operands.
 // The last CTA to finish a (slice, KV head) merges the splits (an arrival
 // counter in the workspace, reset by that CTA; nothing waits on it).
 // Every pipeline wait is bounded in time and reported through an error word.
@@ -48,7 +53,8 @@ constexpr int NWARP = 2 + NPROD;   // softmax, producers, MMA
 constexpr int MMA_WARP = 1 + NPROD;
 }  // namespace dk
 
-template <int D, int QVP>
+// KQ: 0 = 16-bit pool, 1 = INT8 codes + fp16 scales.
+template <int D, int QVP, int KQ>
 struct DkShape {
   static constexpr int KT = D / 64;                  // 128-byte K atoms per row
   static constexpr int QATOM = dk::QROWS * 128;      // bytes of one atom column of the Q tile
@@ -62,18 +68,25 @@ struct DkShape {
   // q_full, kv_full[NST], kv_empty[NST], s_full[2], p_full[2], o_ready, drain
   static constexpr int NBAR = 1 + 2 * dk::NST + 2 + 2 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_SS = ((OFF_MISC + 16 + 127) / 128) * 128;   // S rows of the real query vectors, fp32
-  static constexpr int OFF_SP = OFF_SS + QVP * dk::BN * 4;             // P rows, packed 16-bit pairs
-  static constexpr int SMEM_USED = OFF_SP + QVP * dk::BN * 2;
+  // S rows of the real query vectors (fp32), then in the same place their P
+  // rows (packed 16-bit pairs: BN/2 words of P_hi, BN/2 of P_lo)
+  static constexpr int OFF_SS = ((OFF_MISC + 16 + 127) / 128) * 128;
+  static constexpr int OFF_SC = OFF_SS + QVP * dk::BN * 4;           // [NST][K, V][BN] fp32 scales (KQ)
+  static constexpr int SMEM_USED = OFF_SC + (KQ ? dk::NST * 2 * dk::BN * 4 : 0);
+  // code bytes of one (row, head), 16-byte chunks of them, first tile atom holding them (KQ)
+  static constexpr int CB = KQ ? D : 2 * D;
+  static constexpr int CPRQ = CB / 16;
+  static constexpr int A0 = KT - (CB + 127) / 128;
   static constexpr int SMEM = SMEM_USED + 1024;
   static constexpr uint32_t TMEM_COLS = (2 * dk::BN + D) <= 256 ? 256 : 512;
   static constexpr uint32_t COL_S = 0;               // S0, S1: 64 columns each
   static constexpr uint32_t COL_O = 2 * dk::BN;      // O: D columns
   // vector (16-byte) accesses: Q/K/V tiles (1024-byte swizzle atoms), S and P rows
   static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && TILE % 1024 == 0, "tiles must be 1024-byte aligned");
-  static_assert(OFF_SS % 16 == 0 && OFF_SP % 16 == 0 && (dk::BN * 4) % 16 == 0 && (dk::BN * 2) % 16 == 0,
-                "S/P rows must be 16-byte aligned");
+  static_assert(OFF_SS % 16 == 0 && (dk::BN * 4) % 16 == 0, "S/P rows must be 16-byte aligned");
   static_assert(OFF_BAR % 8 == 0, "mbarriers must be 8-byte aligned");
+  static_assert(OFF_SC % 16 == 0, "scales must be 16-byte aligned");
+  static_assert(!KQ || (A0 >= KT / 2 && CPRQ % 2 == 0), "codes must sit in the tile's upper half");
 };
 
 struct DecodeTcParams {
@@ -93,6 +106,30 @@ __device__ __forceinline__ uint32_t pack2h(float lo, float hi, bool bf16) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Four INT8 codes (one word) -> four 16-bit values of Q's type, exact.
+// bf16: (code + 128) is placed in the low mantissa bits of 2^23 and 2^23 + 128
+// subtracted, which leaves the code as an fp32 whose low 16 bits are zero, so
+// its upper half is the bf16 value.  f16: (code + 128) is placed in the low
+// mantissa bits of 1024 (0x6400) and 1152 subtracted.
+__device__ __forceinline__ uint2 widen_i8x4(uint32_t w, bool bf16) {
+  const uint32_t x = w ^ 0x80808080u;
+  if (bf16) {
+    const float2 lo = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650u)),
+                                             __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7651u))),
+                                 make_float2(-8388736.0f, -8388736.0f));
+    const float2 hi = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7652u)),
+                                             __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7653u))),
+                                 make_float2(-8388736.0f, -8388736.0f));
+    return make_uint2(__byte_perm(__float_as_uint(lo.x), __float_as_uint(lo.y), 0x7632u),
+                      __byte_perm(__float_as_uint(hi.x), __float_as_uint(hi.y), 0x7632u));
+  }
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));   // 1152
+  uint32_t a = __byte_perm(x, 0x64646464u, 0x4140u), b = __byte_perm(x, 0x64646464u, 0x4342u);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&ha), *reinterpret_cast<uint32_t*>(&hb));
+}
+
 __device__ __forceinline__ void wait_drain(uint64_t* b, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(b, parity)) {
@@ -104,12 +141,13 @@ __device__ __forceinline__ void wait_drain(uint64_t* b, uint32_t parity) {
 
 // The softmax role (warp 0) of fa_rows_decode_tc_kernel for QVP = the query
 // vector count rounded up to a power of two.
-template <int D, int QVP>
+template <int D, int QVP, int KQ>
 __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char* sm, uint64_t* s_full, uint64_t* p_full,
-                                           uint64_t* o_ready, volatile int* abort_flag, uint32_t tbase, int T, int cnt,
-                                           int j0, int n_s, const int32_t* rows_g, size_t unit, int split, int s,
-                                           int g) {
-  using Sh = DkShape<D, QVP>;
+                                           uint64_t* o_ready, uint64_t* o_done, uint64_t* kv_full,
+                                           volatile int* abort_flag,
+                                           uint32_t tbase, int T, int cnt, int j0, int n_s, const int32_t* rows_g,
+                                           size_t unit, int split, int s, int g) {
+  using Sh = DkShape<D, QVP, KQ>;
   using namespace dk;
   const float NEG_INF = __int_as_float(0xff800000);
   const int lane = threadIdx.x & 31;
@@ -121,7 +159,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
     // the exponentials and reductions use the whole warp.  P goes back the
     // same way and is stored over S by the lanes that own its rows.
     float* sS = reinterpret_cast<float*>(sm + Sh::OFF_SS);
-    uint32_t* sP = reinterpret_cast<uint32_t*>(sm + Sh::OFF_SP);
+    uint32_t* sP = reinterpret_cast<uint32_t*>(sm + Sh::OFF_SS);   // replaces S once every lane has read it
     constexpr int qvp = QVP;
     constexpr int LPR = 32 / QVP, CPL = BN / LPR;   // lanes per row, columns per lane
     const int row = lane / LPR, part = lane % LPR;
@@ -130,6 +168,9 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
     const float c = p.qscale;
     const uint32_t tO = tbase + Sh::COL_O;
     float m_used = NEG_INF, l = 0.f;            // state of row `row`, held by its LPR lanes
+    // INT8 with f16 queries: P * s_v reaches 256 * 65504 / 127, beyond f16, so
+    // it is carried as P * s_v * 2^-8 and O multiplied back by 2^8 at the end
+    const float pv_scale = (KQ != 0 && !bf16) ? 0.00390625f : 1.f;
     bool ok = true;
     int nxt0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // list entries of the next tile
     int nxt1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
@@ -145,6 +186,13 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
       }
       const int jb = j0 + j * BN;   // list position of column 0
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag)))) break;
+      const float* scK = reinterpret_cast<const float*>(sm + Sh::OFF_SC) + (j % NST) * 2 * BN;
+      if constexpr (KQ != 0) {
+        // the producers' scale stores are ordered before this read by the
+        // stage's full barrier (its phase for tile j stays complete until this
+        // warp releases P of tile j)
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(kv_full + j % NST, (j / NST) & 1, abort_flag)))) break;
+      }
       tc_fence_after();
       {
         uint32_t sr[2][32];
@@ -173,7 +221,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
 #pragma unroll
       for (int k = 0; k < CPL; ++k) {
         const int col = c0 + k;
-        float v = row_ok ? sS[row * BN + col] * c : NEG_INF;
+        float v = row_ok ? sS[row * BN + col] * (KQ ? c * scK[col] : c) : NEG_INF;
         if (!(((vbits >> col) & 1ull) && (jb + col <= lim))) v = NEG_INF;
         x[k] = v;
         mx = fmaxf(mx, v);
@@ -205,20 +253,44 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
       }
       const float mu = (m_used == NEG_INF) ? 0.f : m_used;
       float sum = 0.f;
+      __syncwarp();   // every lane's S reads are done before P overwrites them
+      // P (times the V scale for INT8) goes to the tensor core as two 16-bit
+      // terms, P_hi = rn(P) and P_lo = rn(P - P_hi), so the PV product keeps
+      // about 16 significant bits of P instead of 8 (bf16)
 #pragma unroll
       for (int k = 0; k < CPL; k += 2) {
         const float p0 = fast_ex2(x[k] - mu), p1 = fast_ex2(x[k + 1] - mu);
         sum += p0 + p1;
-        if (row_ok) sP[row * (BN / 2) + (c0 + k) / 2] = pack2h(p0, p1, bf16);
+        float a0 = p0, a1 = p1;
+        if constexpr (KQ != 0) {   // the V scale of each column rides on P (times 2^-8 in f16)
+          a0 *= scK[BN + c0 + k] * pv_scale;
+          a1 *= scK[BN + c0 + k + 1] * pv_scale;
+        }
+        const uint32_t hi = pack2h(a0, a1, bf16);
+        float h0, h1;
+        if (bf16) {
+          h0 = __uint_as_float(hi << 16);
+          h1 = __uint_as_float(hi & 0xffff0000u);
+        } else {
+          const float2 hf = f16x2_to_f2(hi);
+          h0 = hf.x;
+          h1 = hf.y;
+        }
+        const uint32_t lo = pack2h(a0 - h0, a1 - h1, bf16);
+        if (row_ok) {
+          sP[row * BN + (c0 + k) / 2] = hi;
+          sP[row * BN + BN / 2 + (c0 + k) / 2] = lo;
+        }
       }
 #pragma unroll
       for (int w = 1; w < LPR; w <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
       l += sum;
       __syncwarp();
-      {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
         if (lane < QV) {
-          const uint4* src = reinterpret_cast<const uint4*>(sP + lane * (BN / 2));
+          const uint4* src = reinterpret_cast<const uint4*>(sP + lane * BN + half * (BN / 2));
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint4 w4 = src[k];
@@ -228,8 +300,9 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
 #pragma unroll
           for (int k = 0; k < 32; ++k) pk[k] = 0u;
         }
-        tmem_st32(tbase + Sh::COL_S + b * BN, pk);
+        tmem_st32_nowait(tbase + Sh::COL_S + b * BN + half * (BN / 2), pk);
       }
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + b);
@@ -237,7 +310,11 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
     // ---- this split's result: lane r < QV owns O row r; its (m, l) come from lane r*LPR
     const float m_r = __shfl_sync(0xffffffffu, m_used, (lane % qvp) * LPR);
     const float l_r = __shfl_sync(0xffffffffu, l, (lane % qvp) * LPR);
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (T - 1) & 1, abort_flag));
+    // O is final once every PV is done: the MMA warp commits `o_done` (its
+    // drain barrier, one phase) after issuing the last one.  o_ready cannot
+    // serve here: the last S only implies PV of tile T-3, so that barrier may
+    // be two phases behind, where a parity wait cannot tell the phases apart.
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag));
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
@@ -246,7 +323,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
       const int i = r / G, h = g * G + r % G;
       const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
       const size_t pi = (unit * p.nsplit + split) * QV + r;
-      const float inv = l_r > 0.f ? 1.f / l_r : 0.f;
+      const float inv = l_r > 0.f ? 1.f / l_r / pv_scale : 0.f;
 #pragma unroll
       for (int c4 = 0; c4 < D / 32; ++c4) {
         uint32_t o[32];
@@ -262,10 +339,11 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
           for (int k = 0; k < 32; ++k) store_out(p.out, oi * D + c4 * 32 + k, __uint_as_float(o[k]) * inv, p.out_dtype);
         } else if (m_r != NEG_INF) {
           float4* dst = reinterpret_cast<float4*>(p.part_o + pi * D + c4 * 32);
+          const float os = 1.f / pv_scale;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]), __uint_as_float(o[4 * k + 2]),
-                                 __uint_as_float(o[4 * k + 3]));
+            dst[k] = make_float4(__uint_as_float(o[4 * k]) * os, __uint_as_float(o[4 * k + 1]) * os,
+                                 __uint_as_float(o[4 * k + 2]) * os, __uint_as_float(o[4 * k + 3]) * os);
         }
       }
       if (own) {
@@ -279,12 +357,11 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
     }
 }
 
-template <int D, int QVP>
+template <int D, int QVP, int KQ>
 __global__ void __launch_bounds__(dk::NWARP * 32, 2)
     fa_rows_decode_tc_kernel(const DecodeTcParams kp, const __grid_constant__ CUtensorMap tk,
-                             const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap gk,
-                             const __grid_constant__ CUtensorMap gv) {
-  using Sh = DkShape<D, QVP>;
+                             const __grid_constant__ CUtensorMap tv) {
+  using Sh = DkShape<D, QVP, KQ>;
   using namespace dk;
   const DecodeParams& p = kp.a;
   const float NEG_INF = __int_as_float(0xff800000);
@@ -372,8 +449,45 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
     int nrow0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // next tile's rows, one tile ahead
     int nrow1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
     int published = 0;
-    auto publish = [&](int t) {
+    // KQ: this warp's scale loads (entry pw*ROWS + lane%16, K for lanes < 16,
+    // V above) of the two tiles in flight: sc_a the older, sc_b the newer
+    // (raw fp16 bits: converted only at publish, so no instruction waits on the load before then)
+    unsigned short sc_a = 0, sc_b = 0;
+    auto publish = [&](int t, unsigned short sc) {
       if ((gathered >> (t & 31)) & 1u) {
+        if constexpr (KQ != 0) {
+          // widen this warp's rows of the stage in place: every lane reads
+          // the code chunks it copied itself, then writes their 16-bit values
+          constexpr int NIT = ROWS * Sh::CPRQ / 32;
+#pragma unroll
+          for (int mat = 0; mat < 2; ++mat) {
+            unsigned char* tile = sm + (mat ? Sh::OFF_V : Sh::OFF_K) + (t % NST) * Sh::TILE;
+            uint4 cw[NIT];
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) {
+              const int f = it * 32 + lane;
+              const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
+              cw[it] = *reinterpret_cast<const uint4*>(tile + (Sh::A0 + c / 8) * Sh::KV_ATOM + e * 128 +
+                                                       (((c & 7) ^ (e & 7)) << 4));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) {
+              const int f = it * 32 + lane;
+              const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
+              // 16 codes = columns 16c .. 16c+15: two 16-byte chunks of atom c / 4
+              const uint2 a = widen_i8x4(cw[it].x, bf16), b = widen_i8x4(cw[it].y, bf16);
+              const uint2 cc = widen_i8x4(cw[it].z, bf16), d = widen_i8x4(cw[it].w, bf16);
+              unsigned char* row = tile + (c / 4) * Sh::KV_ATOM + e * 128;
+              const int k0 = 2 * (c % 4);
+              *reinterpret_cast<uint4*>(row + ((k0 ^ (e & 7)) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+              *reinterpret_cast<uint4*>(row + (((k0 + 1) ^ (e & 7)) << 4)) = make_uint4(cc.x, cc.y, d.x, d.y);
+            }
+            __syncwarp();
+          }
+          reinterpret_cast<float*>(sm + Sh::OFF_SC)[(t % NST) * 2 * BN + (lane >> 4) * BN + pw * ROWS + (lane & 15)] =
+              __half2float(__ushort_as_half(sc));
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(kv_full + t % NST);
@@ -385,7 +499,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       // it before it can free that stage
       if (j >= NST - 1) {
         cp_async_wait<NST - 2>();
-        publish(j - (NST - 1));
+        publish(j - (NST - 1), sc_a);
         published = j - (NST - 1) + 1;
       }
       if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
@@ -398,11 +512,39 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
         nrow0 = pos < cnt ? __ldg(rows_g + pos) : -1;
         nrow1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
       }
+      unsigned char* Ks = sm + Sh::OFF_K + st * Sh::TILE;
+      unsigned char* Vs = sm + Sh::OFF_V + st * Sh::TILE;
+      if constexpr (KQ != 0) {
+        // codes of this warp's rows -> the upper atoms of row e, chunk c swizzled as the tile
+#pragma unroll
+        for (int it = 0; it < ROWS * Sh::CPRQ / 32; ++it) {
+          const int f = it * 32 + lane;
+          const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
+          const int ra = __shfl_sync(0xffffffffu, rows[0], e & 31);
+          const int rb = __shfl_sync(0xffffffffu, rows[1], e & 31);
+          const int r = e < 32 ? ra : rb;
+          const bool okr = r >= 0;
+          const size_t go = ((size_t)(okr ? r : 0) * p.Hkv + g) * Sh::CB + c * 16;
+          const uint32_t so = (Sh::A0 + c / 8) * Sh::KV_ATOM + e * 128 + (((c & 7) ^ (e & 7)) << 4);
+          cp_async16(Ks + so, kb + go, okr);
+          cp_async16(Vs + so, vb + go, okr);
+        }
+        {
+          const int e = pw * ROWS + (lane & 15);
+          const int ra = __shfl_sync(0xffffffffu, rows[0], e & 31);
+          const int rb = __shfl_sync(0xffffffffu, rows[1], e & 31);
+          const int r = e < 32 ? ra : rb;
+          const uint16_t* sc = (lane >> 4) ? p.v_scale : p.k_scale;
+          sc_a = sc_b;
+          sc_b = r >= 0 ? __ldg(sc + ((size_t)(r >> 6) * p.Hkv + g) * kPage + (r & 63)) : (unsigned short)0;
+        }
+        gathered |= 1u << (j & 31);
+        cp_async_commit();
+        continue;
+      }
       const int r0 = __shfl_sync(0xffffffffu, rows[0], 0);
       bool contig = rows[0] >= 0 && rows[0] == r0 + lane && rows[1] >= 0 && rows[1] == r0 + lane + 32;
       contig = __all_sync(0xffffffffu, contig) && kp.tma_kv;
-      unsigned char* Ks = sm + Sh::OFF_K + st * Sh::TILE;
-      unsigned char* Vs = sm + Sh::OFF_V + st * Sh::TILE;
       if (contig) {
         if (pw == 0) {
           if (lane == 0) {
@@ -441,8 +583,11 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       cp_async_commit();   // one group per tile (empty for TMA tiles)
     }
     cp_async_wait<0>();
-    if (!*abort_flag)
-      for (int t = published; t < T; ++t) publish(t);
+    if (!*abort_flag) {
+      // at most two tiles are left: T-2 (scales in sc_a) and T-1 (sc_b)
+      if (T - published >= 2) publish(T - 2, sc_a);
+      if (T - published >= 1) publish(T - 1, sc_b);
+    }
     if (pw == 0 && lane == 0 && *abort_flag) {
       if (tma_pend & 1u) wait_drain(kv_full + 0, use0 & 1);
       if (tma_pend & 2u) wait_drain(kv_full + 1, use1 & 1);
@@ -482,10 +627,12 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
         if (npv < nqk && mbar_test_wait(p_full + (npv & 1), (npv >> 1) & 1)) {
           const int pst = npv % NST, pb = npv & 1;
           tc_fence_after();
+          // O += P_hi V + P_lo V (P_hi in S columns 0..BN/2-1, P_lo after it)
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
+          for (int kk = 0; kk < 2 * (BN / 16); ++kk)
             mma_ts(tO, tbase + Sh::COL_S + pb * BN + kk * 8,
-                   sdesc_sw128(sV + pst * Sh::TILE + kk * 2048, Sh::KV_ATOM, 1024), id_pv, npv > 0 || kk > 0);
+                   sdesc_sw128(sV + pst * Sh::TILE + (kk % (BN / 16)) * 2048, Sh::KV_ATOM, 1024), id_pv,
+                   npv > 0 || kk > 0);
           tc_commit(kv_empty + pst);
           tc_commit(o_ready);
           ++npv;
@@ -507,7 +654,8 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
     }
   } else {
     // ------------------------------------------------------------ softmax (warp 0)
-    dk_softmax<D, QVP>(p, sm, s_full, p_full, o_ready, abort_flag, tbase, T, cnt, j0, n_s, rows_g, unit, split, s, g);
+    dk_softmax<D, QVP, KQ>(p, sm, s_full, p_full, o_ready, drain, kv_full, abort_flag, tbase, T, cnt, j0, n_s, rows_g, unit,
+                           split, s, g);
   }
 
   tc_fence_before();
@@ -564,64 +712,49 @@ bool dk_map(CUtensorMap* m, const void* base, bool bf16, int D, int Hkv, long lo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D view of a pool [R][Hkv][D] as [R * Hkv] rows of D, box 64 columns x one
-// row (the shape tile::gather4 takes).
-bool dk_gather_map(CUtensorMap* m, const void* base, bool bf16, int D, int Hkv, long long R) {
-  auto enc = dk_encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)R * (cuuint64_t)Hkv};
-  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t es[2] = {1, 1};
-  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
-             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int D, int QVP>
+template <int D, int QVP, int KQ>
 int dk_occupancy() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (cached[dev] > 0) return cached[dev];
-  auto kern = fa_rows_decode_tc_kernel<D, QVP>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkShape<D, QVP>::SMEM) != cudaSuccess)
-    return 0;
+  using Sh = DkShape<D, QVP, KQ>;
+  auto kern = fa_rows_decode_tc_kernel<D, QVP, KQ>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, dk::NWARP * 32, DkShape<D, QVP>::SMEM) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, dk::NWARP * 32, Sh::SMEM) != cudaSuccess) return 0;
   // tensor memory also bounds residency: 512 columns per SM
-  const int by_tmem = 512 / (int)DkShape<D, QVP>::TMEM_COLS;
+  const int by_tmem = 512 / (int)Sh::TMEM_COLS;
   n = n < by_tmem ? n : by_tmem;
   cached[dev] = n;
   return n;
 }
 
-template <int D, int QVP>
+template <int D, int QVP, int KQ>
 cudaError_t dk_launch(const DecodeParams& a, unsigned int* err, cudaStream_t st) {
-  if (dk_occupancy<D, QVP>() <= 0) return cudaErrorInvalidConfiguration;
+  if (dk_occupancy<D, QVP, KQ>() <= 0) return cudaErrorInvalidConfiguration;
   DecodeTcParams kp;
   kp.a = a;
   kp.err = err;
-  kp.tma_kv = a.R >= dk::BN;
+  // TMA tile loads of contiguous runs (16-bit pools only: codes are widened by the producers)
+  kp.tma_kv = KQ == 0 && a.R >= dk::BN;
   const bool bf16 = a.q_bf16 != 0;
-  CUtensorMap tk, tv, gk, gv;
+  CUtensorMap tk, tv;
   memset(&tk, 0, sizeof(tk));
   memset(&tv, 0, sizeof(tv));
   if (kp.tma_kv) {
     if (!dk_map(&tk, a.k, bf16, D, a.Hkv, a.R) || !dk_map(&tv, a.v, bf16, D, a.Hkv, a.R)) return cudaErrorInvalidValue;
   }
-  if (!dk_gather_map(&gk, a.k, bf16, D, a.Hkv, a.R) || !dk_gather_map(&gv, a.v, bf16, D, a.Hkv, a.R))
-    return cudaErrorInvalidValue;
   dim3 grid(a.nsplit, a.Hkv, a.S);
-  fa_rows_decode_tc_kernel<D, QVP><<<grid, dk::NWARP * 32, DkShape<D, QVP>::SMEM, st>>>(kp, tk, tv, gk, gv);
+  fa_rows_decode_tc_kernel<D, QVP, KQ><<<grid, dk::NWARP * 32, DkShape<D, QVP, KQ>::SMEM, st>>>(kp, tk, tv);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool decode_tc_supported(int D, int kind, int qv, int mask_kind) {
-  return (D == 128 || D == 256) && (kind == KV_BF16 || kind == KV_F16) && qv >= 1 && qv <= dk::QROWS &&
-         mask_kind != FA_MASK_DENSE;
+  return (D == 128 || D == 256) && (kind == KV_BF16 || kind == KV_F16 || kind == KV_I8) && qv >= 1 &&
+         qv <= dk::QROWS && mask_kind != FA_MASK_DENSE;
 }
 
 static int qv_pow2(int qv) {
@@ -630,41 +763,45 @@ static int qv_pow2(int qv) {
   return q;
 }
 
-template <int D>
+template <int D, int KQ>
 int dk_occupancy_d(int qvp) {
   switch (qvp) {
-    case 1: return dk_occupancy<D, 1>();
-    case 2: return dk_occupancy<D, 2>();
-    case 4: return dk_occupancy<D, 4>();
-    case 8: return dk_occupancy<D, 8>();
-    case 16: return dk_occupancy<D, 16>();
-    default: return dk_occupancy<D, 32>();
+    case 1: return dk_occupancy<D, 1, KQ>();
+    case 2: return dk_occupancy<D, 2, KQ>();
+    case 4: return dk_occupancy<D, 4, KQ>();
+    case 8: return dk_occupancy<D, 8, KQ>();
+    case 16: return dk_occupancy<D, 16, KQ>();
+    default: return dk_occupancy<D, 32, KQ>();
   }
 }
 
-template <int D>
+template <int D, int KQ>
 cudaError_t dk_launch_d(int qvp, const DecodeParams& a, unsigned int* err, cudaStream_t st) {
   switch (qvp) {
-    case 1: return dk_launch<D, 1>(a, err, st);
-    case 2: return dk_launch<D, 2>(a, err, st);
-    case 4: return dk_launch<D, 4>(a, err, st);
-    case 8: return dk_launch<D, 8>(a, err, st);
-    case 16: return dk_launch<D, 16>(a, err, st);
-    default: return dk_launch<D, 32>(a, err, st);
+    case 1: return dk_launch<D, 1, KQ>(a, err, st);
+    case 2: return dk_launch<D, 2, KQ>(a, err, st);
+    case 4: return dk_launch<D, 4, KQ>(a, err, st);
+    case 8: return dk_launch<D, 8, KQ>(a, err, st);
+    case 16: return dk_launch<D, 16, KQ>(a, err, st);
+    default: return dk_launch<D, 32, KQ>(a, err, st);
   }
 }
 
-int decode_tc_occupancy(int D, int qv) {
-  if (D == 128) return dk_occupancy_d<128>(qv_pow2(qv));
-  if (D == 256) return dk_occupancy_d<256>(qv_pow2(qv));
+int decode_tc_occupancy(int D, int kind, int qv) {
+  const int q = qv_pow2(qv);
+  const bool quant = kind == KV_I8;
+  if (D == 128) return quant ? dk_occupancy_d<128, 1>(q) : dk_occupancy_d<128, 0>(q);
+  if (D == 256) return quant ? dk_occupancy_d<256, 1>(q) : dk_occupancy_d<256, 0>(q);
   return 0;
 }
 
 int decode_tc_tile() { return dk::BN; }
 
-cudaError_t decode_tc_launch(const DecodeParams& a, int D, unsigned int* err, cudaStream_t st) {
-  if (D == 128) return dk_launch_d<128>(qv_pow2(a.QV), a, err, st);
-  if (D == 256) return dk_launch_d<256>(qv_pow2(a.QV), a, err, st);
+cudaError_t decode_tc_launch(const DecodeParams& a, int D, int kind, unsigned int* err, cudaStream_t st) {
+  const int q = qv_pow2(a.QV);
+  const bool quant = kind == KV_I8;
+  if (D == 128) return quant ? dk_launch_d<128, 1>(q, a, err, st) : dk_launch_d<128, 0>(q, a, err, st);
+  if (D == 256) return quant ? dk_launch_d<256, 1>(q, a, err, st) : dk_launch_d<256, 0>(q, a, err, st);
   return cudaErrorInvalidValue;
 }
 

@@ -64,12 +64,12 @@ cudaError_t decode_launch(const DecodeParams& p, int D, int qvp, int kind, cudaS
 // CTAs of the instance that fit on one SM (cached).
 int decode_occupancy(int D, int qvp, int kind);
 
-// Tensor-core decode (16-bit pools, D 128/256, up to 32 query vectors per KV
-// head, no dense mask).  Partials are laid out [unit][split][QV][D].
+// Tensor-core decode (16-bit or INT8 pools, D 128/256, up to 32 query
+// vectors per KV head, no dense mask).  Partials are laid out [unit][split][QV][D].
 bool decode_tc_supported(int D, int kind, int qv, int mask_kind);
-int decode_tc_occupancy(int D, int qv);
+int decode_tc_occupancy(int D, int kind, int qv);
 int decode_tc_tile();
-cudaError_t decode_tc_launch(const DecodeParams& p, int D, unsigned int* err, cudaStream_t st);
+cudaError_t decode_tc_launch(const DecodeParams& p, int D, int kind, unsigned int* err, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // prefill
