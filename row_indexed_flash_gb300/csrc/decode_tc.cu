@@ -69,9 +69,17 @@ struct DkShape {
   static constexpr int NBAR = 1 + 2 * dk::NST + 2 + 2 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // S rows of the real query vectors (fp32), then in the same place their P
-  // rows (packed 16-bit pairs: BN/2 words of P_hi, BN/2 of P_lo)
+  // rows (packed 16-bit pairs: BN/2 words of P_hi, BN/2 of P_lo).  The softmax
+  // spreads each row over LPR lanes that take interleaved column pairs, so the
+  // row strides are padded to put the rows of one access on distinct banks:
+  // SSTR = 2*LPR (mod 32) for the 8-byte S reads, SPP = LPR (mod 32) for the
+  // 4-byte P writes.
+  static constexpr int LPR = 32 / QVP;
+  static constexpr int SSTR = dk::BN + (2 * LPR) % 32;
+  static constexpr int SPP = dk::BN + LPR % 32;
+  static constexpr int SROW = SSTR > SPP ? SSTR : SPP;
   static constexpr int OFF_SS = ((OFF_MISC + 16 + 127) / 128) * 128;
-  static constexpr int OFF_SC = OFF_SS + QVP * dk::BN * 4;           // [NST][K, V][BN] fp32 scales (KQ)
+  static constexpr int OFF_SC = OFF_SS + ((QVP * SROW * 4 + 15) / 16) * 16;   // [NST][K, V][BN] fp32 scales (KQ)
   static constexpr int SMEM_USED = OFF_SC + (KQ ? dk::NST * 2 * dk::BN * 4 : 0);
   // code bytes of one (row, head), 16-byte chunks of them, first tile atom holding them (KQ)
   static constexpr int CB = KQ ? D : 2 * D;
@@ -161,7 +169,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
     float* sS = reinterpret_cast<float*>(sm + Sh::OFF_SS);
     uint32_t* sP = reinterpret_cast<uint32_t*>(sm + Sh::OFF_SS);   // replaces S once every lane has read it
     constexpr int qvp = QVP;
-    constexpr int LPR = 32 / QVP, CPL = BN / LPR;   // lanes per row, columns per lane
+    constexpr int LPR = Sh::LPR, CPL = BN / LPR;   // lanes per row, columns per lane
     const int row = lane / LPR, part = lane % LPR;
     const bool row_ok = row < QV;               // this lane's share is of a real row
     const int lim = (p.mask_kind == FA_MASK_CAUSAL) ? n_s - p.Nq + row / G : n_s - 1;
@@ -201,30 +209,36 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
         tmem_wait_ld_tied(sr[0]);
         tmem_wait_ld_tied(sr[1]);
         if (lane < QV) {
-          float4* dst = reinterpret_cast<float4*>(sS + lane * BN);
+          float2* dst = reinterpret_cast<float2*>(sS + lane * Sh::SSTR);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(sr[0][4 * k]), __uint_as_float(sr[0][4 * k + 1]),
-                                 __uint_as_float(sr[0][4 * k + 2]), __uint_as_float(sr[0][4 * k + 3]));
+          for (int k = 0; k < 16; ++k) dst[k] = make_float2(__uint_as_float(sr[0][2 * k]), __uint_as_float(sr[0][2 * k + 1]));
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[8 + k] = make_float4(__uint_as_float(sr[1][4 * k]), __uint_as_float(sr[1][4 * k + 1]),
-                                     __uint_as_float(sr[1][4 * k + 2]), __uint_as_float(sr[1][4 * k + 3]));
+          for (int k = 0; k < 16; ++k)
+            dst[16 + k] = make_float2(__uint_as_float(sr[1][2 * k]), __uint_as_float(sr[1][2 * k + 1]));
         }
       }
       __syncwarp();
-      // this lane's CPL columns of row `row`, scaled into log2 units, masked
-      const int c0 = part * CPL;
+      // this lane's column pairs 2*(part + LPR*kk) of row `row`, scaled into
+      // log2 units, masked
       const unsigned long long vbits = ((unsigned long long)vb[1] << 32) | vb[0];
       float x[CPL];
       float mx = NEG_INF;
 #pragma unroll
-      for (int k = 0; k < CPL; ++k) {
-        const int col = c0 + k;
-        float v = row_ok ? sS[row * BN + col] * (KQ ? c * scK[col] : c) : NEG_INF;
-        if (!(((vbits >> col) & 1ull) && (jb + col <= lim))) v = NEG_INF;
-        x[k] = v;
-        mx = fmaxf(mx, v);
+      for (int kk = 0; kk < CPL / 2; ++kk) {
+        const int col = 2 * (part + LPR * kk);
+        const float2 sv = *reinterpret_cast<const float2*>(sS + row * Sh::SSTR + col);
+        float c0s = c, c1s = c;
+        if constexpr (KQ != 0) {
+          const float2 sk = *reinterpret_cast<const float2*>(scK + col);
+          c0s = c * sk.x;
+          c1s = c * sk.y;
+        }
+        float v0 = sv.x * c0s, v1 = sv.y * c1s;
+        if (!(row_ok && ((vbits >> col) & 1ull) && (jb + col <= lim))) v0 = NEG_INF;
+        if (!(row_ok && ((vbits >> (col + 1)) & 1ull) && (jb + col + 1 <= lim))) v1 = NEG_INF;
+        x[2 * kk] = v0;
+        x[2 * kk + 1] = v1;
+        mx = fmaxf(mx, fmaxf(v0, v1));
       }
 #pragma unroll
       for (int w = 1; w < LPR; w <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
@@ -258,13 +272,15 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
       // terms, P_hi = rn(P) and P_lo = rn(P - P_hi), so the PV product keeps
       // about 16 significant bits of P instead of 8 (bf16)
 #pragma unroll
-      for (int k = 0; k < CPL; k += 2) {
-        const float p0 = fast_ex2(x[k] - mu), p1 = fast_ex2(x[k + 1] - mu);
+      for (int kk = 0; kk < CPL / 2; ++kk) {
+        const int pp = part + LPR * kk;   // column pair
+        const float p0 = fast_ex2(x[2 * kk] - mu), p1 = fast_ex2(x[2 * kk + 1] - mu);
         sum += p0 + p1;
         float a0 = p0, a1 = p1;
         if constexpr (KQ != 0) {   // the V scale of each column rides on P (times 2^-8 in f16)
-          a0 *= scK[BN + c0 + k] * pv_scale;
-          a1 *= scK[BN + c0 + k + 1] * pv_scale;
+          const float2 sv = *reinterpret_cast<const float2*>(scK + BN + 2 * pp);
+          a0 *= sv.x * pv_scale;
+          a1 *= sv.y * pv_scale;
         }
         const uint32_t hi = pack2h(a0, a1, bf16);
         float h0, h1;
@@ -278,8 +294,8 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
         }
         const uint32_t lo = pack2h(a0 - h0, a1 - h1, bf16);
         if (row_ok) {
-          sP[row * BN + (c0 + k) / 2] = hi;
-          sP[row * BN + BN / 2 + (c0 + k) / 2] = lo;
+          sP[row * Sh::SPP + pp] = hi;
+          sP[row * Sh::SPP + BN / 2 + pp] = lo;
         }
       }
 #pragma unroll
@@ -290,11 +306,22 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
         if (lane < QV) {
-          const uint4* src = reinterpret_cast<const uint4*>(sP + lane * BN + half * (BN / 2));
+          const uint32_t* src = sP + lane * Sh::SPP + half * (BN / 2);
+          if constexpr (Sh::SPP % 4 == 0) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint4 w4 = src[k];
-            pk[4 * k] = w4.x; pk[4 * k + 1] = w4.y; pk[4 * k + 2] = w4.z; pk[4 * k + 3] = w4.w;
+            for (int k = 0; k < 8; ++k) {
+              const uint4 w4 = reinterpret_cast<const uint4*>(src)[k];
+              pk[4 * k] = w4.x; pk[4 * k + 1] = w4.y; pk[4 * k + 2] = w4.z; pk[4 * k + 3] = w4.w;
+            }
+          } else if constexpr (Sh::SPP % 2 == 0) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const uint2 w2 = reinterpret_cast<const uint2*>(src)[k];
+              pk[2 * k] = w2.x; pk[2 * k + 1] = w2.y;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) pk[k] = src[k];
           }
         } else {
 #pragma unroll
