@@ -49,6 +49,7 @@ int kv_kind(fa_dtype d) {
     case FA_BF16: return far::KV_BF16;
     case FA_F16: return far::KV_F16;
     case FA_I8: return far::KV_I8;
+    case FA_I4: return far::KV_I4;
     default: return -1;
   }
 }
@@ -62,9 +63,9 @@ fa_status check_common(const fa_rows_args* a) {
   if (a->Hq % a->Hkv != 0) return fail(FA_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", a->Hq, a->Hkv);
   if (a->n_pool_rows > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "pool rows must fit int32 row indices");
   if (a->q_dtype != FA_F16 && a->q_dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "q dtype must be f16 or bf16");
-  if (kv_kind(a->kv_dtype) < 0) return fail(FA_ERR_UNSUPPORTED, "kv dtype must be f16, bf16 or i8");
-  if (a->kv_dtype != FA_I8 && a->kv_dtype != a->q_dtype)
-    return fail(FA_ERR_UNSUPPORTED, "a 16-bit pool must have the dtype of q");
+  if (kv_kind(a->kv_dtype) < 0) return fail(FA_ERR_UNSUPPORTED, "kv dtype must be f16, bf16, i8 or i4");
+  const bool quant = a->kv_dtype == FA_I8 || a->kv_dtype == FA_I4;
+  if (!quant && a->kv_dtype != a->q_dtype) return fail(FA_ERR_UNSUPPORTED, "a 16-bit pool must have the dtype of q");
   if (a->out_dtype != FA_F32 && a->out_dtype != FA_BF16 && a->out_dtype != FA_F16)
     return fail(FA_ERR_UNSUPPORTED, "out dtype must be f32, bf16 or f16");
   if (a->mask_kind != FA_MASK_NONE && a->mask_kind != FA_MASK_DENSE && a->mask_kind != FA_MASK_CAUSAL)
@@ -75,9 +76,11 @@ fa_status check_common(const fa_rows_args* a) {
   if (a->list_len > 0 && (!a->kv_rows || !a->k || !a->v)) return fail(FA_ERR_INVALID_ARG, "kv_rows, k and v are required");
   if (a->mask_kind == FA_MASK_DENSE && a->list_len > 0 && !a->mask)
     return fail(FA_ERR_INVALID_ARG, "FA_MASK_DENSE needs a mask");
-  if (a->kv_dtype == FA_I8) {
-    if (a->list_len > 0 && (!a->k_scale || !a->v_scale)) return fail(FA_ERR_INVALID_ARG, "INT8 pool needs k_scale and v_scale");
-    if (a->n_pool_rows % far::kPage != 0) return fail(FA_ERR_UNSUPPORTED, "INT8 pool rows must be a multiple of 64");
+  if (quant) {
+    if (a->list_len > 0 && (!a->k_scale || !a->v_scale))
+      return fail(FA_ERR_INVALID_ARG, "a quantised pool needs k_scale and v_scale");
+    if (a->n_pool_rows % far::kPage != 0) return fail(FA_ERR_UNSUPPORTED, "quantised pool rows must be a multiple of 64");
+    if (a->kv_dtype == FA_I4 && a->D % 32 != 0) return fail(FA_ERR_UNSUPPORTED, "INT4 pools need D % 32 == 0");
     if (!aligned(a->k_scale, 4) || !aligned(a->v_scale, 4)) return fail(FA_ERR_INVALID_ARG, "scales must be 4-byte aligned");
   }
   if (!aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->q, 4) || !aligned(a->out, 4) || !aligned(a->kv_rows, 4) ||
@@ -87,7 +90,8 @@ fa_status check_common(const fa_rows_args* a) {
 }
 
 struct DecodePlan {
-  bool tc = false;   // tensor-core kernel
+  bool tc = false;   // tensor-core kernel (either of the two below)
+  bool tcq = false;  // the quantised-pool tensor-core kernel
   int qvp = 0, rows = 0, chunk = 0, nsplit = 0;
   size_t ws = 0;     // workspace bytes
   size_t off_err = 0, off_ml = 0, off_o = 0;
@@ -111,8 +115,12 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   if (qv > 32) return fail(FA_ERR_UNSUPPORTED, "decode packs Nq*Hq/Hkv <= 32 query vectors per KV head (got %lld)", qv);
   const int qvp = next_pow2((int)(qv < 1 ? 1 : qv));
   const int kind = kv_kind(a->kv_dtype);
-  pl->tc = far::decode_tc_supported(a->D, kind, (int)(qv < 1 ? 1 : qv), a->mask_kind) && aligned(a->q, 16) &&
-           a->n_pool_rows * a->Hkv < 0x7fffffffLL;  // gather rows are int32 coordinates r * Hkv + g
+  const int qv1 = (int)(qv < 1 ? 1 : qv);
+  pl->tcq = far::decode_tcq_supported(a->D, kind, qv1, a->mask_kind) && aligned(a->q, 16);
+  pl->tc = pl->tcq || (far::decode_tc_supported(a->D, kind, qv1, a->mask_kind) && aligned(a->q, 16) &&
+                       a->n_pool_rows * a->Hkv < 0x7fffffffLL);  // TMA rows are int32 coordinates r * Hkv + g
+  if (kind == far::KV_I4 && !pl->tcq)
+    return fail(FA_ERR_UNSUPPORTED, "INT4 pools are decoded at D=128 with at most 32 query vectors and no dense mask");
   pl->qvp = qvp;
   pl->rows = pl->tc ? (int)qv : qvp;
   int align = 0, chunk_max = 0;
@@ -139,7 +147,8 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
     return FA_OK;
   }
   int occ = 0;
-  if (pl->tc) occ = far::decode_tc_occupancy(a->D, kind, (int)(qv < 1 ? 1 : qv));
+  if (pl->tcq) occ = far::decode_tcq_occupancy(kind, qv1);
+  else if (pl->tc) occ = far::decode_tc_occupancy(a->D, kind, qv1);
   else if (kind == far::KV_BF16) occ = far::decode_occupancy_bf16(a->D, qvp);
   else if (kind == far::KV_F16) occ = far::decode_occupancy_f16(a->D, qvp);
   else if (kind == far::KV_I8) occ = far::decode_occupancy_i8(a->D, qvp);
@@ -282,7 +291,7 @@ fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_st
   const int kind = kv_kind(a->kv_dtype);
   if (pl.tc) {
     unsigned int* err = pl.ws > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + pl.off_err) : nullptr;
-    e = far::decode_tc_launch(p, a->D, kind, err, s);
+    e = pl.tcq ? far::decode_tcq_launch(p, kind, err, s) : far::decode_tc_launch(p, a->D, kind, err, s);
   } else if (kind == far::KV_BF16) {
     e = far::decode_launch_bf16(p, a->D, pl.qvp, s);
   } else if (kind == far::KV_F16) {

@@ -41,21 +41,23 @@
 
 #include "merge.cuh"
 #include "tc.cuh"
+#include "widen.cuh"
 
 namespace far {
 
 namespace dk {
 constexpr int BN = 64;       // list entries per tile
 constexpr int QROWS = 32;    // query-vector rows kept in shared memory
-constexpr int NST = 3;       // K/V stages
+constexpr int NST = 3;       // K/V stages of the 16-bit kernel (2 CTAs per SM)
 constexpr int NPROD = 4;     // producer warps (each gathers BN / NPROD rows of every tile)
 constexpr int NWARP = 2 + NPROD;   // softmax, producers, MMA
 constexpr int MMA_WARP = 1 + NPROD;
 }  // namespace dk
 
-// KQ: 0 = 16-bit pool, 1 = INT8 codes + fp16 scales.
-template <int D, int QVP, int KQ>
+// KQ: 0 = 16-bit pool, 1 = INT8 codes + fp16 scales.  NS: K/V stages.
+template <int D, int QVP, int KQ, int NS_>
 struct DkShape {
+  static constexpr int NS = NS_;
   static constexpr int KT = D / 64;                  // 128-byte K atoms per row
   static constexpr int QATOM = dk::QROWS * 128;      // bytes of one atom column of the Q tile
   static constexpr int Q_BYTES = KT * QATOM;
@@ -63,10 +65,10 @@ struct DkShape {
   static constexpr int TILE = KT * KV_ATOM;          // one K (or V) tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = ((Q_BYTES + 1023) / 1024) * 1024;
-  static constexpr int OFF_V = OFF_K + dk::NST * TILE;
-  static constexpr int OFF_BAR = OFF_V + dk::NST * TILE;
-  // q_full, kv_full[NST], kv_empty[NST], s_full[2], p_full[2], o_ready, drain
-  static constexpr int NBAR = 1 + 2 * dk::NST + 2 + 2 + 1 + 1;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  // q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_ready, drain
+  static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // S rows of the real query vectors (fp32), then in the same place their P
   // rows (packed 16-bit pairs: BN/2 words of P_hi, BN/2 of P_lo).  The softmax
@@ -79,8 +81,8 @@ struct DkShape {
   static constexpr int SPP = dk::BN + LPR % 32;
   static constexpr int SROW = SSTR > SPP ? SSTR : SPP;
   static constexpr int OFF_SS = ((OFF_MISC + 16 + 127) / 128) * 128;
-  static constexpr int OFF_SC = OFF_SS + ((QVP * SROW * 4 + 15) / 16) * 16;   // [NST][K, V][BN] fp32 scales (KQ)
-  static constexpr int SMEM_USED = OFF_SC + (KQ ? dk::NST * 2 * dk::BN * 4 : 0);
+  static constexpr int OFF_SC = OFF_SS + ((QVP * SROW * 4 + 15) / 16) * 16;   // [K, V][BN] fp32 scales (KQ)
+  static constexpr int SMEM_USED = OFF_SC + (KQ ? 2 * dk::BN * 4 : 0);
   // code bytes of one (row, head), 16-byte chunks of them, first tile atom holding them (KQ)
   static constexpr int CB = KQ ? D : 2 * D;
   static constexpr int CPRQ = CB / 16;
@@ -105,39 +107,6 @@ struct DecodeTcParams {
 
 namespace {
 
-__device__ __forceinline__ uint32_t pack2h(float lo, float hi, bool bf16) {
-  if (bf16) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Four INT8 codes (one word) -> four 16-bit values of Q's type, exact.
-// bf16: (code + 128) is placed in the low mantissa bits of 2^23 and 2^23 + 128
-// subtracted, which leaves the code as an fp32 whose low 16 bits are zero, so
-// its upper half is the bf16 value.  f16: (code + 128) is placed in the low
-// mantissa bits of 1024 (0x6400) and 1152 subtracted.
-__device__ __forceinline__ uint2 widen_i8x4(uint32_t w, bool bf16) {
-  const uint32_t x = w ^ 0x80808080u;
-  if (bf16) {
-    const float2 lo = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650u)),
-                                             __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7651u))),
-                                 make_float2(-8388736.0f, -8388736.0f));
-    const float2 hi = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7652u)),
-                                             __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7653u))),
-                                 make_float2(-8388736.0f, -8388736.0f));
-    return make_uint2(__byte_perm(__float_as_uint(lo.x), __float_as_uint(lo.y), 0x7632u),
-                      __byte_perm(__float_as_uint(hi.x), __float_as_uint(hi.y), 0x7632u));
-  }
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));   // 1152
-  uint32_t a = __byte_perm(x, 0x64646464u, 0x4140u), b = __byte_perm(x, 0x64646464u, 0x4342u);
-  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
-  return make_uint2(*reinterpret_cast<uint32_t*>(&ha), *reinterpret_cast<uint32_t*>(&hb));
-}
-
 __device__ __forceinline__ void wait_drain(uint64_t* b, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(b, parity)) {
@@ -149,13 +118,12 @@ __device__ __forceinline__ void wait_drain(uint64_t* b, uint32_t parity) {
 
 // The softmax role (warp 0) of fa_rows_decode_tc_kernel for QVP = the query
 // vector count rounded up to a power of two.
-template <int D, int QVP, int KQ>
+template <int D, int QVP, int KQ, int NS>
 __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char* sm, uint64_t* s_full, uint64_t* p_full,
-                                           uint64_t* o_ready, uint64_t* o_done, uint64_t* kv_full,
-                                           volatile int* abort_flag,
+                                           uint64_t* o_ready, uint64_t* o_done, volatile int* abort_flag,
                                            uint32_t tbase, int T, int cnt, int j0, int n_s, const int32_t* rows_g,
                                            size_t unit, int split, int s, int g) {
-  using Sh = DkShape<D, QVP, KQ>;
+  using Sh = DkShape<D, QVP, KQ, NS>;
   using namespace dk;
   const float NEG_INF = __int_as_float(0xff800000);
   const int lane = threadIdx.x & 31;
@@ -180,27 +148,45 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
     // it is carried as P * s_v * 2^-8 and O multiplied back by 2^8 at the end
     const float pv_scale = (KQ != 0 && !bf16) ? 0.00390625f : 1.f;
     bool ok = true;
-    int nxt0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // list entries of the next tile
-    int nxt1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
+    // List entries lane and lane + 32 of tile j (cur) and j + 1 (nx), loaded
+    // ahead so no wait lands on their latency; INT8 scales of those entries
+    // one tile ahead (their addresses need the entries).
+    auto entry = [&](int pos) { return pos < cnt ? __ldg(rows_g + pos) : -1; };
+    auto valid = [&](int r) { return r >= 0 && (long long)r < p.R; };
+    auto scale_of = [&](const uint16_t* sc, int r) {
+      return valid(r) ? __ldg(sc + ((size_t)(r >> 6) * p.Hkv + g) * kPage + (r & 63)) : (unsigned short)0;
+    };
+    int cur0 = entry(lane), cur1 = entry(lane + 32);
+    int nx0 = entry(BN + lane), nx1 = entry(BN + lane + 32);
+    unsigned short sk0 = 0, sk1 = 0, sv0 = 0, sv1 = 0;   // scales of tile j's entries
+    if constexpr (KQ != 0) {
+      sk0 = scale_of(p.k_scale, cur0);
+      sk1 = scale_of(p.k_scale, cur1);
+      sv0 = scale_of(p.v_scale, cur0);
+      sv1 = scale_of(p.v_scale, cur1);
+    }
+    float* scK = reinterpret_cast<float*>(sm + Sh::OFF_SC);   // [K, V][BN] scales of the current tile
     for (int j = 0; j < T; ++j) {
       const int b = j & 1;
       unsigned vb[2];
-      vb[0] = __ballot_sync(0xffffffffu, nxt0 >= 0 && (long long)nxt0 < p.R);
-      vb[1] = __ballot_sync(0xffffffffu, nxt1 >= 0 && (long long)nxt1 < p.R);
-      {
-        const int pos = (j + 1) * BN + lane;
-        nxt0 = pos < cnt ? __ldg(rows_g + pos) : -1;
-        nxt1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
+      vb[0] = __ballot_sync(0xffffffffu, valid(cur0));
+      vb[1] = __ballot_sync(0xffffffffu, valid(cur1));
+      if constexpr (KQ != 0) {
+        scK[lane] = __half2float(__ushort_as_half(sk0));
+        scK[lane + 32] = __half2float(__ushort_as_half(sk1));
+        scK[BN + lane] = __half2float(__ushort_as_half(sv0));
+        scK[BN + lane + 32] = __half2float(__ushort_as_half(sv1));
+        sk0 = scale_of(p.k_scale, nx0);
+        sk1 = scale_of(p.k_scale, nx1);
+        sv0 = scale_of(p.v_scale, nx0);
+        sv1 = scale_of(p.v_scale, nx1);
       }
+      cur0 = nx0;
+      cur1 = nx1;
+      nx0 = entry((j + 2) * BN + lane);
+      nx1 = entry((j + 2) * BN + lane + 32);
       const int jb = j0 + j * BN;   // list position of column 0
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag)))) break;
-      const float* scK = reinterpret_cast<const float*>(sm + Sh::OFF_SC) + (j % NST) * 2 * BN;
-      if constexpr (KQ != 0) {
-        // the producers' scale stores are ordered before this read by the
-        // stage's full barrier (its phase for tile j stays complete until this
-        // warp releases P of tile j)
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(kv_full + j % NST, (j / NST) & 1, abort_flag)))) break;
-      }
       tc_fence_after();
       {
         uint32_t sr[2][32];
@@ -384,12 +370,13 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
     }
 }
 
-template <int D, int QVP, int KQ>
+template <int D, int QVP, int KQ, int NS>
 __global__ void __launch_bounds__(dk::NWARP * 32, 2)
     fa_rows_decode_tc_kernel(const DecodeTcParams kp, const __grid_constant__ CUtensorMap tk,
                              const __grid_constant__ CUtensorMap tv) {
-  using Sh = DkShape<D, QVP, KQ>;
+  using Sh = DkShape<D, QVP, KQ, NS>;
   using namespace dk;
+  constexpr int NST = NS;   // stages of this instance
   const DecodeParams& p = kp.a;
   const float NEG_INF = __int_as_float(0xff800000);
   extern __shared__ unsigned char smem_raw[];
@@ -469,18 +456,14 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
     }
-    static_assert(NST == 3, "the producers track three stages in scalars");
+    static_assert(KQ != 0 || NST == 3, "the TMA path tracks three stages in scalars");
     unsigned gathered = 0;   // bit t % 32: this warp gathered its rows of tile t (arrival due at publish)
     unsigned tma_pend = 0;   // bit st: a TMA load into stage st may still be in flight (warp 0)
     int use0 = 0, use1 = 0, use2 = 0;
     int nrow0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // next tile's rows, one tile ahead
     int nrow1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
     int published = 0;
-    // KQ: this warp's scale loads (entry pw*ROWS + lane%16, K for lanes < 16,
-    // V above) of the two tiles in flight: sc_a the older, sc_b the newer
-    // (raw fp16 bits: converted only at publish, so no instruction waits on the load before then)
-    unsigned short sc_a = 0, sc_b = 0;
-    auto publish = [&](int t, unsigned short sc) {
+    auto publish = [&](int t) {
       if ((gathered >> (t & 31)) & 1u) {
         if constexpr (KQ != 0) {
           // widen this warp's rows of the stage in place: every lane reads
@@ -512,8 +495,6 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
             }
             __syncwarp();
           }
-          reinterpret_cast<float*>(sm + Sh::OFF_SC)[(t % NST) * 2 * BN + (lane >> 4) * BN + pw * ROWS + (lane & 15)] =
-              __half2float(__ushort_as_half(sc));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -526,7 +507,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       // it before it can free that stage
       if (j >= NST - 1) {
         cp_async_wait<NST - 2>();
-        publish(j - (NST - 1), sc_a);
+        publish(j - (NST - 1));
         published = j - (NST - 1) + 1;
       }
       if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
@@ -555,15 +536,6 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
           const uint32_t so = (Sh::A0 + c / 8) * Sh::KV_ATOM + e * 128 + (((c & 7) ^ (e & 7)) << 4);
           cp_async16(Ks + so, kb + go, okr);
           cp_async16(Vs + so, vb + go, okr);
-        }
-        {
-          const int e = pw * ROWS + (lane & 15);
-          const int ra = __shfl_sync(0xffffffffu, rows[0], e & 31);
-          const int rb = __shfl_sync(0xffffffffu, rows[1], e & 31);
-          const int r = e < 32 ? ra : rb;
-          const uint16_t* sc = (lane >> 4) ? p.v_scale : p.k_scale;
-          sc_a = sc_b;
-          sc_b = r >= 0 ? __ldg(sc + ((size_t)(r >> 6) * p.Hkv + g) * kPage + (r & 63)) : (unsigned short)0;
         }
         gathered |= 1u << (j & 31);
         cp_async_commit();
@@ -610,11 +582,8 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       cp_async_commit();   // one group per tile (empty for TMA tiles)
     }
     cp_async_wait<0>();
-    if (!*abort_flag) {
-      // at most two tiles are left: T-2 (scales in sc_a) and T-1 (sc_b)
-      if (T - published >= 2) publish(T - 2, sc_a);
-      if (T - published >= 1) publish(T - 1, sc_b);
-    }
+    if (!*abort_flag)
+      for (int t = published; t < T; ++t) publish(t);
     if (pw == 0 && lane == 0 && *abort_flag) {
       if (tma_pend & 1u) wait_drain(kv_full + 0, use0 & 1);
       if (tma_pend & 2u) wait_drain(kv_full + 1, use1 & 1);
@@ -667,7 +636,12 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
         }
         if (progressed) {
           t_idle = 0;
-        } else if (t_idle == 0) {
+          continue;
+        }
+        // idle: back off briefly so this lane's polling does not take issue
+        // slots from the gather warp sharing its scheduler
+        __nanosleep(32);
+        if (t_idle == 0) {
           t_idle = globaltimer();
         } else if (*abort_flag) {
           ok = false;
@@ -681,7 +655,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
     }
   } else {
     // ------------------------------------------------------------ softmax (warp 0)
-    dk_softmax<D, QVP, KQ>(p, sm, s_full, p_full, o_ready, drain, kv_full, abort_flag, tbase, T, cnt, j0, n_s, rows_g, unit,
+    dk_softmax<D, QVP, KQ, NS>(p, sm, s_full, p_full, o_ready, drain, abort_flag, tbase, T, cnt, j0, n_s, rows_g, unit,
                            split, s, g);
   }
 
@@ -739,14 +713,14 @@ bool dk_map(CUtensorMap* m, const void* base, bool bf16, int D, int Hkv, long lo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int QVP, int KQ>
+template <int D, int QVP, int KQ, int NS>
 int dk_occupancy() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (cached[dev] > 0) return cached[dev];
-  using Sh = DkShape<D, QVP, KQ>;
-  auto kern = fa_rows_decode_tc_kernel<D, QVP, KQ>;
+  using Sh = DkShape<D, QVP, KQ, NS>;
+  auto kern = fa_rows_decode_tc_kernel<D, QVP, KQ, NS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, dk::NWARP * 32, Sh::SMEM) != cudaSuccess) return 0;
@@ -757,9 +731,9 @@ int dk_occupancy() {
   return n;
 }
 
-template <int D, int QVP, int KQ>
+template <int D, int QVP, int KQ, int NS>
 cudaError_t dk_launch(const DecodeParams& a, unsigned int* err, cudaStream_t st) {
-  if (dk_occupancy<D, QVP, KQ>() <= 0) return cudaErrorInvalidConfiguration;
+  if (dk_occupancy<D, QVP, KQ, NS>() <= 0) return cudaErrorInvalidConfiguration;
   DecodeTcParams kp;
   kp.a = a;
   kp.err = err;
@@ -773,7 +747,7 @@ cudaError_t dk_launch(const DecodeParams& a, unsigned int* err, cudaStream_t st)
     if (!dk_map(&tk, a.k, bf16, D, a.Hkv, a.R) || !dk_map(&tv, a.v, bf16, D, a.Hkv, a.R)) return cudaErrorInvalidValue;
   }
   dim3 grid(a.nsplit, a.Hkv, a.S);
-  fa_rows_decode_tc_kernel<D, QVP, KQ><<<grid, dk::NWARP * 32, DkShape<D, QVP, KQ>::SMEM, st>>>(kp, tk, tv);
+  fa_rows_decode_tc_kernel<D, QVP, KQ, NS><<<grid, dk::NWARP * 32, DkShape<D, QVP, KQ, NS>::SMEM, st>>>(kp, tk, tv);
   return cudaGetLastError();
 }
 
@@ -784,6 +758,12 @@ bool decode_tc_supported(int D, int kind, int qv, int mask_kind) {
          qv <= dk::QROWS && mask_kind != FA_MASK_DENSE;
 }
 
+// Stages per CTA: the 16-bit kernel runs two CTAs per SM with three stages
+// each; an INT8 stage keeps only half its bytes in flight (codes land in the
+// upper half of a 16-bit tile), so at D 128 the INT8 kernel runs one CTA per
+// SM with six stages.
+constexpr int dk_stages(int D, int KQ) { return KQ != 0 && D == 128 ? 6 : 3; }
+
 static int qv_pow2(int qv) {
   int q = 1;
   while (q < qv) q <<= 1;
@@ -793,24 +773,24 @@ static int qv_pow2(int qv) {
 template <int D, int KQ>
 int dk_occupancy_d(int qvp) {
   switch (qvp) {
-    case 1: return dk_occupancy<D, 1, KQ>();
-    case 2: return dk_occupancy<D, 2, KQ>();
-    case 4: return dk_occupancy<D, 4, KQ>();
-    case 8: return dk_occupancy<D, 8, KQ>();
-    case 16: return dk_occupancy<D, 16, KQ>();
-    default: return dk_occupancy<D, 32, KQ>();
+    case 1: return dk_occupancy<D, 1, KQ, dk_stages(D, KQ)>();
+    case 2: return dk_occupancy<D, 2, KQ, dk_stages(D, KQ)>();
+    case 4: return dk_occupancy<D, 4, KQ, dk_stages(D, KQ)>();
+    case 8: return dk_occupancy<D, 8, KQ, dk_stages(D, KQ)>();
+    case 16: return dk_occupancy<D, 16, KQ, dk_stages(D, KQ)>();
+    default: return dk_occupancy<D, 32, KQ, dk_stages(D, KQ)>();
   }
 }
 
 template <int D, int KQ>
 cudaError_t dk_launch_d(int qvp, const DecodeParams& a, unsigned int* err, cudaStream_t st) {
   switch (qvp) {
-    case 1: return dk_launch<D, 1, KQ>(a, err, st);
-    case 2: return dk_launch<D, 2, KQ>(a, err, st);
-    case 4: return dk_launch<D, 4, KQ>(a, err, st);
-    case 8: return dk_launch<D, 8, KQ>(a, err, st);
-    case 16: return dk_launch<D, 16, KQ>(a, err, st);
-    default: return dk_launch<D, 32, KQ>(a, err, st);
+    case 1: return dk_launch<D, 1, KQ, dk_stages(D, KQ)>(a, err, st);
+    case 2: return dk_launch<D, 2, KQ, dk_stages(D, KQ)>(a, err, st);
+    case 4: return dk_launch<D, 4, KQ, dk_stages(D, KQ)>(a, err, st);
+    case 8: return dk_launch<D, 8, KQ, dk_stages(D, KQ)>(a, err, st);
+    case 16: return dk_launch<D, 16, KQ, dk_stages(D, KQ)>(a, err, st);
+    default: return dk_launch<D, 32, KQ, dk_stages(D, KQ)>(a, err, st);
   }
 }
 

@@ -11,7 +11,7 @@
 namespace far {
 
 // KV storage kinds the kernels are built for.
-enum KvKind { KV_BF16 = 0, KV_F16 = 1, KV_I8 = 2 };
+enum KvKind { KV_BF16 = 0, KV_F16 = 1, KV_I8 = 2, KV_I4 = 3 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -70,6 +70,12 @@ bool decode_tc_supported(int D, int kind, int qv, int mask_kind);
 int decode_tc_occupancy(int D, int kind, int qv);
 int decode_tc_tile();
 cudaError_t decode_tc_launch(const DecodeParams& p, int D, int kind, unsigned int* err, cudaStream_t st);
+
+// Tensor-core decode for quantised pools (INT8 / INT4 codes + fp16 scales),
+// D 128: one CTA per SM with a deep code ring.  Same workspace as above.
+bool decode_tcq_supported(int D, int kind, int qv, int mask_kind);
+int decode_tcq_occupancy(int kind, int qv);
+cudaError_t decode_tcq_launch(const DecodeParams& p, int kind, unsigned int* err, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // prefill

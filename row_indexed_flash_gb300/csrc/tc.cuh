@@ -54,6 +54,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Makes the mbarrier track this thread's earlier cp.async copies: one arrival
+// once they have all landed (the arrival is counted in the barrier's
+// expected count, not added to it).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* b) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+// Waits for every cp.async copy this thread has issued, grouped or not.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Barrier `id` (1..15) over `n` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Waits for the phase with the given parity.  Gives up (returning false and
 // raising *abort) after kWaitLimitNs, or as soon as another role of the CTA
 // has raised *abort.
