@@ -44,16 +44,21 @@ METRIC = "row-indexed attention: decode gathered-KV GB/s, prefill TFLOP/s (vs GB
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "decode": ["row_indexed_flash_gb300/csrc/decode_tc.cu", "row_indexed_flash_gb300/csrc/tc.cuh",
-               "row_indexed_flash_gb300/csrc/merge.cuh", "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
+               "row_indexed_flash_gb300/csrc/merge.cuh", "row_indexed_flash_gb300/csrc/widen.cuh",
+               "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
+    "decode_q": ["row_indexed_flash_gb300/csrc/decode_tcq.cu", "row_indexed_flash_gb300/csrc/tc.cuh",
+                 "row_indexed_flash_gb300/csrc/merge.cuh", "row_indexed_flash_gb300/csrc/widen.cuh",
+                 "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
     "prefill": ["row_indexed_flash_gb300/csrc/prefill.cu", "row_indexed_flash_gb300/csrc/tc.cuh",
                 "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
 }
 KERNEL_NAMES = {"decode": "fa_rows_decode_tc_kernel", "prefill": "fa_rows_prefill_kernel",
-                "decode_cc": "fa_rows_decode_kernel"}
+                "decode_q": "fa_rows_decode_tcq_kernel"}
 PROFILE_FILES = {
     "decode_bf16": "profiles/decode_bf16_4x16384_ncu.txt",
     "prefill_bf16": "profiles/prefill_bf16_4x2048x99936_ncu.txt",
     "prefill_bf16_small": "profiles/prefill_bf16_4x2048x16384_ncu.txt",
+    "paged_int8": "profiles/paged_int8_32seq_ncu.txt",
 }
 
 
@@ -61,9 +66,10 @@ PROFILE_FILES = {
 # workload accounting
 
 
-def decode_bytes(p) -> int:
-    """Algorithmic bytes: each listed row is read once per KV head (K and V)."""
-    per = 2 * p.D * (1 if p.kv_int8 else 2) + (4 if p.kv_int8 else 0)
+def decode_bytes(p, quant=None) -> int:
+    """Algorithmic bytes: each listed row is read once per KV head (K and V
+    codes, plus their two fp16 scales for a quantised pool)."""
+    per = {None: 4 * p.D, "int8": 2 * p.D + 4, "int4": p.D + 4}[quant]
     return p.n_valid() * p.Hkv * per
 
 
@@ -243,8 +249,8 @@ def build_problem(workload: str):
         return synth.decode_bf16_large()
     if workload == "prefill_bf16":
         return synth.prefill_bf16()
-    if workload == "paged_int8":
-        return synth.paged_int8()
+    if workload in ("paged_int8", "paged_int4"):
+        return synth.paged_int8()   # the paged layout; the pool is quantised by the bench
     if workload == "sparse_bf16":
         return synth.sparse_bf16()
     if workload == "decode_f16_small":
@@ -271,13 +277,15 @@ def run_gpu(args, rank, world, p, cpu_baseline):
 
     is_prefill = args.workload.startswith("prefill")
     paged = p.kv_int8
+    quant = ("int4" if args.workload == "paged_int4" else "int8") if paged else None
+    quantise = far.fa_kv_quantize_int4 if quant == "int4" else far.fa_kv_quantize_int8
     q = to_dev(p.q)
     k0, v0 = to_dev(p.k), to_dev(p.v)
     scales = None
     if paged:
-        # write path (not timed): quantise the bf16 pool into INT8 codes + fp16 scales
-        kq, ks = far.fa_kv_quantize_int8(k0, p.R)
-        vq, vs = far.fa_kv_quantize_int8(v0, p.R)
+        # write path (not timed): quantise the bf16 pool into INT8/INT4 codes + fp16 scales
+        kq, ks = quantise(k0, p.R)
+        vq, vs = quantise(v0, p.R)
         del k0, v0
         torch.cuda.synchronize(dev)
         k0, v0, scales = kq, vq, (ks, vs)
@@ -386,14 +394,14 @@ def run_gpu(args, rank, world, p, cpu_baseline):
         return None
 
     pk, pk_src = peaks()
-    kind = "prefill" if is_prefill else "decode"
+    kind = "prefill" if is_prefill else ("decode_q" if paged else "decode")
     if is_prefill:
         work = prefill_flops(p)
         unit, scale_ = "TFLOP/s", 1e12
         peak = pk["bf16_tflops_sustained" if args.steps * step_ms > 2000 else "bf16_tflops"]
         bound = "tensor"
     else:
-        work = decode_bytes(p)
+        work = decode_bytes(p, quant)
         unit, scale_ = "GB/s", 1e9
         peak = pk["hbm_gbs"]
         bound = "hbm"
@@ -455,8 +463,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="decode_bf16", choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8",
-                                                             "sparse_bf16", "decode_f16_small"])
+    ap.add_argument("--workload", default="decode_bf16",
+                    choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int4",
+                             "sparse_bf16", "decode_f16_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -60,8 +60,10 @@ typedef enum fa_mask_kind {
  *
  *   q        [S, Nq, Hq, D]     FA_F16 or FA_BF16
  *   k, v     [R, Hkv, D]        the unified pool: FA_F16/FA_BF16 (same as q),
- *                               or FA_I8 (int8 codes, then k_scale/v_scale)
- *   k_scale, v_scale            FA_I8 only: fp16 bit patterns laid out
+ *                               FA_I8 (int8 codes, then k_scale/v_scale), or
+ *            [R, Hkv, D/2]      FA_I4 (two 4-bit codes per byte, element 2t in
+ *                               the low nibble of byte t; D = 128 only)
+ *   k_scale, v_scale            FA_I8/FA_I4 only: fp16 bit patterns laid out
  *                               [R/64, Hkv, 64], i.e. the scale of (row r,
  *                               head g) sits at ((r/64)*Hkv + g)*64 + r%64;
  *                               value = code * scale (R must be a multiple of 64)
@@ -181,6 +183,22 @@ fa_status fa_kv_quantize_int8(const void* x, fa_dtype x_dtype, int64_t n_rows, i
 
 /* out[r, g, d] = float(q[r, g, d]) * float(scale of (r, g)), exact in fp32. */
 fa_status fa_kv_dequantize_int8(const int8_t* q, const uint16_t* scale, int64_t n_rows, int32_t Hkv, int32_t D,
+                                float* out, fa_stream_t stream);
+
+/*
+ * INT4 KV quantisation for the paged INT4 pool the v100llm article names
+ * (section 2, "INT4/INT8 paged path"; it gives no rule): the INT8 rule above
+ * with 7 in place of 127 (s = fp16_rne(min(amax/7, 65504)), codes in -7..7),
+ * stored as two's-complement nibbles, element 2t in the low nibble of byte t.
+ *   q        [R, Hkv, D/2] uint8 pool; scale the fp16 layout of fa_rows_args.
+ * D must be even and <= 256; negative dst_rows entries are skipped.
+ */
+fa_status fa_kv_quantize_int4(const void* x, fa_dtype x_dtype, int64_t n_rows, int32_t Hkv, int32_t D,
+                              const int32_t* dst_rows, uint8_t* q, uint16_t* scale, int64_t n_pool_rows,
+                              fa_stream_t stream);
+
+/* out[r, g, d] = float(nibble code) * float(scale of (r, g)), exact in fp32. */
+fa_status fa_kv_dequantize_int4(const uint8_t* q, const uint16_t* scale, int64_t n_rows, int32_t Hkv, int32_t D,
                                 float* out, fa_stream_t stream);
 
 /*

@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "FaRowsError", "lib", "library_path", "fa_rows_args", "fa_rows_workspace_size", "fa_rows_workspace_init",
     "fa_rows_decode", "fa_rows_prefill", "fa_rows_validate", "fa_kv_page_table_to_rows", "fa_kv_quantize_int8",
-    "fa_kv_dequantize_int8", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
+    "fa_kv_dequantize_int8", "fa_kv_quantize_int4", "fa_kv_dequantize_int4", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
     "FA_F16", "FA_BF16", "FA_F32", "FA_I8", "FA_I4", "FA_MASK_NONE", "FA_MASK_DENSE", "FA_MASK_CAUSAL",
 ]
 
@@ -75,6 +75,9 @@ _SIGS = {
     "fa_kv_quantize_int8": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                            _P, ctypes.c_int64, _P]),
     "fa_kv_dequantize_int8": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "fa_kv_quantize_int4": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                           _P, ctypes.c_int64, _P]),
+    "fa_kv_dequantize_int4": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P]),
     "fa_kv_append": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                     ctypes.c_int64, _P]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -121,7 +124,7 @@ def _check(status: int):
 # ---------------------------------------------------------------------------
 # marshalling helpers
 
-_DT = {torch.float16: FA_F16, torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.int8: FA_I8}
+_DT = {torch.float16: FA_F16, torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.int8: FA_I8, torch.uint8: FA_I4}
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -170,14 +173,15 @@ def make_args(q, k, v, kv_rows, scale, *, kv_len=None, mask=None, causal=False, 
     """Builds fa_rows_args from torch tensors; allocates ``out``/``lse`` if not given."""
     S, Nq, Hq, D = q.shape
     R, Hkv, Dk = k.shape
-    if tuple(v.shape) != (R, Hkv, Dk) or Dk != D:
+    packed = k.dtype == torch.uint8   # INT4 pool: two codes per byte
+    if tuple(v.shape) != (R, Hkv, Dk) or Dk * (2 if packed else 1) != D:
         raise ValueError(f"k {tuple(k.shape)} / v {tuple(v.shape)} do not match q {tuple(q.shape)}")
     if kv_rows.dtype != torch.int32 or kv_rows.dim() != 2 or kv_rows.shape[0] != S:
         raise ValueError("kv_rows must be int32 [S, L]")
     if k.dtype != v.dtype:
         raise ValueError("k and v must share a dtype")
-    if k.dtype == torch.int8 and (k_scale is None or v_scale is None):
-        raise ValueError("an int8 pool needs k_scale and v_scale")
+    if k.dtype in (torch.int8, torch.uint8) and (k_scale is None or v_scale is None):
+        raise ValueError("a quantised pool needs k_scale and v_scale")
     if kv_len is not None and (kv_len.dtype != torch.int32 or kv_len.shape != (S,)):
         raise ValueError("kv_len must be int32 [S]")
     if mask is not None and (mask.dtype != torch.float32 or tuple(mask.shape) != (S, Nq, kv_rows.shape[1])):
@@ -284,6 +288,28 @@ def fa_kv_dequantize_int8(q: torch.Tensor, scale: torch.Tensor, out=None, stream
     if out is None:
         out = torch.empty((R, Hkv, D), dtype=torch.float32, device=q.device)
     _check(lib().fa_kv_dequantize_int8(_ptr(q), _ptr(scale), R, Hkv, D, _ptr(out), _stream(stream, q.device)))
+    return out
+
+
+def fa_kv_quantize_int4(x: torch.Tensor, n_pool_rows: Optional[int] = None, dst_rows=None, q=None, scale=None,
+                        stream=None):
+    """Quantises x [n, Hkv, D] (bf16/f16) into an INT4 pool; returns (q [R,Hkv,D/2] uint8, scale fp16 [R/64,Hkv,64])."""
+    n, Hkv, D = x.shape
+    R = n if n_pool_rows is None else int(n_pool_rows)
+    if q is None:
+        q = torch.zeros((R, Hkv, D // 2), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.zeros((R // 64, Hkv, 64), dtype=torch.float16, device=x.device)
+    _check(lib().fa_kv_quantize_int4(_ptr(x), _DT[x.dtype], n, Hkv, D, _ptr(dst_rows), _ptr(q), _ptr(scale),
+                                     q.shape[0], _stream(stream, x.device)))
+    return q, scale
+
+
+def fa_kv_dequantize_int4(q: torch.Tensor, scale: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    R, Hkv, Dh = q.shape
+    if out is None:
+        out = torch.empty((R, Hkv, 2 * Dh), dtype=torch.float32, device=q.device)
+    _check(lib().fa_kv_dequantize_int4(_ptr(q), _ptr(scale), R, Hkv, 2 * Dh, _ptr(out), _stream(stream, q.device)))
     return out
 
 

@@ -395,6 +395,34 @@ fa_status fa_kv_dequantize_int8(const int8_t* q, const uint16_t* scale, int64_t 
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "dequantize launch");
 }
 
+fa_status fa_kv_quantize_int4(const void* x, fa_dtype x_dtype, int64_t n_rows, int32_t Hkv, int32_t D,
+                              const int32_t* dst_rows, uint8_t* q, uint16_t* scale, int64_t n_pool_rows,
+                              fa_stream_t stream) {
+  g_err[0] = 0;
+  if (x_dtype != FA_BF16 && x_dtype != FA_F16) return fail(FA_ERR_UNSUPPORTED, "x must be bf16 or f16");
+  if (n_rows < 0 || Hkv <= 0 || D <= 0 || D > 256 || (D & 1) || n_pool_rows < 0)
+    return fail(FA_ERR_INVALID_ARG, "bad sizes (n_rows=%lld Hkv=%d D=%d; D must be even, <= 256)", (long long)n_rows, Hkv,
+                D);
+  if (n_pool_rows % far::kPage) return fail(FA_ERR_UNSUPPORTED, "INT4 pool rows must be a multiple of 64");
+  if (!dst_rows && n_rows > n_pool_rows) return fail(FA_ERR_INVALID_ARG, "identity append needs n_rows <= pool rows");
+  if (n_rows == 0) return FA_OK;
+  if (!x || !q || !scale) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
+  cudaError_t e = far::launch_quantize_int4(x, x_dtype == FA_BF16, n_rows, Hkv, D, dst_rows, q, scale, n_pool_rows,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "quantize launch");
+}
+
+fa_status fa_kv_dequantize_int4(const uint8_t* q, const uint16_t* scale, int64_t n_rows, int32_t Hkv, int32_t D,
+                                float* out, fa_stream_t stream) {
+  g_err[0] = 0;
+  if (n_rows < 0 || Hkv <= 0 || D <= 0 || (D & 1)) return fail(FA_ERR_INVALID_ARG, "bad sizes");
+  if (n_rows % far::kPage) return fail(FA_ERR_UNSUPPORTED, "INT4 pool rows must be a multiple of 64");
+  if (n_rows == 0) return FA_OK;
+  if (!q || !scale || !out) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
+  cudaError_t e = far::launch_dequantize_int4(q, scale, n_rows, Hkv, D, out, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "dequantize launch");
+}
+
 fa_status fa_kv_append(const void* x, fa_dtype dtype, int64_t n_rows, int32_t Hkv, int32_t D, const int32_t* dst_rows,
                        void* pool, int64_t n_pool_rows, fa_stream_t stream) {
   g_err[0] = 0;

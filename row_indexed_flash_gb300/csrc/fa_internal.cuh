@@ -109,6 +109,10 @@ cudaError_t launch_quantize_int8(const void* x, int x_bf16, long long n_rows, in
                                  int8_t* q, uint16_t* scale, long long R, cudaStream_t st);
 cudaError_t launch_dequantize_int8(const int8_t* q, const uint16_t* scale, long long n_rows, int Hkv, int D,
                                    float* out, cudaStream_t st);
+cudaError_t launch_quantize_int4(const void* x, int x_bf16, long long n_rows, int Hkv, int D, const int32_t* dst,
+                                 uint8_t* q, uint16_t* scale, long long R, cudaStream_t st);
+cudaError_t launch_dequantize_int4(const uint8_t* q, const uint16_t* scale, long long n_rows, int Hkv, int D,
+                                   float* out, cudaStream_t st);
 cudaError_t launch_kv_append(const void* x, long long n_rows, int row_bytes, const int32_t* dst, void* pool,
                              long long R, cudaStream_t st);
 cudaError_t launch_validate(const int32_t* rows, const int32_t* kv_len, int S, int L, long long R,

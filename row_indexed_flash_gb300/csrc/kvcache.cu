@@ -1,4 +1,4 @@
-// KV-pool kernels: page-table expansion, INT8 quantise / dequantise, 16-bit
+// KV-pool kernels: page-table expansion, INT8 / INT4 quantise / dequantise, 16-bit
 // row appends and the row-list range check.
 //
 // Paged KV with 64-token pages and INT8 storage: v100llm article, sections
@@ -106,6 +106,97 @@ cudaError_t launch_quantize_int8(const void* x, int x_bf16, long long n_rows, in
   if (blocks > 152 * 64) blocks = 152 * 64;
   quantize_int8_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint16_t*>(x), x_bf16, n_rows, Hkv, D,
                                                              dst, q, scale, R);
+  return cudaGetLastError();
+}
+
+// One warp per (source row, head), INT4: the INT8 rule with 7 in place of
+// 127; two's-complement nibbles, element 2t in the low nibble of byte t.
+// Lane l handles the element pairs l, l + 32, ... (D <= 256).
+__global__ void quantize_int4_kernel(const uint16_t* __restrict__ x, int x_bf16, long long n_rows, int Hkv, int D,
+                                     const int32_t* __restrict__ dst_rows, uint8_t* __restrict__ q,
+                                     uint16_t* __restrict__ scale, long long R) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+  for (long long w = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5); w < n_rows * Hkv; w += warps) {
+    const long long i = w / Hkv;
+    const int g = (int)(w % Hkv);
+    const long long dst = dst_rows ? (long long)dst_rows[i] : i;
+    if (dst < 0 || dst >= R) continue;
+    const uint16_t* src = x + (size_t)w * D;
+    float vals[8];
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int d = 2 * (lane + 32 * u);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float f = 0.f;
+        if (d + e < D) {
+          const uint32_t b = src[d + e];
+          f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
+        }
+        vals[2 * u + e] = f;
+        amax = fmaxf(amax, fabsf(f));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const __half sh = __float2half_rn(fminf(__fdiv_rn(amax, 7.0f), 65504.0f));
+    const float sf = __half2float(sh);
+    uint8_t* qd = q + ((size_t)dst * Hkv + g) * (D / 2);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = lane + 32 * u;   // byte t holds elements 2t, 2t+1
+      if (2 * t < D) {
+        int c0 = 0, c1 = 0;
+        if (sf != 0.f) {
+          c0 = min(max(__float2int_rn(__fdiv_rn(vals[2 * u], sf)), -7), 7);
+          c1 = min(max(__float2int_rn(__fdiv_rn(vals[2 * u + 1], sf)), -7), 7);
+        }
+        qd[t] = (uint8_t)((c0 & 0xF) | ((c1 & 0xF) << 4));
+      }
+    }
+    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = __half_as_ushort(sh);
+  }
+}
+
+cudaError_t launch_quantize_int4(const void* x, int x_bf16, long long n_rows, int Hkv, int D, const int32_t* dst,
+                                 uint8_t* q, uint16_t* scale, long long R, cudaStream_t st) {
+  const long long warps = n_rows * Hkv;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (warps + 7) / 8;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  quantize_int4_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint16_t*>(x), x_bf16, n_rows, Hkv, D,
+                                                             dst, q, scale, R);
+  return cudaGetLastError();
+}
+
+// out = float(nibble code) * float(scale), exact in fp32.
+__global__ void dequantize_int4_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ scale,
+                                       long long n_rows, int Hkv, int D, float* __restrict__ out) {
+  const long long n = n_rows * Hkv * D;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n; t += (long long)gridDim.x * blockDim.x) {
+    const long long rh = t / D;
+    const long long r = rh / Hkv;
+    const int g = (int)(rh % Hkv);
+    const int d = (int)(t % D);
+    const int byte = q[rh * (D / 2) + d / 2];
+    int c = (d & 1) ? (byte >> 4) : (byte & 0xF);
+    c = c >= 8 ? c - 16 : c;
+    const float sf = __half2float(__ushort_as_half(scale[((size_t)(r / kPage) * Hkv + g) * kPage + (r % kPage)]));
+    out[t] = __fmul_rn((float)c, sf);
+  }
+}
+
+cudaError_t launch_dequantize_int4(const uint8_t* q, const uint16_t* scale, long long n_rows, int Hkv, int D,
+                                   float* out, cudaStream_t st) {
+  const long long n = n_rows * Hkv * D;
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (n + threads - 1) / threads;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  dequantize_int4_kernel<<<(unsigned)blocks, threads, 0, st>>>(q, scale, n_rows, Hkv, D, out);
   return cudaGetLastError();
 }
 
