@@ -251,7 +251,7 @@ def build_problem(workload: str):
         return synth.prefill_bf16()
     if workload in ("paged_int8", "paged_int4"):
         return synth.paged_int8()   # the paged layout; the pool is quantised by the bench
-    if workload == "sparse_bf16":
+    if workload in ("sparse_bf16", "sparse_select_bf16"):
         return synth.sparse_bf16()
     if workload == "decode_f16_small":
         return synth.decode_fp16_small()
@@ -294,6 +294,11 @@ def run_gpu(args, rank, world, p, cpu_baseline):
         rows = torch.empty((p.S, p.L), dtype=torch.int32, device=dev)
     else:
         rows = torch.from_numpy(p.kv_rows).to(dev)
+    select = args.workload == "sparse_select_bf16"
+    if select:
+        # each step builds the list (4 sinks + 1,532 by score + 512 recent) from a
+        # seeded fp32 score per position, then decodes over it
+        sel_score = torch.from_numpy(synth.rng(9).standard_normal((1, p.R)).astype(np.float32)).to(dev)
     pool_bytes = 2 * k0.numel() * k0.element_size()
     # rotate over enough pool copies that each step reads data not left in L2
     n_copies = max(1, min(3, int(math.ceil(3 * 129e6 / pool_bytes)) + 1)) if not is_prefill else 1
@@ -315,6 +320,11 @@ def run_gpu(args, rank, world, p, cpu_baseline):
     lib = far.lib()
 
     def step(i):
+        if select:
+            st = lib.fa_kv_sparse_rows(sel_score.data_ptr(), p.R, None, 1, 4, 512, 1532, None, rows.data_ptr(),
+                                       rows.shape[1], sh)
+            if st != 0:
+                raise far.FaRowsError(st, far.fa_last_error())
         if paged:   # page tables -> row lists, then the decode (both kernels of the step)
             st = lib.fa_kv_page_table_to_rows(pt.data_ptr(), pt.shape[1], sl.data_ptr(), p.S, p.page_size,
                                               rows.data_ptr(), p.L, sh)
@@ -447,7 +457,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4),
         },
-        "gpu_launches": args.steps * (2 if paged else 1),
+        "gpu_launches": args.steps * (2 if (paged or select) else 1),
         "clocks": clk.summary(),
         "cpu_baseline": cpu_baseline,
     }
@@ -465,7 +475,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode_bf16",
                     choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int4",
-                             "sparse_bf16", "decode_f16_small"])
+                             "sparse_bf16", "sparse_select_bf16", "decode_f16_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -202,6 +202,25 @@ fa_status fa_kv_dequantize_int4(const uint8_t* q, const uint16_t* scale, int64_t
                                 float* out, fa_stream_t stream);
 
 /*
+ * Sparse row-list builder (v100llm article, section 5: anchor + recent + sink
+ * selection; the llama.cpp-v100 README's QSA reads such a subset of a long
+ * context).  For each slice s with n = min(n_len[s], n_max) positions
+ * (n_len NULL: n = n_max): positions 0 .. sinks-1, the k positions of
+ * [sinks, n - recent) with the largest score[s, pos], and n-recent .. n-1,
+ * in increasing position order, padded with -1.  Ties in score go to the
+ * smaller position; a NaN score ranks below every number.  Slices with no
+ * more than k middle positions list every position.
+ *   score    [S, n_max] fp32, caller-provided (the learned indexer that would
+ *            produce it is not part of this library)
+ *   row_map  [S, n_max] int32 position -> pool row, or NULL (row = position)
+ *   kv_rows  [S, list_len] int32 output; list_len >= sinks + recent + k
+ * One CTA per slice; the output is bit-exact (an integer selection).
+ */
+fa_status fa_kv_sparse_rows(const float* score, int32_t n_max, const int32_t* n_len, int32_t S, int32_t sinks,
+                            int32_t recent, int32_t k, const int32_t* row_map, int32_t* kv_rows, int32_t list_len,
+                            fa_stream_t stream);
+
+/*
  * KV append for 16-bit pools: pool[dst_rows[i]] = x[i] for i < n_rows
  * (negative dst = skip).  x and pool are [*, Hkv, D] of the same 16-bit dtype.
  */

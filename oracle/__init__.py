@@ -15,7 +15,8 @@ the listed rows (no lossy summary, no importance-based dropping).  The old
 path it replaces built a dense mask over the whole unified cache; that form is
 written out separately as ``attend_dense`` and serves as a cross-check.
 
-Paged INT8 KV with 64-token pages follows the v100llm article (sections 1-2).
+Paged INT8 KV with 64-token pages follows the v100llm article (sections 1-2);
+the sinks + recent + top-k row-list builder its section 5 (``select_rows``).
 
 Every function here is pinned by tests in ``tests/test_oracle_*.py`` against
 closed forms, invariants, brute force on tiny inputs and the dense-mask form;
@@ -28,3 +29,4 @@ from .kvcache import (  # noqa: F401
     widen_bf16, widen_f16, widen, quantize_int8, dequantize_int8, pack_scales, unpack_scales,
     page_table_to_rows, quantize_int4, dequantize_int4, append_rows,
 )
+from .sparse import select_rows  # noqa: F401

@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "FaRowsError", "lib", "library_path", "fa_rows_args", "fa_rows_workspace_size", "fa_rows_workspace_init",
     "fa_rows_decode", "fa_rows_prefill", "fa_rows_validate", "fa_kv_page_table_to_rows", "fa_kv_quantize_int8",
-    "fa_kv_dequantize_int8", "fa_kv_quantize_int4", "fa_kv_dequantize_int4", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
+    "fa_kv_dequantize_int8", "fa_kv_quantize_int4", "fa_kv_dequantize_int4", "fa_kv_sparse_rows", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
     "FA_F16", "FA_BF16", "FA_F32", "FA_I8", "FA_I4", "FA_MASK_NONE", "FA_MASK_DENSE", "FA_MASK_CAUSAL",
 ]
 
@@ -78,6 +78,8 @@ _SIGS = {
     "fa_kv_quantize_int4": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                            _P, ctypes.c_int64, _P]),
     "fa_kv_dequantize_int4": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "fa_kv_sparse_rows": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, _P, _P, ctypes.c_int32, _P]),
     "fa_kv_append": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                     ctypes.c_int64, _P]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -310,6 +312,20 @@ def fa_kv_dequantize_int4(q: torch.Tensor, scale: torch.Tensor, out=None, stream
     if out is None:
         out = torch.empty((R, Hkv, 2 * Dh), dtype=torch.float32, device=q.device)
     _check(lib().fa_kv_dequantize_int4(_ptr(q), _ptr(scale), R, Hkv, 2 * Dh, _ptr(out), _stream(stream, q.device)))
+    return out
+
+
+def fa_kv_sparse_rows(score: torch.Tensor, sinks: int, recent: int, k: int, list_len: Optional[int] = None,
+                      n_len=None, row_map=None, out=None, stream=None) -> torch.Tensor:
+    """Sorted kv_rows [S, list_len] of sinks + top-k(score) + recent per slice (score fp32 [S, n_max])."""
+    if score.dtype != torch.float32 or score.dim() != 2:
+        raise ValueError("score must be float32 [S, n_max]")
+    S, n_max = score.shape
+    L = sinks + recent + k if list_len is None else int(list_len)
+    if out is None:
+        out = torch.empty((S, L), dtype=torch.int32, device=score.device)
+    _check(lib().fa_kv_sparse_rows(_ptr(score), n_max, _ptr(n_len), S, sinks, recent, k, _ptr(row_map), _ptr(out),
+                                   L, _stream(stream, score.device)))
     return out
 
 

@@ -423,6 +423,22 @@ fa_status fa_kv_dequantize_int4(const uint8_t* q, const uint16_t* scale, int64_t
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "dequantize launch");
 }
 
+fa_status fa_kv_sparse_rows(const float* score, int32_t n_max, const int32_t* n_len, int32_t S, int32_t sinks,
+                            int32_t recent, int32_t k, const int32_t* row_map, int32_t* kv_rows, int32_t list_len,
+                            fa_stream_t stream) {
+  g_err[0] = 0;
+  if (S < 0 || n_max < 0 || sinks < 0 || recent < 0 || k < 0 || list_len < 0)
+    return fail(FA_ERR_INVALID_ARG, "negative size");
+  if ((long long)sinks + recent + k > list_len)
+    return fail(FA_ERR_INVALID_ARG, "list_len %d < sinks + recent + k = %lld", list_len,
+                (long long)sinks + recent + k);
+  if (S == 0 || list_len == 0) return FA_OK;
+  if (!kv_rows || (n_max > 0 && !score)) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
+  cudaError_t e = far::launch_sparse_rows(score, n_max, n_len, S, sinks, recent, k, row_map, kv_rows, list_len,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "sparse rows launch");
+}
+
 fa_status fa_kv_append(const void* x, fa_dtype dtype, int64_t n_rows, int32_t Hkv, int32_t D, const int32_t* dst_rows,
                        void* pool, int64_t n_pool_rows, fa_stream_t stream) {
   g_err[0] = 0;

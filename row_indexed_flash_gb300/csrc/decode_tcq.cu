@@ -320,6 +320,20 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       unsigned long long t_idle = 0;
       while (ok && npv < T) {
         bool progressed = false;
+        // PV of the oldest tile once its P is written: O_(tile parity) += P V
+        if (npv < nqk && mbar_test_wait(p_full + npv % NS, (npv / NS) & 1)) {
+          const int b = npv % NB, sb = npv % NS;
+          tc_fence_after();
+          const uint32_t vtile = sB + b * 2 * Sh::TILE + Sh::TILE;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tbase + Sh::COL_O + (npv & 1) * D, tbase + Sh::COL_S + sb * BN + kk * 8,
+                   sdesc_sw128(vtile + kk * 2048, Sh::KV_ATOM, 1024), id_pv, npv > 1 || kk > 0);
+          tc_commit(buf_empty + b);
+          tc_commit(o_ready + (npv & 1));
+          ++npv;
+          progressed = true;
+        }
         // QK of the next tile once its widened K/V are in a buffer and its S
         // buffer is free (the PV of the tile NS back has been issued)
         if (nqk < T && nqk < npv + NS && mbar_test_wait(buf_full + nqk % NB, (nqk / NB) & 1)) {
@@ -334,20 +348,6 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
           }
           tc_commit(s_full + sb);
           ++nqk;
-          progressed = true;
-        }
-        // PV of the oldest tile once its P is written: O_(tile parity) += P V
-        if (npv < nqk && mbar_test_wait(p_full + npv % NS, (npv / NS) & 1)) {
-          const int b = npv % NB, sb = npv % NS;
-          tc_fence_after();
-          const uint32_t vtile = sB + b * 2 * Sh::TILE + Sh::TILE;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tbase + Sh::COL_O + (npv & 1) * D, tbase + Sh::COL_S + sb * BN + kk * 8,
-                   sdesc_sw128(vtile + kk * 2048, Sh::KV_ATOM, 1024), id_pv, npv > 1 || kk > 0);
-          tc_commit(buf_empty + b);
-          tc_commit(o_ready + (npv & 1));
-          ++npv;
           progressed = true;
         }
         if (progressed) {

@@ -115,6 +115,8 @@ cudaError_t launch_dequantize_int4(const uint8_t* q, const uint16_t* scale, long
                                    float* out, cudaStream_t st);
 cudaError_t launch_kv_append(const void* x, long long n_rows, int row_bytes, const int32_t* dst, void* pool,
                              long long R, cudaStream_t st);
+cudaError_t launch_sparse_rows(const float* score, int n_max, const int32_t* n_len, int S, int sinks, int recent, int k,
+                               const int32_t* row_map, int32_t* rows, int list_len, cudaStream_t st);
 cudaError_t launch_validate(const int32_t* rows, const int32_t* kv_len, int S, int L, long long R,
                             long long* status, cudaStream_t st);
 
