@@ -319,7 +319,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
 
     lib = far.lib()
 
-    def step(i):
+    def step(i, sh=sh):
         if select:
             st = lib.fa_kv_sparse_rows(sel_score.data_ptr(), p.R, None, 1, 4, 512, 1532, None, rows.data_ptr(),
                                        rows.shape[1], sh)
@@ -338,6 +338,32 @@ def run_gpu(args, rank, world, p, cpu_baseline):
         step(i)
     torch.cuda.synchronize(dev)
 
+    # Each step's launches are captured once per pool copy in a CUDA graph
+    # and replayed: the small workloads are otherwise bound by host launch
+    # time.  The captured kernels and arguments are exactly those of step(i).
+    graphs = None
+    if not args.no_graph:
+        try:
+            graphs = []
+            for i in range(len(a_list)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    cap = torch.cuda.current_stream(dev).cuda_stream
+                    step(i, cap)
+                graphs.append(g)
+            for i in range(len(graphs)):
+                graphs[i].replay()
+            torch.cuda.synchronize(dev)
+        except Exception as exc:   # fall back to direct launches
+            print(f"# CUDA graph capture failed ({exc}); timing direct launches", file=sys.stderr)
+            graphs = None
+
+    def timed_step(i):
+        if graphs is not None:
+            graphs[i % len(graphs)].replay()
+        else:
+            step(i)
+
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
@@ -348,7 +374,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
         t0.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            step(i)
+            timed_step(i)
             ev[i][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
@@ -437,6 +463,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             "l2": (f"inputs larger than L2: {len(pools)} pool copies of {pool_bytes / 1e6:.0f} MB rotated"
                    if not is_prefill else f"pool {pool_bytes / 1e9:.2f} GB > L2"),
             "parallelism": f"replicas x{world}",
+            "launch": "cuda_graph" if graphs is not None else "direct",
         },
         "roofline": {
             "bound": bound,
@@ -477,6 +504,7 @@ def main():
                     choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int4",
                              "sparse_bf16", "sparse_select_bf16", "decode_f16_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

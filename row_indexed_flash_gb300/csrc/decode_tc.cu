@@ -41,6 +41,7 @@
 
 #include "merge.cuh"
 #include "tc.cuh"
+#include "tmap.cuh"
 #include "widen.cuh"
 
 namespace far {
@@ -688,29 +689,12 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 dk_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 bool dk_map(CUtensorMap* m, const void* base, bool bf16, int D, int Hkv, long long R) {
-  auto enc = dk_encode_fn();
-  if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)R};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * Hkv * 2};
   const cuuint32_t box[3] = {64, 1, (cuuint32_t)dk::BN};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
-             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return tmap_encode_3d(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, dims,
+                        strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int D, int QVP, int KQ, int NS>
@@ -762,7 +746,7 @@ bool decode_tc_supported(int D, int kind, int qv, int mask_kind) {
 // each; an INT8 stage keeps only half its bytes in flight (codes land in the
 // upper half of a 16-bit tile), so at D 128 the INT8 kernel runs one CTA per
 // SM with six stages.
-constexpr int dk_stages(int D, int KQ) { return KQ != 0 && D == 128 ? 6 : 3; }
+constexpr int dk_stages(int D, int KQ) { return KQ != 0 && D == 128 ? 6 : dk::NST; }
 
 static int qv_pow2(int qv) {
   int q = 1;

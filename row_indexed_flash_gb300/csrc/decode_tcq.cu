@@ -46,6 +46,7 @@
 
 #include "merge.cuh"
 #include "tc.cuh"
+#include "tmap.cuh"
 #include "widen.cuh"
 
 namespace far {
@@ -678,31 +679,13 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 dq_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 // Code pool [R][Hkv][CB bytes] as a 3-D byte tensor; box = CB bytes x one
 // head x 64 rows, unswizzled (the widen warps read it row-major).
 bool dq_map(CUtensorMap* m, const void* base, int CB, int Hkv, long long R) {
-  auto enc = dq_encode_fn();
-  if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)CB, (cuuint64_t)Hkv, (cuuint64_t)R};
   const cuuint64_t strides[2] = {(cuuint64_t)CB, (cuuint64_t)CB * Hkv};
   const cuuint32_t box[3] = {(cuuint32_t)CB, 1, (cuuint32_t)dq::BN};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return tmap_encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <int QVP, int KQ>
