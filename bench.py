@@ -69,7 +69,7 @@ PROFILE_FILES = {
 def decode_bytes(p, quant=None) -> int:
     """Algorithmic bytes: each listed row is read once per KV head (K and V
     codes, plus their two fp16 scales for a quantised pool)."""
-    per = {None: 4 * p.D, "int8": 2 * p.D + 4, "int4": p.D + 4}[quant]
+    per = {None: 4 * p.D, "int8": 2 * p.D + 4, "fp8": 2 * p.D + 4, "int4": p.D + 4}[quant]
     return p.n_valid() * p.Hkv * per
 
 
@@ -249,7 +249,7 @@ def build_problem(workload: str):
         return synth.decode_bf16_large()
     if workload == "prefill_bf16":
         return synth.prefill_bf16()
-    if workload in ("paged_int8", "paged_int4"):
+    if workload in ("paged_int8", "paged_int4", "paged_fp8"):
         return synth.paged_int8()   # the paged layout; the pool is quantised by the bench
     if workload in ("sparse_bf16", "sparse_select_bf16"):
         return synth.sparse_bf16()
@@ -277,8 +277,8 @@ def run_gpu(args, rank, world, p, cpu_baseline):
 
     is_prefill = args.workload.startswith("prefill")
     paged = p.kv_int8
-    quant = ("int4" if args.workload == "paged_int4" else "int8") if paged else None
-    quantise = far.fa_kv_quantize_int4 if quant == "int4" else far.fa_kv_quantize_int8
+    quant = {"paged_int4": "int4", "paged_fp8": "fp8"}.get(args.workload, "int8") if paged else None
+    quantise = {"int4": far.fa_kv_quantize_int4, "fp8": far.fa_kv_quantize_fp8}.get(quant, far.fa_kv_quantize_int8)
     q = to_dev(p.q)
     k0, v0 = to_dev(p.k), to_dev(p.v)
     scales = None
@@ -501,7 +501,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode_bf16",
-                    choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int4",
+                    choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int4", "paged_fp8",
                              "sparse_bf16", "sparse_select_bf16", "decode_f16_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")

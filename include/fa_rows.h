@@ -43,7 +43,7 @@ typedef enum fa_status {
   FA_ERR_CUDA = 5          /* a CUDA launch or runtime call failed              */
 } fa_status;
 
-typedef enum fa_dtype { FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2, FA_I8 = 3, FA_I4 = 4 } fa_dtype;
+typedef enum fa_dtype { FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2, FA_I8 = 3, FA_I4 = 4, FA_F8E4M3 = 5 } fa_dtype;
 
 typedef enum fa_mask_kind {
   FA_MASK_NONE = 0,
@@ -62,8 +62,9 @@ typedef enum fa_mask_kind {
  *   k, v     [R, Hkv, D]        the unified pool: FA_F16/FA_BF16 (same as q),
  *                               FA_I8 (int8 codes, then k_scale/v_scale), or
  *            [R, Hkv, D/2]      FA_I4 (two 4-bit codes per byte, element 2t in
- *                               the low nibble of byte t; D = 128 only)
- *   k_scale, v_scale            FA_I8/FA_I4 only: fp16 bit patterns laid out
+ *                               the low nibble of byte t; D = 128 only), or
+ *            [R, Hkv, D]        FA_F8E4M3 (OCP E4M3 bytes; D = 128 only)
+ *   k_scale, v_scale            quantised pools only: fp16 bit patterns laid out
  *                               [R/64, Hkv, 64], i.e. the scale of (row r,
  *                               head g) sits at ((r/64)*Hkv + g)*64 + r%64;
  *                               value = code * scale (R must be a multiple of 64)
@@ -200,6 +201,22 @@ fa_status fa_kv_quantize_int4(const void* x, fa_dtype x_dtype, int64_t n_rows, i
 /* out[r, g, d] = float(nibble code) * float(scale of (r, g)), exact in fp32. */
 fa_status fa_kv_dequantize_int4(const uint8_t* q, const uint16_t* scale, int64_t n_rows, int32_t Hkv, int32_t D,
                                 float* out, fa_stream_t stream);
+
+/*
+ * FP8 E4M3 KV quantisation.  "llama.cpp 0.9.0 inference boundaries"
+ * (section 4) adds the OCP FP8 E4M3 type in saturating mode and leaves its KV
+ * use and scaling to later work; the rule here mirrors the INT8 one:
+ * s = fp16_rne(min(amax/448, 65504)); code = E4M3 of x/s (one fp32 division,
+ * round to nearest even, saturating to +-448, NaN -> 0x7f); s = 0 gives 0.
+ *   q        [R, Hkv, D] E4M3 bytes; scale the fp16 layout of fa_rows_args.
+ */
+fa_status fa_kv_quantize_fp8(const void* x, fa_dtype x_dtype, int64_t n_rows, int32_t Hkv, int32_t D,
+                             const int32_t* dst_rows, uint8_t* q, uint16_t* scale, int64_t n_pool_rows,
+                             fa_stream_t stream);
+
+/* out[r, g, d] = float(E4M3 value of q[r, g, d]) * float(scale of (r, g)), exact in fp32. */
+fa_status fa_kv_dequantize_fp8(const uint8_t* q, const uint16_t* scale, int64_t n_rows, int32_t Hkv, int32_t D,
+                               float* out, fa_stream_t stream);
 
 /*
  * Sparse row-list builder (v100llm article, section 5: anchor + recent + sink

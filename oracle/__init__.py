@@ -28,5 +28,6 @@ from .attention import attend_rows, attend_dense, visible_positions  # noqa: F40
 from .kvcache import (  # noqa: F401
     widen_bf16, widen_f16, widen, quantize_int8, dequantize_int8, pack_scales, unpack_scales,
     page_table_to_rows, quantize_int4, dequantize_int4, append_rows,
+    e4m3_value, e4m3_encode, quantize_fp8, dequantize_fp8,
 )
 from .sparse import select_rows  # noqa: F401

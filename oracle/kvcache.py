@@ -178,3 +178,75 @@ def append_rows(pool: np.ndarray, new: np.ndarray, dst_rows: np.ndarray,
             pool[r] = qv[i]
             sc[r // PAGE, :, r % PAGE] = s[i]
     return pool, sc
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 codec ("llama.cpp 0.9.0 inference boundaries", section 4: the OCP
+# FP8 E4M3 type in saturating mode; the pages defer its use for the KV cache
+# and its scaling, so the reading here mirrors the INT8 one)
+#
+# * s = fp16(min(amax / 448, 65504)) (one fp32 division, round to nearest
+#   even), per (row, head); s == 0 gives code 0;
+# * code = E4M3(x / s): x / s one fp32 division, then round to nearest even on
+#   the E4M3 grid (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+#   subnormal step 2^-9, largest finite 448, no infinities), saturating to
+#   +-448; a NaN quotient gives the NaN code 0x7f;
+# * dequantisation is float32(E4M3 value) * float32(s), exact in fp32 (a 4-bit
+#   by 11-bit significand product).
+
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code: np.ndarray) -> np.ndarray:
+    """Value of each E4M3 byte (float64; NaN for the two NaN codes)."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    mag = np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(y: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the nearest E4M3 code (ties to even), saturating."""
+    y = np.asarray(y, dtype=np.float64)
+    out = np.zeros(y.shape, dtype=np.uint8)
+    nan = np.isnan(y)
+    sign = np.signbit(y)
+    a = np.minimum(np.abs(np.where(nan, 0.0, y)), E4M3_MAX)
+    # step of the grid around a: 2^-9 below the smallest normal 2^-6, else 2^(e-3)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    step = np.where(a < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3))
+    q = np.rint(a / step) * step            # exact: a / step is representable, rint ties to even
+    q = np.minimum(q, E4M3_MAX)
+    # encode the magnitude q
+    sub = q < 2.0 ** -6
+    qe = np.floor(np.log2(np.where(q > 0, q, 1.0)))
+    mant = np.where(sub, q / 2.0 ** -9, (q / 2.0 ** qe - 1.0) * 8.0)
+    expo = np.where(sub, 0, qe + 7)
+    code = (expo.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
+    code = np.where(sign, code | 0x80, code)
+    out[...] = code.astype(np.uint8)
+    out[nan] = 0x7F
+    return out
+
+
+def quantize_fp8(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """FP8 E4M3 per (row, head) with an fp16 scale; returns (codes uint8 [N, H, D], s float16 [N, H])."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    ratio = amax / np.float32(E4M3_MAX)
+    s16 = np.minimum(ratio, np.float32(65504.0)).astype(np.float16)
+    s32 = s16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        quot = x32 / s32
+    codes = e4m3_encode(quot)
+    codes = np.where(s32 == 0, np.uint8(0), codes)
+    return codes.astype(np.uint8), s16
+
+
+def dequantize_fp8(codes: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """float32(E4M3 value) * float32(s), exact in fp32."""
+    v = e4m3_value(codes).astype(np.float32)
+    return v * np.asarray(s, dtype=np.float16).astype(np.float32)[..., None]

@@ -22,11 +22,11 @@ import torch
 __all__ = [
     "FaRowsError", "lib", "library_path", "fa_rows_args", "fa_rows_workspace_size", "fa_rows_workspace_init",
     "fa_rows_decode", "fa_rows_prefill", "fa_rows_validate", "fa_kv_page_table_to_rows", "fa_kv_quantize_int8",
-    "fa_kv_dequantize_int8", "fa_kv_quantize_int4", "fa_kv_dequantize_int4", "fa_kv_sparse_rows", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
-    "FA_F16", "FA_BF16", "FA_F32", "FA_I8", "FA_I4", "FA_MASK_NONE", "FA_MASK_DENSE", "FA_MASK_CAUSAL",
+    "fa_kv_dequantize_int8", "fa_kv_quantize_int4", "fa_kv_dequantize_int4", "fa_kv_quantize_fp8", "fa_kv_dequantize_fp8", "fa_kv_sparse_rows", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
+    "FA_F16", "FA_BF16", "FA_F32", "FA_I8", "FA_I4", "FA_F8E4M3", "FA_MASK_NONE", "FA_MASK_DENSE", "FA_MASK_CAUSAL",
 ]
 
-FA_F16, FA_BF16, FA_F32, FA_I8, FA_I4 = 0, 1, 2, 3, 4
+FA_F16, FA_BF16, FA_F32, FA_I8, FA_I4, FA_F8E4M3 = 0, 1, 2, 3, 4, 5
 FA_MASK_NONE, FA_MASK_DENSE, FA_MASK_CAUSAL = 0, 1, 2
 _STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_WORKSPACE",
            4: "FA_ERR_INDEX_OOB", 5: "FA_ERR_CUDA"}
@@ -78,6 +78,9 @@ _SIGS = {
     "fa_kv_quantize_int4": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                            _P, ctypes.c_int64, _P]),
     "fa_kv_dequantize_int4": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "fa_kv_quantize_fp8": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                          _P, ctypes.c_int64, _P]),
+    "fa_kv_dequantize_fp8": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P]),
     "fa_kv_sparse_rows": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, _P, _P, ctypes.c_int32, _P]),
     "fa_kv_append": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
@@ -126,7 +129,8 @@ def _check(status: int):
 # ---------------------------------------------------------------------------
 # marshalling helpers
 
-_DT = {torch.float16: FA_F16, torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.int8: FA_I8, torch.uint8: FA_I4}
+_DT = {torch.float16: FA_F16, torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.int8: FA_I8, torch.uint8: FA_I4,
+       torch.float8_e4m3fn: FA_F8E4M3}
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -182,7 +186,7 @@ def make_args(q, k, v, kv_rows, scale, *, kv_len=None, mask=None, causal=False, 
         raise ValueError("kv_rows must be int32 [S, L]")
     if k.dtype != v.dtype:
         raise ValueError("k and v must share a dtype")
-    if k.dtype in (torch.int8, torch.uint8) and (k_scale is None or v_scale is None):
+    if k.dtype in (torch.int8, torch.uint8, torch.float8_e4m3fn) and (k_scale is None or v_scale is None):
         raise ValueError("a quantised pool needs k_scale and v_scale")
     if kv_len is not None and (kv_len.dtype != torch.int32 or kv_len.shape != (S,)):
         raise ValueError("kv_len must be int32 [S]")
@@ -312,6 +316,28 @@ def fa_kv_dequantize_int4(q: torch.Tensor, scale: torch.Tensor, out=None, stream
     if out is None:
         out = torch.empty((R, Hkv, 2 * Dh), dtype=torch.float32, device=q.device)
     _check(lib().fa_kv_dequantize_int4(_ptr(q), _ptr(scale), R, Hkv, 2 * Dh, _ptr(out), _stream(stream, q.device)))
+    return out
+
+
+def fa_kv_quantize_fp8(x: torch.Tensor, n_pool_rows: Optional[int] = None, dst_rows=None, q=None, scale=None,
+                       stream=None):
+    """Quantises x [n, Hkv, D] (bf16/f16) into an FP8 E4M3 pool; returns (q [R,Hkv,D] float8_e4m3fn, scale fp16)."""
+    n, Hkv, D = x.shape
+    R = n if n_pool_rows is None else int(n_pool_rows)
+    if q is None:
+        q = torch.zeros((R, Hkv, D), dtype=torch.float8_e4m3fn, device=x.device)
+    if scale is None:
+        scale = torch.zeros((R // 64, Hkv, 64), dtype=torch.float16, device=x.device)
+    _check(lib().fa_kv_quantize_fp8(_ptr(x), _DT[x.dtype], n, Hkv, D, _ptr(dst_rows), _ptr(q), _ptr(scale),
+                                    q.shape[0], _stream(stream, x.device)))
+    return q, scale
+
+
+def fa_kv_dequantize_fp8(q: torch.Tensor, scale: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    R, Hkv, D = q.shape
+    if out is None:
+        out = torch.empty((R, Hkv, D), dtype=torch.float32, device=q.device)
+    _check(lib().fa_kv_dequantize_fp8(_ptr(q), _ptr(scale), R, Hkv, D, _ptr(out), _stream(stream, q.device)))
     return out
 
 

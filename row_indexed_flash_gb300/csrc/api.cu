@@ -50,6 +50,7 @@ int kv_kind(fa_dtype d) {
     case FA_F16: return far::KV_F16;
     case FA_I8: return far::KV_I8;
     case FA_I4: return far::KV_I4;
+    case FA_F8E4M3: return far::KV_F8;
     default: return -1;
   }
 }
@@ -63,8 +64,8 @@ fa_status check_common(const fa_rows_args* a) {
   if (a->Hq % a->Hkv != 0) return fail(FA_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", a->Hq, a->Hkv);
   if (a->n_pool_rows > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "pool rows must fit int32 row indices");
   if (a->q_dtype != FA_F16 && a->q_dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "q dtype must be f16 or bf16");
-  if (kv_kind(a->kv_dtype) < 0) return fail(FA_ERR_UNSUPPORTED, "kv dtype must be f16, bf16, i8 or i4");
-  const bool quant = a->kv_dtype == FA_I8 || a->kv_dtype == FA_I4;
+  if (kv_kind(a->kv_dtype) < 0) return fail(FA_ERR_UNSUPPORTED, "kv dtype must be f16, bf16, i8, i4 or f8e4m3");
+  const bool quant = a->kv_dtype == FA_I8 || a->kv_dtype == FA_I4 || a->kv_dtype == FA_F8E4M3;
   if (!quant && a->kv_dtype != a->q_dtype) return fail(FA_ERR_UNSUPPORTED, "a 16-bit pool must have the dtype of q");
   if (a->out_dtype != FA_F32 && a->out_dtype != FA_BF16 && a->out_dtype != FA_F16)
     return fail(FA_ERR_UNSUPPORTED, "out dtype must be f32, bf16 or f16");
@@ -119,8 +120,8 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   pl->tcq = far::decode_tcq_supported(a->D, kind, qv1, a->mask_kind) && aligned(a->q, 16);
   pl->tc = pl->tcq || (far::decode_tc_supported(a->D, kind, qv1, a->mask_kind) && aligned(a->q, 16) &&
                        a->n_pool_rows * a->Hkv < 0x7fffffffLL);  // TMA rows are int32 coordinates r * Hkv + g
-  if (kind == far::KV_I4 && !pl->tcq)
-    return fail(FA_ERR_UNSUPPORTED, "INT4 pools are decoded at D=128 with at most 32 query vectors and no dense mask");
+  if ((kind == far::KV_I4 || kind == far::KV_F8) && !pl->tcq)
+    return fail(FA_ERR_UNSUPPORTED, "INT4/FP8 pools are decoded at D=128 with at most 32 query vectors and no dense mask");
   pl->qvp = qvp;
   pl->rows = pl->tc ? (int)qv : qvp;
   int align = 0, chunk_max = 0;
@@ -420,6 +421,33 @@ fa_status fa_kv_dequantize_int4(const uint8_t* q, const uint16_t* scale, int64_t
   if (n_rows == 0) return FA_OK;
   if (!q || !scale || !out) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
   cudaError_t e = far::launch_dequantize_int4(q, scale, n_rows, Hkv, D, out, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "dequantize launch");
+}
+
+fa_status fa_kv_quantize_fp8(const void* x, fa_dtype x_dtype, int64_t n_rows, int32_t Hkv, int32_t D,
+                             const int32_t* dst_rows, uint8_t* q, uint16_t* scale, int64_t n_pool_rows,
+                             fa_stream_t stream) {
+  g_err[0] = 0;
+  if (x_dtype != FA_BF16 && x_dtype != FA_F16) return fail(FA_ERR_UNSUPPORTED, "x must be bf16 or f16");
+  if (n_rows < 0 || Hkv <= 0 || D <= 0 || D > 256 || n_pool_rows < 0)
+    return fail(FA_ERR_INVALID_ARG, "bad sizes (n_rows=%lld Hkv=%d D=%d)", (long long)n_rows, Hkv, D);
+  if (n_pool_rows % far::kPage) return fail(FA_ERR_UNSUPPORTED, "FP8 pool rows must be a multiple of 64");
+  if (!dst_rows && n_rows > n_pool_rows) return fail(FA_ERR_INVALID_ARG, "identity append needs n_rows <= pool rows");
+  if (n_rows == 0) return FA_OK;
+  if (!x || !q || !scale) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
+  cudaError_t e = far::launch_quantize_fp8(x, x_dtype == FA_BF16, n_rows, Hkv, D, dst_rows, q, scale, n_pool_rows,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "quantize launch");
+}
+
+fa_status fa_kv_dequantize_fp8(const uint8_t* q, const uint16_t* scale, int64_t n_rows, int32_t Hkv, int32_t D,
+                               float* out, fa_stream_t stream) {
+  g_err[0] = 0;
+  if (n_rows < 0 || Hkv <= 0 || D <= 0) return fail(FA_ERR_INVALID_ARG, "bad sizes");
+  if (n_rows % far::kPage) return fail(FA_ERR_UNSUPPORTED, "FP8 pool rows must be a multiple of 64");
+  if (n_rows == 0) return FA_OK;
+  if (!q || !scale || !out) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
+  cudaError_t e = far::launch_dequantize_fp8(q, scale, n_rows, Hkv, D, out, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "dequantize launch");
 }
 

@@ -1,5 +1,5 @@
-// Split-KV decode over row-indexed lists for quantised pools (INT8 or INT4
-// codes with one fp16 scale per (row, KV head)), head_dim 128, on the
+// Split-KV decode over row-indexed lists for quantised pools (INT8, INT4 or
+// FP8 E4M3 codes with one fp16 scale per (row, KV head)), head_dim 128, on the
 // 5th-generation tensor cores.
 //
 // The operation ("llama.cpp 0.9.0 inference boundaries", section 1) is the
@@ -79,10 +79,10 @@ __device__ __forceinline__ int widen_slot(int warp) {
 }
 }  // namespace dq
 
-// KQ: 1 = INT8 codes, 2 = INT4 codes (two per byte).
+// KQ: 1 = INT8 codes, 2 = INT4 codes (two per byte), 3 = FP8 E4M3 codes.
 template <int QVP, int KQ>
 struct DqShape {
-  static constexpr int CB = KQ == 1 ? dq::D : dq::D / 2;   // code bytes of one (row, head)
+  static constexpr int CB = KQ == 2 ? dq::D / 2 : dq::D;   // code bytes of one (row, head)
   static constexpr int CPR = CB / 16;                      // their 16-byte chunks
   static constexpr int QATOM = dq::QROWS * 128;
   static constexpr int Q_BYTES = 2 * QATOM;
@@ -622,10 +622,15 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
             __half2 x2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), sv2);
             return *reinterpret_cast<uint32_t*>(&x2);
           };
-          if constexpr (KQ == 1) {
+          if constexpr (KQ == 1 || KQ == 3) {
             // 16 codes = columns 16q .. 16q+15: two 16-byte chunks of atom q / 4
-            const uint2 a = widen_i8x4(cw.x, bf16), b1 = widen_i8x4(cw.y, bf16);
-            const uint2 c2 = widen_i8x4(cw.z, bf16), d = widen_i8x4(cw.w, bf16);
+            uint2 a, b1, c2, d;
+            if constexpr (KQ == 1) {
+              a = widen_i8x4(cw.x, bf16), b1 = widen_i8x4(cw.y, bf16);
+              c2 = widen_i8x4(cw.z, bf16), d = widen_i8x4(cw.w, bf16);
+            } else {
+              a = widen_e4m3x4(cw.x), b1 = widen_e4m3x4(cw.y), c2 = widen_e4m3x4(cw.z), d = widen_e4m3x4(cw.w);
+            }
             unsigned char* rowp = tile + (q / 4) * Sh::KV_ATOM + e * 128;
             const int k0 = 2 * (q % 4);
             *reinterpret_cast<uint4*>(rowp + ((k0 ^ (e & 7)) << 4)) = make_uint4(vs(a.x), vs(a.y), vs(b1.x), vs(b1.y));
@@ -753,15 +758,20 @@ cudaError_t dq_launch_q(int qvp, const DecodeParams& a, unsigned int* err, cudaS
 }  // namespace
 
 bool decode_tcq_supported(int D, int kind, int qv, int mask_kind) {
-  return D == dq::D && (kind == KV_I8 || kind == KV_I4) && qv >= 1 && qv <= dq::QROWS && mask_kind != FA_MASK_DENSE;
+  return D == dq::D && (kind == KV_I8 || kind == KV_I4 || kind == KV_F8) && qv >= 1 && qv <= dq::QROWS &&
+         mask_kind != FA_MASK_DENSE;
 }
 
 int decode_tcq_occupancy(int kind, int qv) {
-  return kind == KV_I4 ? dq_occupancy_q<2>(dq_pow2(qv)) : dq_occupancy_q<1>(dq_pow2(qv));
+  if (kind == KV_I4) return dq_occupancy_q<2>(dq_pow2(qv));
+  if (kind == KV_F8) return dq_occupancy_q<3>(dq_pow2(qv));
+  return dq_occupancy_q<1>(dq_pow2(qv));
 }
 
 cudaError_t decode_tcq_launch(const DecodeParams& a, int kind, unsigned int* err, cudaStream_t st) {
-  return kind == KV_I4 ? dq_launch_q<2>(dq_pow2(a.QV), a, err, st) : dq_launch_q<1>(dq_pow2(a.QV), a, err, st);
+  if (kind == KV_I4) return dq_launch_q<2>(dq_pow2(a.QV), a, err, st);
+  if (kind == KV_F8) return dq_launch_q<3>(dq_pow2(a.QV), a, err, st);
+  return dq_launch_q<1>(dq_pow2(a.QV), a, err, st);
 }
 
 }  // namespace far

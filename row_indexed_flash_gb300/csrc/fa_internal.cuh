@@ -11,7 +11,7 @@
 namespace far {
 
 // KV storage kinds the kernels are built for.
-enum KvKind { KV_BF16 = 0, KV_F16 = 1, KV_I8 = 2, KV_I4 = 3 };
+enum KvKind { KV_BF16 = 0, KV_F16 = 1, KV_I8 = 2, KV_I4 = 3, KV_F8 = 4 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -71,7 +71,7 @@ int decode_tc_occupancy(int D, int kind, int qv);
 int decode_tc_tile();
 cudaError_t decode_tc_launch(const DecodeParams& p, int D, int kind, unsigned int* err, cudaStream_t st);
 
-// Tensor-core decode for quantised pools (INT8 / INT4 codes + fp16 scales),
+// Tensor-core decode for quantised pools (INT8 / INT4 / FP8 codes + fp16 scales),
 // D 128: one CTA per SM with a deep code ring.  Same workspace as above.
 bool decode_tcq_supported(int D, int kind, int qv, int mask_kind);
 int decode_tcq_occupancy(int kind, int qv);
@@ -113,6 +113,10 @@ cudaError_t launch_quantize_int4(const void* x, int x_bf16, long long n_rows, in
                                  uint8_t* q, uint16_t* scale, long long R, cudaStream_t st);
 cudaError_t launch_dequantize_int4(const uint8_t* q, const uint16_t* scale, long long n_rows, int Hkv, int D,
                                    float* out, cudaStream_t st);
+cudaError_t launch_quantize_fp8(const void* x, int x_bf16, long long n_rows, int Hkv, int D, const int32_t* dst,
+                                uint8_t* q, uint16_t* scale, long long R, cudaStream_t st);
+cudaError_t launch_dequantize_fp8(const uint8_t* q, const uint16_t* scale, long long n_rows, int Hkv, int D,
+                                  float* out, cudaStream_t st);
 cudaError_t launch_kv_append(const void* x, long long n_rows, int row_bytes, const int32_t* dst, void* pool,
                              long long R, cudaStream_t st);
 cudaError_t launch_sparse_rows(const float* score, int n_max, const int32_t* n_len, int S, int sinks, int recent, int k,

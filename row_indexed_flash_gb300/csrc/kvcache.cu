@@ -1,9 +1,10 @@
-// KV-pool kernels: page-table expansion, INT8 / INT4 quantise / dequantise, 16-bit
+// KV-pool kernels: page-table expansion, INT8 / INT4 / FP8 quantise / dequantise, 16-bit
 // row appends and the row-list range check.
 //
 // Paged KV with 64-token pages and INT8 storage: v100llm article, sections
 // 1-2.  Negative row = padding: "llama.cpp 0.9.0 inference boundaries",
 // section 1.
+#include <cuda_fp8.h>
 #include <limits.h>
 
 #include "fa_internal.cuh"
@@ -197,6 +198,86 @@ cudaError_t launch_dequantize_int4(const uint8_t* q, const uint16_t* scale, long
   long long blocks = (n + threads - 1) / threads;
   if (blocks > 152 * 64) blocks = 152 * 64;
   dequantize_int4_kernel<<<(unsigned)blocks, threads, 0, st>>>(q, scale, n_rows, Hkv, D, out);
+  return cudaGetLastError();
+}
+
+// One warp per (source row, head), FP8 E4M3: s = fp16(min(amax/448, 65504)),
+// code = the saturating round-to-nearest-even E4M3 of x/s (one fp32 division);
+// s = 0 gives code 0.
+__global__ void quantize_fp8_kernel(const uint16_t* __restrict__ x, int x_bf16, long long n_rows, int Hkv, int D,
+                                    const int32_t* __restrict__ dst_rows, uint8_t* __restrict__ q,
+                                    uint16_t* __restrict__ scale, long long R) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+  for (long long w = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5); w < n_rows * Hkv; w += warps) {
+    const long long i = w / Hkv;
+    const int g = (int)(w % Hkv);
+    const long long dst = dst_rows ? (long long)dst_rows[i] : i;
+    if (dst < 0 || dst >= R) continue;
+    const uint16_t* src = x + (size_t)w * D;
+    float vals[8];
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int d = lane + 32 * u;
+      float f = 0.f;
+      if (d < D) {
+        const uint32_t b = src[d];
+        f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
+      }
+      vals[u] = f;
+      amax = fmaxf(amax, fabsf(f));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const __half sh = __float2half_rn(fminf(__fdiv_rn(amax, 448.0f), 65504.0f));
+    const float sf = __half2float(sh);
+    uint8_t* qd = q + ((size_t)dst * Hkv + g) * D;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int d = lane + 32 * u;
+      if (d < D)
+        qd[d] = sf != 0.f ? (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(vals[u], sf), __NV_SATFINITE, __NV_E4M3) : 0;
+    }
+    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = __half_as_ushort(sh);
+  }
+}
+
+cudaError_t launch_quantize_fp8(const void* x, int x_bf16, long long n_rows, int Hkv, int D, const int32_t* dst,
+                                uint8_t* q, uint16_t* scale, long long R, cudaStream_t st) {
+  const long long warps = n_rows * Hkv;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (warps + 7) / 8;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  quantize_fp8_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint16_t*>(x), x_bf16, n_rows, Hkv, D,
+                                                            dst, q, scale, R);
+  return cudaGetLastError();
+}
+
+// out = float(E4M3 value) * float(scale), exact in fp32.
+__global__ void dequantize_fp8_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ scale,
+                                      long long n_rows, int Hkv, int D, float* __restrict__ out) {
+  const long long n = n_rows * Hkv * D;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n; t += (long long)gridDim.x * blockDim.x) {
+    const long long rh = t / D;
+    const long long r = rh / Hkv;
+    const int g = (int)(rh % Hkv);
+    const __half_raw hv = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)q[t], __NV_E4M3);
+    const float v = __half2float(__half(hv));
+    const float sf = __half2float(__ushort_as_half(scale[((size_t)(r / kPage) * Hkv + g) * kPage + (r % kPage)]));
+    out[t] = __fmul_rn(v, sf);
+  }
+}
+
+cudaError_t launch_dequantize_fp8(const uint8_t* q, const uint16_t* scale, long long n_rows, int Hkv, int D,
+                                  float* out, cudaStream_t st) {
+  const long long n = n_rows * Hkv * D;
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (n + threads - 1) / threads;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  dequantize_fp8_kernel<<<(unsigned)blocks, threads, 0, st>>>(q, scale, n_rows, Hkv, D, out);
   return cudaGetLastError();
 }
 

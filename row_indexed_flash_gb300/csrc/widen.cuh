@@ -2,6 +2,8 @@
 // shared by the tensor-core decode kernels.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "fa_internal.cuh"
 
 namespace far {
@@ -67,6 +69,14 @@ __device__ __forceinline__ uint4 widen_i4x8(uint32_t w, bool bf16) {
   const uint2 a = widen_u4x4(__byte_perm(even, odd, 0x5140u), bf16);     // elements 0..3
   const uint2 b = widen_u4x4(__byte_perm(even, odd, 0x7362u), bf16);     // elements 4..7
   return make_uint4(a.x, a.y, b.x, b.y);
+}
+
+// Four FP8 E4M3 codes (one word, element t in byte t) -> four f16 values,
+// exact (every E4M3 value is an f16 value).
+__device__ __forceinline__ uint2 widen_e4m3x4(uint32_t w) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  return make_uint2((uint32_t)lo.x | ((uint32_t)lo.y << 16), (uint32_t)hi.x | ((uint32_t)hi.y << 16));
 }
 
 }  // namespace far
