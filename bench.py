@@ -299,6 +299,8 @@ def run_gpu(args, rank, world, p, cpu_baseline):
         # each step builds the list (4 sinks + 1,532 by score + 512 recent) from a
         # seeded fp32 score per position, then decodes over it
         sel_score = torch.from_numpy(synth.rng(9).standard_normal((1, p.R)).astype(np.float32)).to(dev)
+        sel_ws = torch.empty(max(far.lib().fa_kv_sparse_rows_workspace_size(1, p.R), 16), dtype=torch.uint8,
+                             device=dev)
     pool_bytes = 2 * k0.numel() * k0.element_size()
     # rotate over enough pool copies that each step reads data not left in L2
     n_copies = max(1, min(3, int(math.ceil(3 * 129e6 / pool_bytes)) + 1)) if not is_prefill else 1
@@ -322,7 +324,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
     def step(i, sh=sh):
         if select:
             st = lib.fa_kv_sparse_rows(sel_score.data_ptr(), p.R, None, 1, 4, 512, 1532, None, rows.data_ptr(),
-                                       rows.shape[1], sh)
+                                       rows.shape[1], sel_ws.data_ptr(), sel_ws.numel(), sh)
             if st != 0:
                 raise far.FaRowsError(st, far.fa_last_error())
         if paged:   # page tables -> row lists, then the decode (both kernels of the step)

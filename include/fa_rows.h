@@ -231,11 +231,16 @@ fa_status fa_kv_dequantize_fp8(const uint8_t* q, const uint16_t* scale, int64_t 
  *            produce it is not part of this library)
  *   row_map  [S, n_max] int32 position -> pool row, or NULL (row = position)
  *   kv_rows  [S, list_len] int32 output; list_len >= sinks + recent + k
- * One CTA per slice; the output is bit-exact (an integer selection).
+ *   ws       scratch of fa_kv_sparse_rows_workspace_size(S, n_max) bytes
+ *            (16-byte aligned; its contents need no initialisation): each
+ *            slice is then spread over blocks of 8192 positions (several
+ *            launches on the stream).  NULL: one CTA per slice, no scratch.
+ * The output is bit-exact (an integer selection) either way.
  */
+size_t fa_kv_sparse_rows_workspace_size(int32_t S, int32_t n_max);
 fa_status fa_kv_sparse_rows(const float* score, int32_t n_max, const int32_t* n_len, int32_t S, int32_t sinks,
                             int32_t recent, int32_t k, const int32_t* row_map, int32_t* kv_rows, int32_t list_len,
-                            fa_stream_t stream);
+                            void* ws, size_t ws_bytes, fa_stream_t stream);
 
 /*
  * KV append for 16-bit pools: pool[dst_rows[i]] = x[i] for i < n_rows

@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "FaRowsError", "lib", "library_path", "fa_rows_args", "fa_rows_workspace_size", "fa_rows_workspace_init",
     "fa_rows_decode", "fa_rows_prefill", "fa_rows_validate", "fa_kv_page_table_to_rows", "fa_kv_quantize_int8",
-    "fa_kv_dequantize_int8", "fa_kv_quantize_int4", "fa_kv_dequantize_int4", "fa_kv_quantize_fp8", "fa_kv_dequantize_fp8", "fa_kv_sparse_rows", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
+    "fa_kv_dequantize_int8", "fa_kv_quantize_int4", "fa_kv_dequantize_int4", "fa_kv_quantize_fp8", "fa_kv_dequantize_fp8", "fa_kv_sparse_rows_workspace_size", "fa_kv_sparse_rows", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
     "FA_F16", "FA_BF16", "FA_F32", "FA_I8", "FA_I4", "FA_F8E4M3", "FA_MASK_NONE", "FA_MASK_DENSE", "FA_MASK_CAUSAL",
 ]
 
@@ -81,8 +81,9 @@ _SIGS = {
     "fa_kv_quantize_fp8": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                           _P, ctypes.c_int64, _P]),
     "fa_kv_dequantize_fp8": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "fa_kv_sparse_rows_workspace_size": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
     "fa_kv_sparse_rows": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                         ctypes.c_int32, _P, _P, ctypes.c_int32, _P]),
+                                         ctypes.c_int32, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "fa_kv_append": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                     ctypes.c_int64, _P]),
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -342,16 +343,26 @@ def fa_kv_dequantize_fp8(q: torch.Tensor, scale: torch.Tensor, out=None, stream=
 
 
 def fa_kv_sparse_rows(score: torch.Tensor, sinks: int, recent: int, k: int, list_len: Optional[int] = None,
-                      n_len=None, row_map=None, out=None, stream=None) -> torch.Tensor:
-    """Sorted kv_rows [S, list_len] of sinks + top-k(score) + recent per slice (score fp32 [S, n_max])."""
+                      n_len=None, row_map=None, out=None, workspace="auto", stream=None) -> torch.Tensor:
+    """Sorted kv_rows [S, list_len] of sinks + top-k(score) + recent per slice (score fp32 [S, n_max]).
+
+    workspace: "auto" allocates the multi-block scratch, None runs one block
+    per slice without scratch, or a uint8 tensor of at least
+    fa_kv_sparse_rows_workspace_size(S, n_max) bytes.
+    """
     if score.dtype != torch.float32 or score.dim() != 2:
         raise ValueError("score must be float32 [S, n_max]")
     S, n_max = score.shape
     L = sinks + recent + k if list_len is None else int(list_len)
     if out is None:
         out = torch.empty((S, L), dtype=torch.int32, device=score.device)
+    if isinstance(workspace, str):
+        nbytes = lib().fa_kv_sparse_rows_workspace_size(S, n_max)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=score.device)
+    wptr = _ptr(workspace)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().fa_kv_sparse_rows(_ptr(score), n_max, _ptr(n_len), S, sinks, recent, k, _ptr(row_map), _ptr(out),
-                                   L, _stream(stream, score.device)))
+                                   L, wptr, wbytes, _stream(stream, score.device)))
     return out
 
 

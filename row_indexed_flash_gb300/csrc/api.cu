@@ -451,9 +451,15 @@ fa_status fa_kv_dequantize_fp8(const uint8_t* q, const uint16_t* scale, int64_t 
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "dequantize launch");
 }
 
+size_t fa_kv_sparse_rows_workspace_size(int32_t S, int32_t n_max) {
+  g_err[0] = 0;
+  if (S <= 0 || n_max < 0) return 0;
+  return far::sparse_rows_workspace(S, n_max);
+}
+
 fa_status fa_kv_sparse_rows(const float* score, int32_t n_max, const int32_t* n_len, int32_t S, int32_t sinks,
                             int32_t recent, int32_t k, const int32_t* row_map, int32_t* kv_rows, int32_t list_len,
-                            fa_stream_t stream) {
+                            void* ws, size_t ws_bytes, fa_stream_t stream) {
   g_err[0] = 0;
   if (S < 0 || n_max < 0 || sinks < 0 || recent < 0 || k < 0 || list_len < 0)
     return fail(FA_ERR_INVALID_ARG, "negative size");
@@ -462,8 +468,16 @@ fa_status fa_kv_sparse_rows(const float* score, int32_t n_max, const int32_t* n_
                 (long long)sinks + recent + k);
   if (S == 0 || list_len == 0) return FA_OK;
   if (!kv_rows || (n_max > 0 && !score)) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
-  cudaError_t e = far::launch_sparse_rows(score, n_max, n_len, S, sinks, recent, k, row_map, kv_rows, list_len,
-                                          reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (ws) {
+    const size_t need = far::sparse_rows_workspace(S, n_max);
+    if (ws_bytes < need || !aligned(ws, 16))
+      return fail(FA_ERR_WORKSPACE, "sparse rows workspace must be %zu bytes, 16-byte aligned", need);
+    e = far::launch_sparse_rows_ws(score, n_max, n_len, S, sinks, recent, k, row_map, kv_rows, list_len, ws, st);
+  } else {
+    e = far::launch_sparse_rows(score, n_max, n_len, S, sinks, recent, k, row_map, kv_rows, list_len, st);
+  }
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "sparse rows launch");
 }
 

@@ -121,6 +121,10 @@ cudaError_t launch_kv_append(const void* x, long long n_rows, int row_bytes, con
                              long long R, cudaStream_t st);
 cudaError_t launch_sparse_rows(const float* score, int n_max, const int32_t* n_len, int S, int sinks, int recent, int k,
                                const int32_t* row_map, int32_t* rows, int list_len, cudaStream_t st);
+size_t sparse_rows_workspace(int S, int n_max);
+cudaError_t launch_sparse_rows_ws(const float* score, int n_max, const int32_t* n_len, int S, int sinks, int recent,
+                                  int k, const int32_t* row_map, int32_t* rows, int list_len, void* ws,
+                                  cudaStream_t st);
 cudaError_t launch_validate(const int32_t* rows, const int32_t* kv_len, int S, int L, long long R,
                             long long* status, cudaStream_t st);
 

@@ -228,7 +228,254 @@ __global__ void __launch_bounds__(kSelThreads) sparse_rows_kernel(const float* _
   for (int j = out_at + tid; j < list_len; j += kSelThreads) out[j] = -1;
 }
 
+// ---------------------------------------------------------------------------
+// Multi-CTA form (with a workspace): the same selection, each slice spread
+// over blocks of kChunk middle positions.  Three histogram passes add block
+// histograms into global ones, each followed by a one-warp pick of the next
+// digit; a count pass and an ordered write pass place the chosen positions.
+
+constexpr int kChunk = 8192;        // middle positions per block
+constexpr int kMThreads = 1024;     // kChunk / 8 positions per thread
+
+struct SliceGeom {
+  int n, lo, hi, m, kk;
+  bool take_all;
+};
+
+__device__ __forceinline__ SliceGeom slice_geom(int s, int n_max, const int32_t* n_len, int sinks, int recent, int k) {
+  SliceGeom q;
+  q.n = n_len ? min(max(__ldg(n_len + s), 0), n_max) : n_max;
+  q.lo = min(sinks, q.n);
+  q.hi = max(q.lo, q.n - recent);
+  q.m = q.hi - q.lo;
+  q.kk = min(k, q.m);
+  q.take_all = q.kk == q.m;
+  return q;
+}
+
+// workspace of one slice: hist[3][kSelBins], state[4] (prefix, remaining), counts[nblk][2] (above, equal)
+__device__ __forceinline__ int* ws_hist(int* ws, int s, int nblk, int pass) {
+  return ws + (size_t)s * (3 * kSelBins + 4 + 2 * nblk) + pass * kSelBins;
+}
+__device__ __forceinline__ int* ws_state(int* ws, int s, int nblk) {
+  return ws + (size_t)s * (3 * kSelBins + 4 + 2 * nblk) + 3 * kSelBins;
+}
+__device__ __forceinline__ int* ws_counts(int* ws, int s, int nblk) { return ws_state(ws, s, nblk) + 4; }
+
+__device__ __forceinline__ float load_score(const float* sc, int pos) { return __ldg(sc + pos); }
+
+template <int PASS>
+__global__ void __launch_bounds__(kMThreads) sparse_hist_kernel(const float* __restrict__ score, int n_max,
+                                                                const int32_t* __restrict__ n_len, int sinks,
+                                                                int recent, int k, int* __restrict__ ws, int nblk) {
+  __shared__ int hist[4][kSelBins];
+  const int s = blockIdx.y, b = blockIdx.x, tid = threadIdx.x;
+  const SliceGeom q = slice_geom(s, n_max, n_len, sinks, recent, k);
+  if (q.take_all || q.kk == 0) return;
+  const int c0 = q.lo + b * kChunk;
+  if (c0 >= q.hi) return;
+  const int c1 = min(q.hi, c0 + kChunk);
+  constexpr int shift = PASS == 0 ? 21 : (PASS == 1 ? 10 : 0);
+  constexpr uint32_t bmask = PASS == 2 ? 0x3ffu : 0x7ffu;
+  constexpr uint32_t mask = PASS == 0 ? 0u : (PASS == 1 ? 0xffe00000u : 0xfffffc00u);
+  const uint32_t prefix = PASS == 0 ? 0u : (uint32_t)ws_state(ws, s, nblk)[0];
+  for (int t = tid; t < 4 * kSelBins; t += kMThreads) (&hist[0][0])[t] = 0;
+  __syncthreads();
+  int* my = hist[(tid >> 5) & 3];
+  const float* sc = score + (size_t)s * n_max;
+#pragma unroll
+  for (int u = 0; u < kChunk / kMThreads; ++u) {
+    const int pos = c0 + u * kMThreads + tid;
+    const bool in = pos < c1;
+    const uint32_t key = in ? order_key(load_score(sc, pos)) : 0u;
+    const bool live = in && (key & mask) == prefix;
+    const uint32_t bin = live ? (key >> shift) & bmask : 0xffffffffu;
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (live && (tid & 31) == __ffs(peers) - 1) atomicAdd(&my[bin], __popc(peers));
+  }
+  __syncthreads();
+  int* gh = ws_hist(ws, s, nblk, PASS);
+  for (int t = tid; t < kSelBins; t += kMThreads) {
+    const int v = hist[0][t] + hist[1][t] + hist[2][t] + hist[3][t];
+    if (v) atomicAdd(gh + t, v);
+  }
+}
+
+// One warp per slice: the digit of PASS where the count from the top reaches
+// the number still to take; state <- (prefix with that digit, remaining).
+template <int PASS>
+__global__ void sparse_pick_kernel(int n_max, const int32_t* __restrict__ n_len, int sinks, int recent, int k,
+                                   int* __restrict__ ws, int nblk) {
+  const int s = blockIdx.x, lane = threadIdx.x;
+  const SliceGeom q = slice_geom(s, n_max, n_len, sinks, recent, k);
+  if (q.take_all || q.kk == 0) return;
+  constexpr int shift = PASS == 0 ? 21 : (PASS == 1 ? 10 : 0);
+  int* st = ws_state(ws, s, nblk);
+  const int* gh = ws_hist(ws, s, nblk, PASS);
+  const uint32_t prefix = PASS == 0 ? 0u : (uint32_t)st[0];
+  const int remaining = PASS == 0 ? q.kk : st[1];
+  const int b0 = 64 * (31 - lane);
+  int local = 0;
+  for (int t = 0; t < 64; ++t) local += gh[b0 + t];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int above = incl - local;
+  if (above < remaining && incl >= remaining) {
+    int cum = above;
+    for (int t = 63; t >= 0; --t) {
+      const int c = gh[b0 + t];
+      if (cum + c >= remaining) {
+        st[0] = (int)(prefix | ((uint32_t)(b0 + t) << shift));
+        st[1] = remaining - cum;
+        break;
+      }
+      cum += c;
+    }
+  }
+}
+
+// Per block: keys above the threshold and keys equal to it.
+__global__ void __launch_bounds__(kMThreads) sparse_count_kernel(const float* __restrict__ score, int n_max,
+                                                                 const int32_t* __restrict__ n_len, int sinks,
+                                                                 int recent, int k, int* __restrict__ ws, int nblk) {
+  __shared__ int red[2];
+  const int s = blockIdx.y, b = blockIdx.x, tid = threadIdx.x;
+  const SliceGeom q = slice_geom(s, n_max, n_len, sinks, recent, k);
+  const int c0 = q.lo + b * kChunk;
+  const int c1 = min(q.hi, c0 + kChunk);
+  if (tid < 2) red[tid] = 0;
+  __syncthreads();
+  const uint32_t T = q.kk == 0 ? 0xffffffffu : (uint32_t)ws_state(ws, s, nblk)[0];
+  int above = 0, equal = 0;
+  if (c0 < q.hi) {
+    const float* sc = score + (size_t)s * n_max;
+    for (int pos = c0 + tid; pos < c1; pos += kMThreads) {
+      const uint32_t key = order_key(load_score(sc, pos));
+      above += q.take_all || key > T;
+      equal += !q.take_all && key == T;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    above += __shfl_xor_sync(0xffffffffu, above, o);
+    equal += __shfl_xor_sync(0xffffffffu, equal, o);
+  }
+  if ((tid & 31) == 0) {
+    atomicAdd(&red[0], above);
+    atomicAdd(&red[1], equal);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int* cnt = ws_counts(ws, s, nblk);
+    cnt[2 * b] = red[0];
+    cnt[2 * b + 1] = red[1];
+  }
+}
+
+// Per block: its chosen positions at their place in the list (after the
+// sinks and the earlier blocks' choices); block 0 also writes the sinks, the
+// recent positions and the padding.
+__global__ void __launch_bounds__(kMThreads) sparse_write_kernel(const float* __restrict__ score, int n_max,
+                                                                 const int32_t* __restrict__ n_len, int sinks,
+                                                                 int recent, int k,
+                                                                 const int32_t* __restrict__ row_map,
+                                                                 int32_t* __restrict__ rows, int list_len,
+                                                                 const int* __restrict__ ws, int nblk) {
+  __shared__ int warp_sums[32];
+  __shared__ int base[2];
+  const int s = blockIdx.y, b = blockIdx.x, tid = threadIdx.x;
+  const SliceGeom q = slice_geom(s, n_max, n_len, sinks, recent, k);
+  const int32_t* map = row_map ? row_map + (size_t)s * n_max : nullptr;
+  int32_t* out = rows + (size_t)s * list_len;
+  auto row_of = [&](int pos) { return map ? __ldg(map + pos) : pos; };
+  const int* st = ws_state(const_cast<int*>(ws), s, nblk);
+  const uint32_t T = (q.take_all || q.kk == 0) ? 0xffffffffu : (uint32_t)st[0];
+  const int need_eq = (q.take_all || q.kk == 0) ? 0 : st[1];
+  if (b == 0) {
+    for (int pos = tid; pos < q.lo; pos += kMThreads) out[pos] = row_of(pos);
+    const int r0 = q.lo + q.kk;
+    for (int pos = q.hi + tid; pos < q.n; pos += kMThreads) out[r0 + (pos - q.hi)] = row_of(pos);
+    for (int jj = r0 + (q.n - q.hi) + tid; jj < list_len; jj += kMThreads) out[jj] = -1;
+  }
+  const int c0 = q.lo + b * kChunk;
+  if (c0 >= q.hi) return;
+  const int c1 = min(q.hi, c0 + kChunk);
+  if (tid == 0) {
+    // output position and equal keys before this block
+    const int* cnt = ws_counts(const_cast<int*>(ws), s, nblk);
+    int at = q.lo, eq_seen = 0;
+    for (int bb = 0; bb < b; ++bb) {
+      const int a = cnt[2 * bb], e = cnt[2 * bb + 1];
+      at += a + min(e, max(need_eq - eq_seen, 0));
+      eq_seen += e;
+    }
+    base[0] = at;
+    base[1] = eq_seen;
+  }
+  __syncthreads();
+  const float* sc = score + (size_t)s * n_max;
+  constexpr int PER = kChunk / kMThreads;
+  const int p0 = c0 + tid * PER;
+  uint32_t keys[PER];
+  int n_eq = 0;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int pos = p0 + u;
+    keys[u] = pos < c1 ? order_key(load_score(sc, pos)) : 0u;
+    n_eq += (pos < c1 && !q.take_all && keys[u] == T) ? 1 : 0;
+  }
+  int eq_total = 0;
+  int eq_before = base[1] + block_exclusive_scan(n_eq, warp_sums, &eq_total);
+  unsigned sel_bits = 0u;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int pos = p0 + u;
+    if (pos >= c1) continue;
+    bool sel = q.take_all || keys[u] > T;
+    if (!q.take_all && keys[u] == T) {
+      sel = eq_before < need_eq;
+      ++eq_before;
+    }
+    sel_bits |= (sel ? 1u : 0u) << u;
+  }
+  int sel_total = 0;
+  int at = base[0] + block_exclusive_scan(__popc(sel_bits), warp_sums, &sel_total);
+#pragma unroll
+  for (int u = 0; u < PER; ++u)
+    if ((sel_bits >> u) & 1u) out[at++] = row_of(p0 + u);
+}
+
 }  // namespace
+
+size_t sparse_rows_workspace(int S, int n_max) {
+  const int nblk = n_max > 0 ? (n_max + kChunk - 1) / kChunk : 1;
+  return (size_t)S * (3 * kSelBins + 4 + 2 * nblk) * sizeof(int);
+}
+
+cudaError_t launch_sparse_rows_ws(const float* score, int n_max, const int32_t* n_len, int S, int sinks, int recent,
+                                  int k, const int32_t* row_map, int32_t* rows, int list_len, void* ws,
+                                  cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  const int nblk = n_max > 0 ? (n_max + kChunk - 1) / kChunk : 1;
+  cudaError_t e = cudaMemsetAsync(ws, 0, sparse_rows_workspace(S, n_max), st);
+  if (e != cudaSuccess) return e;
+  int* w = static_cast<int*>(ws);
+  const dim3 grid(nblk, S);
+  sparse_hist_kernel<0><<<grid, kMThreads, 0, st>>>(score, n_max, n_len, sinks, recent, k, w, nblk);
+  sparse_pick_kernel<0><<<S, 32, 0, st>>>(n_max, n_len, sinks, recent, k, w, nblk);
+  sparse_hist_kernel<1><<<grid, kMThreads, 0, st>>>(score, n_max, n_len, sinks, recent, k, w, nblk);
+  sparse_pick_kernel<1><<<S, 32, 0, st>>>(n_max, n_len, sinks, recent, k, w, nblk);
+  sparse_hist_kernel<2><<<grid, kMThreads, 0, st>>>(score, n_max, n_len, sinks, recent, k, w, nblk);
+  sparse_pick_kernel<2><<<S, 32, 0, st>>>(n_max, n_len, sinks, recent, k, w, nblk);
+  sparse_count_kernel<<<grid, kMThreads, 0, st>>>(score, n_max, n_len, sinks, recent, k, w, nblk);
+  sparse_write_kernel<<<grid, kMThreads, 0, st>>>(score, n_max, n_len, sinks, recent, k, row_map, rows, list_len, w,
+                                                  nblk);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_sparse_rows(const float* score, int n_max, const int32_t* n_len, int S, int sinks, int recent, int k,
                                const int32_t* row_map, int32_t* rows, int list_len, cudaStream_t st) {

@@ -24,6 +24,7 @@ def _scores(seed, S, n, ties=False, nan_frac=0.0):
     return sc
 
 
+@pytest.mark.parametrize("ws", ["auto", None])
 @pytest.mark.parametrize("case", [
     dict(S=3, n=1000, sinks=4, recent=16, k=37, ties=True),
     dict(S=2, n=5000, sinks=0, recent=0, k=100),
@@ -35,7 +36,7 @@ def _scores(seed, S, n, ties=False, nan_frac=0.0):
     dict(S=3, n=4099, sinks=3, recent=5, k=77, ties=True),           # rows not 16-byte aligned
     dict(S=1, n=70001, sinks=5, recent=7, k=1000, nan_frac=0.01),
 ])
-def test_sparse_rows_match_oracle(case):
+def test_sparse_rows_match_oracle(case, ws):
     S, n = case["S"], case["n"]
     sc = _scores(100 + S + n, S, n, case.get("ties", False), case.get("nan_frac", 0.0))
     n_len = None
@@ -44,7 +45,7 @@ def test_sparse_rows_match_oracle(case):
     L = case["sinks"] + case["recent"] + case["k"] + 3   # some padding
     want = oracle.select_rows(sc, case["sinks"], case["recent"], case["k"], L, n_len=n_len)
     got = far.fa_kv_sparse_rows(torch.from_numpy(sc).cuda(), case["sinks"], case["recent"], case["k"], L,
-                                n_len=None if n_len is None else torch.from_numpy(n_len).cuda())
+                                n_len=None if n_len is None else torch.from_numpy(n_len).cuda(), workspace=ws)
     assert np.array_equal(got.cpu().numpy(), want)
 
 
@@ -64,12 +65,16 @@ def test_sparse_rows_at_the_sparse_workload_size_then_decode():
     want = oracle.select_rows(sc, 4, 512, 1532, 2048)
     rows = far.fa_kv_sparse_rows(torch.from_numpy(sc).cuda(), 4, 512, 1532)
     assert np.array_equal(rows.cpu().numpy(), want)
+    assert np.array_equal(far.fa_kv_sparse_rows(torch.from_numpy(sc).cuda(), 4, 512, 1532, workspace=None).cpu().numpy(),
+                          want)
     out, _ = far.fa_rows_decode(dev_bits(p.q, "bf16"), dev_bits(p.k, "bf16"), dev_bits(p.v, "bf16"), rows, p.scale)
     ref, _ = oracle_for(p, kv_rows=want)
     assert_parity(out, ref, "built sparse list")
 
 
-def test_sparse_rows_reject_a_short_list():
+def test_sparse_rows_reject_a_short_list_and_a_short_workspace():
     sc = torch.zeros((1, 100), dtype=torch.float32, device="cuda")
     with pytest.raises(far.FaRowsError):
         far.fa_kv_sparse_rows(sc, 4, 4, 10, list_len=17)
+    with pytest.raises(far.FaRowsError):
+        far.fa_kv_sparse_rows(sc, 4, 4, 10, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
