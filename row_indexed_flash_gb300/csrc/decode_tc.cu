@@ -639,9 +639,6 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
           t_idle = 0;
           continue;
         }
-        // idle: back off briefly so this lane's polling does not take issue
-        // slots from the gather warp sharing its scheduler
-        __nanosleep(32);
         if (t_idle == 0) {
           t_idle = globaltimer();
         } else if (*abort_flag) {
