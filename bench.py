@@ -59,6 +59,7 @@ PROFILE_FILES = {
     "prefill_bf16": "profiles/prefill_bf16_4x2048x99936_ncu.txt",
     "prefill_bf16_small": "profiles/prefill_bf16_4x2048x16384_ncu.txt",
     "paged_int8": "profiles/paged_int8_32seq_ncu.txt",
+    "paged_int8_small": "profiles/paged_int8_16seq_ncu.txt",
 }
 
 
@@ -251,6 +252,9 @@ def build_problem(workload: str):
         return synth.prefill_bf16()
     if workload in ("paged_int8", "paged_int4", "paged_fp8"):
         return synth.paged_int8()   # the paged layout; the pool is quantised by the bench
+    if workload == "paged_int8_small":
+        # profiling size: 16 sequences of 1k-32k tokens (about 250 MB of codes, above L2)
+        return synth.paged_int8(n_seq=16, lo=1024, hi=32768)
     if workload in ("sparse_bf16", "sparse_select_bf16"):
         return synth.sparse_bf16()
     if workload == "decode_f16_small":
@@ -503,7 +507,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode_bf16",
-                    choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int4", "paged_fp8",
+                    choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int8_small",
+                             "paged_int4", "paged_fp8",
                              "sparse_bf16", "sparse_select_bf16", "decode_f16_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
