@@ -409,7 +409,10 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < NST; ++i) {
-      mbar_init(kv_full + i, NPROD);   // one arrival per producer warp (warp 0's may carry TMA bytes)
+      // 16-bit pools: one arrival per producer lane (asynchronous, when its
+      // copies land; lane 0 of warp 1 may carry TMA bytes instead).  INT8:
+      // one per producer warp, after it has widened its rows in place.
+      mbar_init(kv_full + i, KQ == 0 ? NPROD * 32 : NPROD);
       mbar_init(kv_empty + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -457,113 +460,47 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
     }
-    static_assert(KQ != 0 || NST == 3, "the TMA path tracks three stages in scalars");
-    unsigned gathered = 0;   // bit t % 32: this warp gathered its rows of tile t (arrival due at publish)
-    unsigned tma_pend = 0;   // bit st: a TMA load into stage st may still be in flight (warp 0)
-    int use0 = 0, use1 = 0, use2 = 0;
-    int nrow0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // next tile's rows, one tile ahead
-    int nrow1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
-    int published = 0;
-    auto publish = [&](int t) {
-      if ((gathered >> (t & 31)) & 1u) {
-        if constexpr (KQ != 0) {
-          // widen this warp's rows of the stage in place: every lane reads
-          // the code chunks it copied itself, then writes their 16-bit values
-          constexpr int NIT = ROWS * Sh::CPRQ / 32;
+    if constexpr (KQ == 0) {
+      // Each lane's copies arrive on the stage's barrier by themselves when
+      // they land (the MMA thread orders them for the tensor core with a
+      // proxy fence), so a warp never waits for its loads: it issues tile j
+      // as soon as the PV of tile j - NST has freed the stage, and all NST
+      // stages can be in flight at once.
+      unsigned tma_pend = 0, tma_par = 0;   // stages with a TMA load issued, and its phase parity (warp 1)
+      int nrow0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // next tile's rows, one tile ahead
+      int nrow1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
+      for (int j = 0; j < T; ++j) {
+        const int st = j % NST, u = j / NST;
+        if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
+        int rows[2] = {nrow0, nrow1};
 #pragma unroll
-          for (int mat = 0; mat < 2; ++mat) {
-            unsigned char* tile = sm + (mat ? Sh::OFF_V : Sh::OFF_K) + (t % NST) * Sh::TILE;
-            uint4 cw[NIT];
-#pragma unroll
-            for (int it = 0; it < NIT; ++it) {
-              const int f = it * 32 + lane;
-              const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
-              cw[it] = *reinterpret_cast<const uint4*>(tile + (Sh::A0 + c / 8) * Sh::KV_ATOM + e * 128 +
-                                                       (((c & 7) ^ (e & 7)) << 4));
-            }
-            __syncwarp();
-#pragma unroll
-            for (int it = 0; it < NIT; ++it) {
-              const int f = it * 32 + lane;
-              const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
-              // 16 codes = columns 16c .. 16c+15: two 16-byte chunks of atom c / 4
-              const uint2 a = widen_i8x4(cw[it].x, bf16), b = widen_i8x4(cw[it].y, bf16);
-              const uint2 cc = widen_i8x4(cw[it].z, bf16), d = widen_i8x4(cw[it].w, bf16);
-              unsigned char* row = tile + (c / 4) * Sh::KV_ATOM + e * 128;
-              const int k0 = 2 * (c % 4);
-              *reinterpret_cast<uint4*>(row + ((k0 ^ (e & 7)) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
-              *reinterpret_cast<uint4*>(row + (((k0 + 1) ^ (e & 7)) << 4)) = make_uint4(cc.x, cc.y, d.x, d.y);
-            }
-            __syncwarp();
-          }
+        for (int t = 0; t < 2; ++t)
+          if (rows[t] < 0 || (long long)rows[t] >= p.R) rows[t] = -1;
+        {
+          const int pos = (j + 1) * BN + lane;
+          nrow0 = pos < cnt ? __ldg(rows_g + pos) : -1;
+          nrow1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(kv_full + t % NST);
-      }
-    };
-    for (int j = 0; j < T; ++j) {
-      const int st = j % NST, u = j / NST;
-      // publish tile j - (NST - 1) before waiting for stage st: the MMA needs
-      // it before it can free that stage
-      if (j >= NST - 1) {
-        cp_async_wait<NST - 2>();
-        publish(j - (NST - 1));
-        published = j - (NST - 1) + 1;
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
-      int rows[2] = {nrow0, nrow1};
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (rows[t] < 0 || (long long)rows[t] >= p.R) rows[t] = -1;
-      {
-        const int pos = (j + 1) * BN + lane;
-        nrow0 = pos < cnt ? __ldg(rows_g + pos) : -1;
-        nrow1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
-      }
-      unsigned char* Ks = sm + Sh::OFF_K + st * Sh::TILE;
-      unsigned char* Vs = sm + Sh::OFF_V + st * Sh::TILE;
-      if constexpr (KQ != 0) {
-        // codes of this warp's rows -> the upper atoms of row e, chunk c swizzled as the tile
-#pragma unroll
-        for (int it = 0; it < ROWS * Sh::CPRQ / 32; ++it) {
-          const int f = it * 32 + lane;
-          const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
-          const int ra = __shfl_sync(0xffffffffu, rows[0], e & 31);
-          const int rb = __shfl_sync(0xffffffffu, rows[1], e & 31);
-          const int r = e < 32 ? ra : rb;
-          const bool okr = r >= 0;
-          const size_t go = ((size_t)(okr ? r : 0) * p.Hkv + g) * Sh::CB + c * 16;
-          const uint32_t so = (Sh::A0 + c / 8) * Sh::KV_ATOM + e * 128 + (((c & 7) ^ (e & 7)) << 4);
-          cp_async16(Ks + so, kb + go, okr);
-          cp_async16(Vs + so, vb + go, okr);
-        }
-        gathered |= 1u << (j & 31);
-        cp_async_commit();
-        continue;
-      }
-      const int r0 = __shfl_sync(0xffffffffu, rows[0], 0);
-      bool contig = rows[0] >= 0 && rows[0] == r0 + lane && rows[1] >= 0 && rows[1] == r0 + lane + 32;
-      contig = __all_sync(0xffffffffu, contig) && kp.tma_kv;
-      if (contig) {
-        if (pw == 0) {
-          if (lane == 0) {
+        unsigned char* Ks = sm + Sh::OFF_K + st * Sh::TILE;
+        unsigned char* Vs = sm + Sh::OFF_V + st * Sh::TILE;
+        const int r0 = __shfl_sync(0xffffffffu, rows[0], 0);
+        bool contig = rows[0] >= 0 && rows[0] == r0 + lane && rows[1] >= 0 && rows[1] == r0 + lane + 32;
+        contig = __all_sync(0xffffffffu, contig) && kp.tma_kv;
+        if (contig) {
+          if (pw == 0 && lane == 0) {
             mbar_arrive_expect_tx(kv_full + st, 2 * Sh::TILE);
 #pragma unroll
             for (int a = 0; a < Sh::KT; ++a) {
               tma_load_3d(Ks + a * Sh::KV_ATOM, &tk, a * 64, g, r0, kv_full + st);
               tma_load_3d(Vs + a * Sh::KV_ATOM, &tv, a * 64, g, r0, kv_full + st);
             }
+          } else {
+            mbar_arrive(kv_full + st);
           }
           tma_pend |= 1u << st;
-          if (st == 0) use0 = u;
-          else if (st == 1) use1 = u;
-          else use2 = u;
-        } else if (lane == 0) {
-          mbar_arrive(kv_full + st);   // this warp has no part in a TMA tile
+          tma_par = (tma_par & ~(1u << st)) | ((unsigned)(u & 1) << st);
+          continue;
         }
-        gathered &= ~(1u << (j & 31));
-      } else {
         // this warp's rows pw*ROWS .. pw*ROWS+ROWS-1: 16 lanes cover one row
 #pragma unroll 4
         for (int it = 0; it < ROWS * CPR / 32; ++it) {
@@ -578,17 +515,93 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
           cp_async16(Ks + so, kb + go, okr);
           cp_async16(Vs + so, vb + go, okr);
         }
-        gathered |= 1u << (j & 31);
+        cp_async_mbar_arrive_noinc(kv_full + st);
       }
-      cp_async_commit();   // one group per tile (empty for TMA tiles)
-    }
-    cp_async_wait<0>();
-    if (!*abort_flag)
-      for (int t = published; t < T; ++t) publish(t);
-    if (pw == 0 && lane == 0 && *abort_flag) {
-      if (tma_pend & 1u) wait_drain(kv_full + 0, use0 & 1);
-      if (tma_pend & 2u) wait_drain(kv_full + 1, use1 & 1);
-      if (tma_pend & 4u) wait_drain(kv_full + 2, use2 & 1);
+      cp_async_wait_all();
+      if (pw == 0 && lane == 0 && *abort_flag) {   // no TMA load may still be writing when the CTA exits
+        for (int c = 0; c < NST; ++c)
+          if ((tma_pend >> c) & 1u) wait_drain(kv_full + c, (tma_par >> c) & 1u);
+      }
+    } else {
+      // INT8 codes: each warp widens its rows of a stage in place once they
+      // have landed, then publishes it, NST - 1 tiles after issuing it.
+      int nrow0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // next tile's rows, one tile ahead
+      int nrow1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
+      int published = 0;
+      auto publish = [&](int t) {
+        // every lane reads the code chunks it copied itself, then writes
+        // their 16-bit values
+        constexpr int NIT = ROWS * Sh::CPRQ / 32;
+#pragma unroll
+        for (int mat = 0; mat < 2; ++mat) {
+          unsigned char* tile = sm + (mat ? Sh::OFF_V : Sh::OFF_K) + (t % NST) * Sh::TILE;
+          uint4 cw[NIT];
+#pragma unroll
+          for (int it = 0; it < NIT; ++it) {
+            const int f = it * 32 + lane;
+            const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
+            cw[it] = *reinterpret_cast<const uint4*>(tile + (Sh::A0 + c / 8) * Sh::KV_ATOM + e * 128 +
+                                                     (((c & 7) ^ (e & 7)) << 4));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < NIT; ++it) {
+            const int f = it * 32 + lane;
+            const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
+            // 16 codes = columns 16c .. 16c+15: two 16-byte chunks of atom c / 4
+            const uint2 a = widen_i8x4(cw[it].x, bf16), b = widen_i8x4(cw[it].y, bf16);
+            const uint2 cc = widen_i8x4(cw[it].z, bf16), d = widen_i8x4(cw[it].w, bf16);
+            unsigned char* row = tile + (c / 4) * Sh::KV_ATOM + e * 128;
+            const int k0 = 2 * (c % 4);
+            *reinterpret_cast<uint4*>(row + ((k0 ^ (e & 7)) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+            *reinterpret_cast<uint4*>(row + (((k0 + 1) ^ (e & 7)) << 4)) = make_uint4(cc.x, cc.y, d.x, d.y);
+          }
+          __syncwarp();
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kv_full + t % NST);
+      };
+      for (int j = 0; j < T; ++j) {
+        const int st = j % NST, u = j / NST;
+        // publish tile j - (NST - 1) before waiting for stage st: the MMA
+        // needs it before it can free that stage
+        if (j >= NST - 1) {
+          cp_async_wait<NST - 2>();
+          publish(j - (NST - 1));
+          published = j - (NST - 1) + 1;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
+        int rows[2] = {nrow0, nrow1};
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (rows[t] < 0 || (long long)rows[t] >= p.R) rows[t] = -1;
+        {
+          const int pos = (j + 1) * BN + lane;
+          nrow0 = pos < cnt ? __ldg(rows_g + pos) : -1;
+          nrow1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
+        }
+        unsigned char* Ks = sm + Sh::OFF_K + st * Sh::TILE;
+        unsigned char* Vs = sm + Sh::OFF_V + st * Sh::TILE;
+        // codes of this warp's rows -> the upper atoms of row e, chunk c swizzled as the tile
+#pragma unroll
+        for (int it = 0; it < ROWS * Sh::CPRQ / 32; ++it) {
+          const int f = it * 32 + lane;
+          const int e = pw * ROWS + f / Sh::CPRQ, c = f % Sh::CPRQ;
+          const int ra = __shfl_sync(0xffffffffu, rows[0], e & 31);
+          const int rb = __shfl_sync(0xffffffffu, rows[1], e & 31);
+          const int r = e < 32 ? ra : rb;
+          const bool okr = r >= 0;
+          const size_t go = ((size_t)(okr ? r : 0) * p.Hkv + g) * Sh::CB + c * 16;
+          const uint32_t so = (Sh::A0 + c / 8) * Sh::KV_ATOM + e * 128 + (((c & 7) ^ (e & 7)) << 4);
+          cp_async16(Ks + so, kb + go, okr);
+          cp_async16(Vs + so, vb + go, okr);
+        }
+        cp_async_commit();
+      }
+      cp_async_wait<0>();
+      if (!*abort_flag)
+        for (int t = published; t < T; ++t) publish(t);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
@@ -610,6 +623,9 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
         if (nqk < T && nqk < npv + 2 && mbar_test_wait(kv_full + nqk % NST, (nqk / NST) & 1)) {
           const int st = nqk % NST, b = nqk & 1;
           tc_fence_after();
+          // 16-bit stages are written by cp.async copies that arrived on
+          // kv_full by themselves: order them before the tensor core's reads
+          if constexpr (KQ == 0) fence_proxy_async_smem();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t a_off = (kk >> 2) * Sh::QATOM + (kk & 3) * 32;
