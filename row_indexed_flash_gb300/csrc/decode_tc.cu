@@ -606,7 +606,11 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && T > 0) {
-      const uint32_t id_qk = make_idesc_f16(128, BN, bf16, false);
+      // With at most 16 query vectors their S rows fit an M=64 product (rows
+      // 0-15 land in tensor-memory lanes 0-15), which the tensor pipe runs in
+      // about two thirds of the M=128 time at N=64; PV stays at M=128, where
+      // M=64 takes as long.
+      const uint32_t id_qk = make_idesc_f16(QVP <= 16 ? 64 : 128, BN, bf16, false);
       const uint32_t id_pv = make_idesc_f16(128, D, bf16, true);
       const uint32_t sQ = smem_u32(sm + Sh::OFF_Q), sK = smem_u32(sm + Sh::OFF_K), sV = smem_u32(sm + Sh::OFF_V);
       const uint32_t tO = tbase + Sh::COL_O;
