@@ -50,7 +50,7 @@ namespace dk {
 constexpr int BN = 64;       // list entries per tile
 constexpr int QROWS = 32;    // query-vector rows kept in shared memory
 constexpr int NST = 3;       // K/V stages of the 16-bit kernel (2 CTAs per SM)
-constexpr int NPROD = 4;     // producer warps (each gathers BN / NPROD rows of every tile)
+constexpr int NPROD = 4;     // producer warps (16-bit pools: two gather K, two V)
 constexpr int NWARP = 2 + NPROD;   // softmax, producers, MMA
 constexpr int MMA_WARP = 1 + NPROD;
 }  // namespace dk
@@ -68,8 +68,8 @@ struct DkShape {
   static constexpr int OFF_K = ((Q_BYTES + 1023) / 1024) * 1024;
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_BAR = OFF_V + NS * TILE;
-  // q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_ready, drain
-  static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1;
+  // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2], o_ready, drain
+  static constexpr int NBAR = 1 + 4 * NS + 2 + 2 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // S rows of the real query vectors (fp32), then in the same place their P
   // rows (packed 16-bit pairs: BN/2 words of P_hi, BN/2 of P_lo).  The softmax
@@ -384,9 +384,13 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + NST;
-  uint64_t* s_full = kv_empty + NST;
+  // K and V stages fill and drain separately: a K stage is free once the QK
+  // has read it, a V stage once the PV has
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NST;
+  uint64_t* k_empty = v_full + NST;
+  uint64_t* v_empty = k_empty + NST;
+  uint64_t* s_full = v_empty + NST;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_ready = p_full + 2;
   uint64_t* drain = o_ready + 1;
@@ -409,11 +413,14 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < NST; ++i) {
-      // 16-bit pools: one arrival per producer lane (asynchronous, when its
-      // copies land; lane 0 of warp 1 may carry TMA bytes instead).  INT8:
-      // one per producer warp, after it has widened its rows in place.
-      mbar_init(kv_full + i, KQ == 0 ? NPROD * 32 : NPROD);
-      mbar_init(kv_empty + i, 1);
+      // 16-bit pools: one arrival per lane of the two warps gathering the
+      // matrix (asynchronous, when its copies land; a TMA tile's bytes ride
+      // on the first lane's).  INT8: one per producer warp on both, after it
+      // has widened its rows of K and V in place.
+      mbar_init(k_full + i, KQ == 0 ? 64 : NPROD);
+      mbar_init(v_full + i, KQ == 0 ? 64 : NPROD);
+      mbar_init(k_empty + i, 1);
+      mbar_init(v_empty + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
@@ -437,12 +444,11 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
     // ------------------------------------------------------------ producers
     // Gathered rows are fetched with cp.async by NPROD warps (the load/store
     // path sustains far more independent row requests than one warp or the
-    // TMA gather unit); each warp publishes its part of a tile NST - 1 tiles
-    // after issuing it, once its copies have landed.  A tile whose 64 listed
-    // rows form one contiguous pool run is loaded by TMA tile loads instead.
+    // TMA gather unit).  A tile whose 64 listed rows form one contiguous pool
+    // run is loaded by TMA tile loads instead.
     const int pw = warp - 1;
     constexpr int CPR = D / 8;                  // 16-byte chunks per (row, head)
-    constexpr int ROWS = BN / NPROD;            // rows per producer warp
+    constexpr int ROWS = BN / NPROD;            // rows per producer warp (INT8)
     const char* kb = static_cast<const char*>(p.k);
     const char* vb = static_cast<const char*>(p.v);
     if (pw == 0 && T > 0) {
@@ -461,17 +467,26 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       if (lane == 0) mbar_arrive(q_full);
     }
     if constexpr (KQ == 0) {
-      // Each lane's copies arrive on the stage's barrier by themselves when
-      // they land (the MMA thread orders them for the tensor core with a
-      // proxy fence), so a warp never waits for its loads: it issues tile j
-      // as soon as the PV of tile j - NST has freed the stage, and all NST
-      // stages can be in flight at once.
-      unsigned tma_pend = 0, tma_par = 0;   // stages with a TMA load issued, and its phase parity (warp 1)
+      // Warps 1-2 gather K, warps 3-4 gather V, 32 rows of each tile per
+      // warp.  Each lane's copies arrive on the stage's barrier by
+      // themselves when they land (the MMA thread orders them for the tensor
+      // core with a proxy fence), so a warp never waits for its loads: it
+      // issues tile j as soon as the QK (K) or PV (V) of tile j - NST has
+      // freed the stage.
+      const bool isv = pw >= 2;
+      const int gw = pw & 1;
+      constexpr int GROWS = BN / 2;   // rows per warp of a group
+      uint64_t* full = isv ? v_full : k_full;
+      uint64_t* empty = isv ? v_empty : k_empty;
+      unsigned char* const mat = sm + (isv ? Sh::OFF_V : Sh::OFF_K);
+      const char* const src = isv ? vb : kb;
+      const void* const tmap = isv ? static_cast<const void*>(&tv) : static_cast<const void*>(&tk);
+      unsigned tma_pend = 0, tma_par = 0;   // stages with a TMA load issued, and its phase parity (gw 0, lane 0)
       int nrow0 = lane < cnt ? __ldg(rows_g + lane) : -1;   // next tile's rows, one tile ahead
       int nrow1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
       for (int j = 0; j < T; ++j) {
         const int st = j % NST, u = j / NST;
-        if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(empty + st, (u & 1) ^ 1, abort_flag))) break;
         int rows[2] = {nrow0, nrow1};
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -481,46 +496,40 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
           nrow0 = pos < cnt ? __ldg(rows_g + pos) : -1;
           nrow1 = pos + 32 < cnt ? __ldg(rows_g + pos + 32) : -1;
         }
-        unsigned char* Ks = sm + Sh::OFF_K + st * Sh::TILE;
-        unsigned char* Vs = sm + Sh::OFF_V + st * Sh::TILE;
+        unsigned char* dst = mat + st * Sh::TILE;
         const int r0 = __shfl_sync(0xffffffffu, rows[0], 0);
         bool contig = rows[0] >= 0 && rows[0] == r0 + lane && rows[1] >= 0 && rows[1] == r0 + lane + 32;
         contig = __all_sync(0xffffffffu, contig) && kp.tma_kv;
         if (contig) {
-          if (pw == 0 && lane == 0) {
-            mbar_arrive_expect_tx(kv_full + st, 2 * Sh::TILE);
+          if (gw == 0 && lane == 0) {
+            mbar_arrive_expect_tx(full + st, Sh::TILE);
 #pragma unroll
-            for (int a = 0; a < Sh::KT; ++a) {
-              tma_load_3d(Ks + a * Sh::KV_ATOM, &tk, a * 64, g, r0, kv_full + st);
-              tma_load_3d(Vs + a * Sh::KV_ATOM, &tv, a * 64, g, r0, kv_full + st);
-            }
+            for (int a = 0; a < Sh::KT; ++a) tma_load_3d(dst + a * Sh::KV_ATOM, tmap, a * 64, g, r0, full + st);
           } else {
-            mbar_arrive(kv_full + st);
+            mbar_arrive(full + st);
           }
           tma_pend |= 1u << st;
           tma_par = (tma_par & ~(1u << st)) | ((unsigned)(u & 1) << st);
           continue;
         }
-        // this warp's rows pw*ROWS .. pw*ROWS+ROWS-1: 16 lanes cover one row
+        // this warp's rows gw*GROWS .. gw*GROWS+GROWS-1: 16 (D/8) lanes cover one row
 #pragma unroll 4
-        for (int it = 0; it < ROWS * CPR / 32; ++it) {
+        for (int it = 0; it < GROWS * CPR / 32; ++it) {
           const int f = it * 32 + lane;
-          const int e = pw * ROWS + f / CPR, c = f % CPR;
+          const int e = gw * GROWS + f / CPR, c = f % CPR;
           const int ra = __shfl_sync(0xffffffffu, rows[0], e & 31);
           const int rb = __shfl_sync(0xffffffffu, rows[1], e & 31);
           const int r = e < 32 ? ra : rb;
           const bool okr = r >= 0;
           const size_t go = ((size_t)(okr ? r : 0) * p.Hkv + g) * (D * 2) + c * 16;
-          const uint32_t so = (c >> 3) * Sh::KV_ATOM + e * 128 + (((c & 7) ^ (e & 7)) << 4);
-          cp_async16(Ks + so, kb + go, okr);
-          cp_async16(Vs + so, vb + go, okr);
+          cp_async16(dst + (c >> 3) * Sh::KV_ATOM + e * 128 + (((c & 7) ^ (e & 7)) << 4), src + go, okr);
         }
-        cp_async_mbar_arrive_noinc(kv_full + st);
+        cp_async_mbar_arrive_noinc(full + st);
       }
       cp_async_wait_all();
-      if (pw == 0 && lane == 0 && *abort_flag) {   // no TMA load may still be writing when the CTA exits
+      if (gw == 0 && lane == 0 && *abort_flag) {   // no TMA load may still be writing when the CTA exits
         for (int c = 0; c < NST; ++c)
-          if ((tma_pend >> c) & 1u) wait_drain(kv_full + c, (tma_par >> c) & 1u);
+          if ((tma_pend >> c) & 1u) wait_drain(full + c, (tma_par >> c) & 1u);
       }
     } else {
       // INT8 codes: each warp widens its rows of a stage in place once they
@@ -560,18 +569,22 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(kv_full + t % NST);
+        if (lane == 0) {
+          mbar_arrive(k_full + t % NST);
+          mbar_arrive(v_full + t % NST);
+        }
       };
       for (int j = 0; j < T; ++j) {
         const int st = j % NST, u = j / NST;
         // publish tile j - (NST - 1) before waiting for stage st: the MMA
-        // needs it before it can free that stage
+        // needs it before it can free that stage (its V half, freed by the
+        // PV, is the later of the two)
         if (j >= NST - 1) {
           cp_async_wait<NST - 2>();
           publish(j - (NST - 1));
           published = j - (NST - 1) + 1;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(v_empty + st, (u & 1) ^ 1, abort_flag))) break;
         int rows[2] = {nrow0, nrow1};
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -624,11 +637,11 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       unsigned long long t_idle = 0;
       while (ok && npv < T) {
         bool progressed = false;
-        if (nqk < T && nqk < npv + 2 && mbar_test_wait(kv_full + nqk % NST, (nqk / NST) & 1)) {
+        if (nqk < T && nqk < npv + 2 && mbar_test_wait(k_full + nqk % NST, (nqk / NST) & 1)) {
           const int st = nqk % NST, b = nqk & 1;
           tc_fence_after();
           // 16-bit stages are written by cp.async copies that arrived on
-          // kv_full by themselves: order them before the tensor core's reads
+          // k_full by themselves: order them before the tensor core's reads
           if constexpr (KQ == 0) fence_proxy_async_smem();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -638,19 +651,22 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
                    sdesc_sw128(sK + st * Sh::TILE + b_off, 16, 1024), id_qk, kk > 0);
           }
           tc_commit(s_full + b);
+          tc_commit(k_empty + st);
           ++nqk;
           progressed = true;
         }
-        if (npv < nqk && mbar_test_wait(p_full + (npv & 1), (npv >> 1) & 1)) {
+        if (npv < nqk && mbar_test_wait(p_full + (npv & 1), (npv >> 1) & 1) &&
+            mbar_test_wait(v_full + npv % NST, (npv / NST) & 1)) {
           const int pst = npv % NST, pb = npv & 1;
           tc_fence_after();
+          if constexpr (KQ == 0) fence_proxy_async_smem();
           // O += P_hi V + P_lo V (P_hi in S columns 0..BN/2-1, P_lo after it)
 #pragma unroll
           for (int kk = 0; kk < 2 * (BN / 16); ++kk)
             mma_ts(tO, tbase + Sh::COL_S + pb * BN + kk * 8,
                    sdesc_sw128(sV + pst * Sh::TILE + (kk % (BN / 16)) * 2048, Sh::KV_ATOM, 1024), id_pv,
                    npv > 0 || kk > 0);
-          tc_commit(kv_empty + pst);
+          tc_commit(v_empty + pst);
           tc_commit(o_ready);
           ++npv;
           progressed = true;

@@ -120,6 +120,31 @@ def test_out_of_range_rows_are_skipped_like_padding_and_reported():
     assert far.fa_rows_validate(torch.from_numpy(p.kv_rows).cuda(), p.R) == (0, -1)
 
 
+@pytest.mark.parametrize("hq,hkv,dtype,causal", [(8, 2, "bf16", False), (16, 1, "bf16", True), (32, 1, "bf16", False),
+                                                 (8, 2, "f16", False)])
+def test_decode_contiguous_runs(hq, hkv, dtype, causal):
+    """Lists made of contiguous pool runs (whole 64-entry tiles of one run take
+    the tile-load path, the rest are gathered), with a ragged padded tail."""
+    S, L, R = 2, 1500, 6000
+    p = synth.random_problem(3500 + hq, S=S, Nq=1, Hq=hq, Hkv=hkv, D=128, R=R, L=L, dtype=dtype, pad_frac=0.0,
+                             causal=causal)
+    g = np.random.default_rng(11 + hq)
+    rows = np.empty((S, L), np.int32)
+    rows[0] = 1000 + np.arange(L)                 # one run: every full tile is contiguous
+    pos = 0
+    while pos < L:                                # runs of 20..300 rows at random starts
+        n = min(int(g.integers(20, 300)), L - pos)
+        start = int(g.integers(0, R - n))
+        rows[1, pos:pos + n] = start + np.arange(n)
+        pos += n
+    rows[:, -37:] = -1
+    p2 = synth.Problem(**{**p.__dict__, "kv_rows": rows})
+    out, lse = run_decode(p2)
+    ref, ref_lse = oracle_for(p2)
+    assert_parity(out, ref, f"runs hq={hq} hkv={hkv} {dtype} causal={causal}")
+    assert_lse(lse, ref_lse)
+
+
 def test_repeated_calls_are_identical_and_split_plans_agree():
     p = synth.random_problem(3400, S=4, Hq=32, Hkv=8, D=128, R=40000, L=16000, pad_frac=0.0)
     a, _ = run_decode(p)
