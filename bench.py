@@ -64,6 +64,29 @@ PROFILE_FILES = {
 
 
 # ---------------------------------------------------------------------------
+# ranks: each rank runs an independent replica of the workload
+
+
+def max_over_ranks(vals, dist_mod=None, device=None):
+    """Each value's maximum over all ranks of the default process group (the
+    values themselves when there is one rank or no group)."""
+    vals = [float(x) for x in vals]
+    if dist_mod is None or not dist_mod.is_available() or not dist_mod.is_initialized():
+        return vals
+    if dist_mod.get_world_size() == 1:
+        return vals
+    import torch
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world: int, work_per_rank: float, step_ms: float, scale: float) -> float:
+    """Work of all ranks per second of the slowest rank's step, in units of scale."""
+    return world * work_per_rank / (step_ms * 1e-3) / scale
+
+
+# ---------------------------------------------------------------------------
 # workload accounting
 
 
@@ -429,9 +452,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
 
     step_ms = total_ms / args.steps
     if world > 1:
-        t = torch.tensor([step_ms, e2e_ms, mean_launch_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms, mean_launch_ms = t.tolist()
+        step_ms, e2e_ms, mean_launch_ms = max_over_ranks([step_ms, e2e_ms, mean_launch_ms], dist, dev)
     if rank != 0:
         return None
 
@@ -447,7 +468,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
         unit, scale_ = "GB/s", 1e9
         peak = pk["hbm_gbs"]
         bound = "hbm"
-    value = world * work / (step_ms * 1e-3) / scale_
+    value = whole_job_rate(world, work, step_ms, scale_)
     achieved = work / (mean_launch_ms * 1e-3) / scale_
     res = {
         "metric": METRIC,
@@ -484,7 +505,7 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             "work_per_launch": work,
         },
         "e2e": {
-            "value": round(world * work / (e2e_ms * 1e-3) / scale_, 2),
+            "value": round(whole_job_rate(world, work, e2e_ms, scale_), 2),
             "unit": unit,
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
