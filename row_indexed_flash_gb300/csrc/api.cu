@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "decode.cuh"
 #include "fa_internal.cuh"
 
@@ -32,16 +34,17 @@ int next_pow2(int x) {
   return p;
 }
 
+// SM count of the current device, cached per device once it has been read
+// (a failed query is not cached: it answers 1 and is retried next time).
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    cached[dev] = n;
-  }
-  return cached[dev];
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+  cached[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 int kv_kind(fa_dtype d) {
