@@ -521,6 +521,202 @@ def run_gpu(args, rank, world, p, cpu_baseline):
 # ---------------------------------------------------------------------------
 
 
+APPEND = dict(n_seq=4, new=2048, R=400000, Hkv=8, D=128)
+
+
+def append_bytes(n_rows: int, Hkv: int, D: int) -> int:
+    """Algorithmic bytes of an INT8 append: per (row, head) the 16-bit input,
+    the codes and the fp16 scale; per row its destination index."""
+    return n_rows * (Hkv * (2 * D + D + 2) + 4)
+
+
+def append_oracle_rate(min_seconds: float = 0.0, passes_wanted: int = 0):
+    """The oracle's append (quantise + scatter, int8) timed on a bounded
+    sample: one sequence's 2,048 new rows into a 16,384-row pool, for
+    passes_wanted passes, else until min_seconds have passed."""
+    import oracle
+    c = APPEND
+    g = synth.rng(synth.SEED_BASE + 7)
+    x = oracle.widen_bf16(synth.normal_bits(g, (c["new"], c["Hkv"], c["D"]), "bf16")).astype(np.float32)
+    pool = np.zeros((16384, c["Hkv"], c["D"]), np.int8)
+    sc = np.zeros((16384 // 64, c["Hkv"], 64), np.float16)
+    dst = (4096 + np.arange(c["new"])).astype(np.int32)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.append_rows(pool, x, dst, sc, fmt="int8")
+        passes += 1
+        dt = time.perf_counter() - t0
+        if (passes >= passes_wanted) if passes_wanted > 0 else (dt >= min_seconds):
+            break
+    v = passes * append_bytes(c["new"], c["Hkv"], c["D"]) / dt / 1e9
+    return v, dt, passes
+
+
+def run_append(args, rank, world, cpu_baseline):
+    """Fused KV append: each step quantises a ubatch of new K rows (bf16,
+    4 sequences x 2,048 tokens) to INT8 and writes codes and scales into
+    fresh 64-row pages of a 400,000-row pool (one 2,048-row block of pages per
+    sequence at a seeded random position): one fa_kv_quantize_int8 call."""
+    import ctypes
+
+    import torch
+    import torch.distributed as dist
+
+    import row_indexed_flash_gb300 as far
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    c = APPEND
+    n_seq, new, R, Hkv, D = c["n_seq"], c["new"], c["R"], c["Hkv"], c["D"]
+    n = n_seq * new
+    g = synth.rng(synth.SEED_BASE + 6)
+    x0 = torch.from_numpy(synth.normal_bits(g, (n, Hkv, D), "bf16").view(np.int16)).view(torch.bfloat16).to(dev)
+    x_bytes = x0.numel() * 2
+    # inputs larger than L2: rotate over copies of the ubatch, each written to its own pages
+    n_copies = int(math.ceil(2 * 129e6 / x_bytes)) + 1
+    blocks = g.permutation(R // new)[: n_copies * n_seq]
+    dsts = [torch.from_numpy(np.concatenate([blocks[ci * n_seq + si] * new + np.arange(new)
+                                             for si in range(n_seq)]).astype(np.int32)).to(dev)
+            for ci in range(n_copies)]
+    xs = [x0] + [x0.clone() for _ in range(n_copies - 1)]
+    q = torch.zeros((R, Hkv, D), dtype=torch.int8, device=dev)
+    sc = torch.zeros((R // 64, Hkv, 64), dtype=torch.float16, device=dev)
+    lib = far.lib()
+    bf = far._DT[torch.bfloat16]
+
+    def step(i, sh=sh):
+        st = lib.fa_kv_quantize_int8(xs[i % n_copies].data_ptr(), bf, n, Hkv, D, dsts[i % n_copies].data_ptr(),
+                                     q.data_ptr(), sc.data_ptr(), R, sh)
+        if st != 0:
+            raise far.FaRowsError(st, far.fa_last_error())
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    graphs = None
+    if not args.no_graph:
+        try:
+            graphs = []
+            for i in range(n_copies):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    step(i, torch.cuda.current_stream(dev).cuda_stream)
+                graphs.append(gr)
+            for gr in graphs:
+                gr.replay()
+            torch.cuda.synchronize(dev)
+        except Exception as exc:
+            print(f"# CUDA graph capture failed ({exc}); timing direct launches", file=sys.stderr)
+            graphs = None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            if graphs is not None:
+                graphs[i % n_copies].replay()
+            else:
+                step(i)
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    step_ms = t0.elapsed_time(t1) / args.steps
+    launch_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    # end to end: the ubatch and its destinations copied in from pinned host
+    # memory, the call, and the written codes and scales copied back
+    hx = x0.cpu().pin_memory()
+    hd = dsts[0].cpu().pin_memory()
+    dx, dd = torch.empty_like(x0), torch.empty_like(dsts[0])
+    starts = [int(blocks[si]) * new for si in range(n_seq)]
+    hq = [torch.empty((new, Hkv, D), dtype=torch.int8).pin_memory() for _ in range(n_seq)]
+    hs = [torch.empty((new // 64, Hkv, 64), dtype=torch.float16).pin_memory() for _ in range(n_seq)]
+    h2d = hx.numel() * 2 + hd.numel() * 4
+    d2h = sum(t.numel() for t in hq) + sum(t.numel() * 2 for t in hs)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dd.copy_(hd, non_blocking=True)
+        st = lib.fa_kv_quantize_int8(dx.data_ptr(), bf, n, Hkv, D, dd.data_ptr(), q.data_ptr(), sc.data_ptr(), R, sh)
+        if st != 0:
+            raise far.FaRowsError(st, far.fa_last_error())
+        for si in range(n_seq):
+            r0 = starts[si]
+            hq[si].copy_(q[r0:r0 + new], non_blocking=True)
+            hs[si].copy_(sc[r0 // 64:(r0 + new) // 64], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        step_ms, e2e_ms, launch_ms = max_over_ranks([step_ms, e2e_ms, launch_ms], dist, dev)
+    if rank != 0:
+        return None
+    pk, pk_src = peaks()
+    work = append_bytes(n, Hkv, D)
+    achieved = work / (launch_ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC,
+        "value": round(whole_job_rate(world, work, step_ms, 1e9), 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8",
+        "data": "synthetic (seeded N(0,1) bf16 rows)",
+        "config": {
+            "workload": f"kv-append int8: {n_seq} x {new} new rows into a {R}-row pool, {Hkv} KV heads, D{D}",
+            "l2": f"inputs larger than L2: {n_copies} ubatch copies of {x_bytes / 1e6:.1f} MB rotated, "
+                  f"each to its own pages",
+            "parallelism": f"replicas x{world}",
+            "launch": "cuda_graph" if graphs is not None else "direct",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": pk["hbm_gbs"],
+            "peak_source": pk_src,
+            "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4),
+            "traffic": None,
+            "kernel": "quantize_int8_kernel",
+            "kernel_ms": round(launch_ms, 5),
+            "work_per_launch": work,
+        },
+        "e2e": {
+            "value": round(whole_job_rate(world, work, e2e_ms, 1e9), 2),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms, 4),
+        },
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu_baseline,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -530,7 +726,7 @@ def main():
     ap.add_argument("--workload", default="decode_bf16",
                     choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int8_small",
                              "paged_int4", "paged_fp8",
-                             "sparse_bf16", "sparse_select_bf16", "decode_f16_small"])
+                             "sparse_bf16", "sparse_select_bf16", "decode_f16_small", "kv_append_int8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
     args = ap.parse_args()
@@ -540,6 +736,39 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     procs = os.cpu_count() or 1
+
+    if args.workload == "kv_append_int8":
+        if args.impl == "reference":
+            if rank != 0:
+                return
+            append_oracle_rate(passes_wanted=args.warmup)
+            v, dt, passes = append_oracle_rate(passes_wanted=args.steps)
+            print(json.dumps({
+                "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / passes * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+                "data": "synthetic", "config": {"workload": "kv-append int8 (oracle append_rows, bounded sample)"},
+                "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"2,048 rows into a 16,384-row pool x {passes} passes"},
+                "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            }))
+            return
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl")
+        cpu_baseline = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            v, dt, passes = append_oracle_rate(10.0)
+            cpu_baseline = {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": f"append_rows (int8) of 2,048 rows into a 16,384-row pool x {passes} passes, "
+                                      f"{dt:.1f} s wall"}
+        res = run_append(args, rank, world, cpu_baseline)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        if res is not None:
+            print(json.dumps(res))
+        return
 
     if args.impl == "reference":
         if rank != 0:
