@@ -120,11 +120,44 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_sha(kind: str) -> str:
+def code_only(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and every run of
+    whitespace collapsed to one space (string and character literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def source_sha(kind: str, read=None) -> str:
+    """Hash of the code (comments and layout excluded) of a kernel's sources:
+    the key under which ncu summaries in profiles/ record what they measured."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        if read is None:
+            with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+                text = f.read()
+        else:
+            text = read(rel)
+        h.update(code_only(text).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

@@ -8,28 +8,34 @@
 // CUDA cores cannot form the dot products at that rate without becoming the
 // bottleneck (a widening conversion and a fused multiply-add per element for
 // every query vector), while the tensor pipe is idle.  So the Nq*G query
-// vectors that share a KV head (at most 32) are placed in the rows of a
-// 128-row MMA tile; the other rows carry whatever lies in shared memory after
+// vectors that share a KV head (at most 32) are placed in the rows of an
+// MMA tile; the other rows carry whatever lies in shared memory after
 // the query rows and only ever produce rows of S, P and O that are never read
 // (an MMA row depends on its own A row only).
 //
 // One CTA handles one (slice, KV head, split) item, 64 list entries per tile:
-//   producers      4 warps: cp.async gathers of the listed rows into the
-//                  128-byte-swizzled layout (padding rows zero-filled), or one
-//                  TMA tile load per 64-column atom when the 64 listed rows are
-//                  one contiguous pool run; 3 stages.
-//   MMA warp       S_b = Q K^T (M=128, N=64, both operands in shared memory),
-//                  then O += P_b V (P from tensor memory, V MN-major), S
-//                  double-buffered so the next QK overlaps the softmax.
-//   softmax warp   one lane per query vector: masks, keeps a reference max that
-//                  only moves when it grows by more than 2^8 (then rescales O in
-//                  place), writes P over S as 16-bit pairs, and at the end
-//                  writes the split's (max, sum, O) or the final output.
+//   producers      2 warps gather K and 2 gather V (cp.async of the listed
+//                  rows into the 128-byte-swizzled layout, padding rows
+//                  zero-filled), or one TMA tile load per 64-column atom when
+//                  the 64 listed rows are one contiguous pool run.  K and V
+//                  have separate rings of 3 stages; the copies arrive on the
+//                  stage's barrier by themselves, a K stage is freed by its
+//                  QK and a V stage by its PV.
+//   MMA warp       S_b = Q K^T (M=64 for at most 16 query vectors, else 128;
+//                  N=64; both operands in shared memory), then O += P_b V
+//                  (M=128, P from tensor memory, V MN-major), S double-
+//                  buffered so the next QK overlaps the softmax.
+//   softmax warp   the query vectors' S rows are spread over the warp (32/QVP
+//                  lanes per row): masks, a reference max that only moves
+//                  when it grows by more than 2^8 (then O is rescaled in
+//                  place), P written over S as a 16-bit hi/lo pair, and at the
+//                  end the split's (max, sum, O) or the final output.
 // INT8 pools (codes with one fp16 scale per (row, KV head)) take the same
-// pipeline: the producers gather the codes into the upper half of the stage's
-// tile, widen them in place to Q's 16-bit type (exact: |code| <= 127), and
-// store the rows' scales beside the tile; the softmax folds the K scale into
-// the logit and the V scale into P, so the MMAs see plain 16-bit operands.
+// pipeline with all four producer warps on both matrices: they gather the
+// codes into the upper half of the stage's tiles, widen them in place to Q's
+// 16-bit type (exact: |code| <= 127), and store the rows' scales beside the
+// tile; the softmax folds the K scale into the logit and the V scale into P,
+// so the MMAs see plain 16-bit operands.
 // The last CTA to finish a (slice, KV head) merges the splits (an arrival
 // counter in the workspace, reset by that CTA; nothing waits on it).
 // Every pipeline wait is bounded in time and reported through an error word.
