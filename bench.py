@@ -7,7 +7,14 @@ sequence (lists sorted ascending).  Metric: gathered-KV GB/s = listed rows x
 
 ``--workload prefill_bf16`` measures the prefill chunk (4 x 2,048 query rows
 over 99,936-row lists in a 400,000-row pool, causal) in tensor TFLOP/s with
-4*D FLOPs per visible (query, key, head) triple.
+4*D FLOPs per visible (query, key, head) triple.  Other workloads:
+``paged_int8`` / ``paged_int4`` / ``paged_fp8`` (page tables expanded to row
+lists, then the quantised-pool decode), ``sparse_bf16`` (sink + recent +
+selected list, D 256), ``sparse_select_bf16`` (the list built from a score each
+step, then the decode), ``decode_f16_small``, the profiling sizes
+``prefill_bf16_small`` / ``paged_int8_small``, and ``kv_append_int8`` (a
+ubatch of new rows quantised into fresh pages; GB/s of its input, codes,
+scales and destination indices).
 
 One JSON line on stdout (rank 0).  Under torchrun each rank runs an
 independent replica of the workload (the path shards by sequence with no
