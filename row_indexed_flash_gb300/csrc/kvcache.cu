@@ -98,6 +98,72 @@ __global__ void quantize_int8_kernel(const uint16_t* __restrict__ x, int x_bf16,
   }
 }
 
+// The same rule for D = 32 * EPL (64, 128, 256) with 16-byte aligned x and q:
+// lane l holds elements EPL*l .. EPL*l + EPL - 1, loaded and stored with one
+// vector access each, and the row's values are loaded together with its
+// destination index rather than after it.
+template <int EPL>
+__global__ void quantize_int8_vec_kernel(const uint16_t* __restrict__ x, int x_bf16, long long n_rows, int Hkv,
+                                         const int32_t* __restrict__ dst_rows, int8_t* __restrict__ q,
+                                         uint16_t* __restrict__ scale, long long R) {
+  constexpr int D = 32 * EPL;
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+  for (long long w = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5); w < n_rows * Hkv; w += warps) {
+    const long long i = w / Hkv;
+    const int g = (int)(w % Hkv);
+    const uint16_t* src = x + (size_t)w * D + lane * EPL;
+    uint32_t raw[EPL / 2];
+    if constexpr (EPL == 2) {
+      raw[0] = __ldg(reinterpret_cast<const unsigned int*>(src));
+    } else if constexpr (EPL == 4) {
+      const uint2 t = __ldg(reinterpret_cast<const uint2*>(src));
+      raw[0] = t.x;
+      raw[1] = t.y;
+    } else {
+      const uint4 t = __ldg(reinterpret_cast<const uint4*>(src));
+      raw[0] = t.x;
+      raw[1] = t.y;
+      raw[2] = t.z;
+      raw[3] = t.w;
+    }
+    const long long dst = dst_rows ? (long long)__ldg(dst_rows + i) : i;
+    float vals[EPL];
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < EPL / 2; ++k) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t b = e ? (raw[k] >> 16) : (raw[k] & 0xffffu);
+        const float f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
+        vals[2 * k + e] = f;
+        amax = fmaxf(amax, fabsf(f));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (dst < 0 || dst >= R) continue;   // the same for every lane of the warp
+    const __half sh = __float2half_rn(fminf(__fdiv_rn(amax, 127.0f), 65504.0f));
+    const float sf = __half2float(sh);
+    uint32_t packed[(EPL + 3) / 4] = {};
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      int c = 0;
+      if (sf != 0.f) c = min(max(__float2int_rn(__fdiv_rn(vals[e], sf)), -127), 127);
+      packed[e / 4] |= ((uint32_t)c & 0xffu) << (8 * (e % 4));
+    }
+    int8_t* qd = q + ((size_t)dst * Hkv + g) * D + lane * EPL;
+    if constexpr (EPL == 2) {
+      *reinterpret_cast<uint16_t*>(qd) = (uint16_t)packed[0];
+    } else if constexpr (EPL == 4) {
+      *reinterpret_cast<uint32_t*>(qd) = packed[0];
+    } else {
+      *reinterpret_cast<uint2*>(qd) = make_uint2(packed[0], packed[1]);
+    }
+    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = __half_as_ushort(sh);
+  }
+}
+
 cudaError_t launch_quantize_int8(const void* x, int x_bf16, long long n_rows, int Hkv, int D, const int32_t* dst,
                                  int8_t* q, uint16_t* scale, long long R, cudaStream_t st) {
   const long long warps = n_rows * Hkv;
@@ -105,8 +171,16 @@ cudaError_t launch_quantize_int8(const void* x, int x_bf16, long long n_rows, in
   const int threads = 256;
   long long blocks = (warps + 7) / 8;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  quantize_int8_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint16_t*>(x), x_bf16, n_rows, Hkv, D,
-                                                             dst, q, scale, R);
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  const bool aligned16 = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (reinterpret_cast<uintptr_t>(q) % 16 == 0);
+  if (aligned16 && D == 64)
+    quantize_int8_vec_kernel<2><<<(unsigned)blocks, threads, 0, st>>>(xs, x_bf16, n_rows, Hkv, dst, q, scale, R);
+  else if (aligned16 && D == 128)
+    quantize_int8_vec_kernel<4><<<(unsigned)blocks, threads, 0, st>>>(xs, x_bf16, n_rows, Hkv, dst, q, scale, R);
+  else if (aligned16 && D == 256)
+    quantize_int8_vec_kernel<8><<<(unsigned)blocks, threads, 0, st>>>(xs, x_bf16, n_rows, Hkv, dst, q, scale, R);
+  else
+    quantize_int8_kernel<<<(unsigned)blocks, threads, 0, st>>>(xs, x_bf16, n_rows, Hkv, D, dst, q, scale, R);
   return cudaGetLastError();
 }
 
