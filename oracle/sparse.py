@@ -7,7 +7,7 @@ tokens an attention step reads as anchor + recent + sink, and the
 llama.cpp-v100 README's QSA sparse attention reads a selected subset of a
 long context; "llama.cpp 0.9.0 inference boundaries" (section 1) is the
 consumer: a sorted ``kv_rows`` list per query slice.  The learned indexer
-that produces the scores is not part of this build: the caller supplies one
+that produces the scores is not part of this library: the caller supplies one
 score per position.  Readings (the pages fix none of these):
 
 * positions ``0 .. sinks-1`` (sinks) and ``n-recent .. n-1`` (recent) are

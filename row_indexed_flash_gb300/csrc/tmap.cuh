@@ -1,4 +1,4 @@
-// Host side: encoding of TMA tensor maps through the driver entry point, with
+// Host side: encoding of TMA tensor maps through the CUDA driver API entry point, with
 // a small cache so that repeated calls on the same tensors (a decode step per
 // token) skip the encode.  Shared by the kernels' launch code.
 #pragma once
