@@ -1,13 +1,19 @@
 """Benchmark of row-indexed attention over a unified KV pool on GB300.
 
-Default workload: decode, bf16, 4 sequences x 16,384 rows in a 65,536-row
+Headline workload: decode, bf16, 4 sequences x 16,384 rows in a 65,536-row
 shuffled pool, 32 query / 8 KV heads, head_dim 128, one query token per
 sequence (lists sorted ascending).  Metric: gathered-KV GB/s = listed rows x
 (K + V bytes) per KV head, per second; padding, indices, Q and O excluded.
 
-``--workload prefill_bf16`` measures the prefill chunk (4 x 2,048 query rows
-over 99,936-row lists in a 400,000-row pool, causal) in tensor TFLOP/s with
-4*D FLOPs per visible (query, key, head) triple.  Other workloads:
+A default run on one GPU also measures, in the same JSON line under
+``configs``, the other configurations: the small fp16 decode, the prefill
+chunk (4 x 2,048 query rows over 99,936-row lists in a 400,000-row pool,
+causal; tensor TFLOP/s with 4*D FLOPs per visible (query, key, head) triple)
+in its ubatch-run layout and with every row shuffled over the pool, the paged
+INT8 decode and the sparse long-context decode -- each with its own roofline,
+clocks, end-to-end figure and oracle baseline.
+
+``--workload NAME`` measures one workload alone.  Workloads:
 ``paged_int8`` / ``paged_int4`` / ``paged_fp8`` (page tables expanded to row
 lists, then the quantised-pool decode), ``sparse_bf16`` (sink + recent +
 selected list, D 256), ``sparse_select_bf16`` (the list built from a score each
@@ -64,6 +70,7 @@ KERNEL_NAMES = {"decode": "fa_rows_decode_tc_kernel", "prefill": "fa_rows_prefil
 PROFILE_FILES = {
     "decode_bf16": "profiles/decode_bf16_4x16384_ncu.txt",
     "prefill_bf16": "profiles/prefill_bf16_4x2048x99936_ncu.txt",
+    "prefill_bf16_shuffled": "profiles/prefill_bf16_shuffled_4x2048x99936_ncu.txt",
     "prefill_bf16_small": "profiles/prefill_bf16_4x2048x16384_ncu.txt",
     "paged_int8": "profiles/paged_int8_32seq_ncu.txt",
     "paged_int8_small": "profiles/paged_int8_16seq_ncu.txt",
@@ -192,6 +199,14 @@ def profiled_traffic(workload: str, kind: str):
 # CPU oracle legs (fork pool, created before any CUDA call)
 
 _P = None
+_PAGED = None   # paged sample: quantiser name and, per sampled slice, its pages' codes and scales
+
+
+def quant_of(workload: str):
+    """Pool codec of a workload (None for 16-bit pools)."""
+    if not workload.startswith("paged"):
+        return None
+    return {"paged_int4": "int4", "paged_fp8": "fp8"}.get(workload, "int8")
 
 
 def _oracle_unit(args):
@@ -199,6 +214,20 @@ def _oracle_unit(args):
     s, g, qrows = args
     p = _P
     G = p.Hq // p.Hkv
+    if _PAGED is not None:
+        # paged decode of (slice s, KV head g): expand the slice's page table
+        # over a pool of its own pages, dequantise them, attend over the list
+        kc, ks, vc, vs = _PAGED[s]
+        deq = {"int8": oracle.dequantize_int8, "int4": oracle.dequantize_int4,
+               "fp8": oracle.dequantize_fp8}[_PAGED["quant"]]
+        n_pages = kc.shape[0] // p.page_size
+        rows = oracle.page_table_to_rows(np.arange(n_pages, dtype=np.int32)[None, :], p.seq_len[s:s + 1], p.L,
+                                         p.page_size)
+        k = deq(kc[:, g:g + 1], ks[:, g:g + 1]).astype(np.float64)
+        v = deq(vc[:, g:g + 1], vs[:, g:g + 1]).astype(np.float64)
+        q = oracle.widen(p.q[s:s + 1, :, g * G:(g + 1) * G], p.dtype)
+        oracle.attend_rows(q, k, v, rows, p.scale)
+        return s, g
     if qrows is None:
         q = oracle.widen(p.q[s:s + 1, :, g * G:(g + 1) * G], p.dtype)
         extra = {}
@@ -230,6 +259,37 @@ def oracle_units(p, prefill: bool, q_sample: int = 4):
     return units, work
 
 
+def paged_oracle_units(p, quant: str, min_rows: int = 65536):
+    """Units of the paged oracle leg: the (slice, KV head) pairs of a seeded
+    sample of slices holding at least ``min_rows`` listed rows.  Each sampled
+    slice's pages are quantised by the oracle's own codec beforehand (the write
+    path, not timed); a unit then expands the page table, dequantises and
+    attends.  Work = listed rows x (codes + two fp16 scales) per KV head."""
+    global _PAGED
+    import oracle
+    quantise = {"int8": oracle.quantize_int8, "int4": oracle.quantize_int4, "fp8": oracle.quantize_fp8}[quant]
+    order = synth.rng(synth.SEED_BASE + 99).permutation(p.S)
+    chosen, total = [], 0
+    for s in order:
+        chosen.append(int(s))
+        total += int(p.seq_len[s])
+        if total >= min_rows:
+            break
+    paged = {"quant": quant}
+    for s in chosen:
+        n_pages = (int(p.seq_len[s]) + p.page_size - 1) // p.page_size
+        pages = p.page_table[s, :n_pages].astype(np.int64)
+        rows = (pages[:, None] * p.page_size + np.arange(p.page_size)[None, :]).ravel()
+        kc, ks = quantise(oracle.widen(p.k[rows], p.dtype).astype(np.float32))
+        vc, vs = quantise(oracle.widen(p.v[rows], p.dtype).astype(np.float32))
+        paged[s] = (kc, ks, vc, vs)
+    _PAGED = paged
+    per_row = {"int8": 2 * p.D + 4, "fp8": 2 * p.D + 4, "int4": p.D + 4}[quant]
+    units = [(s, g, None) for s in chosen for g in range(p.Hkv)]
+    work = [int(p.seq_len[s]) * per_row for s in chosen for g in range(p.Hkv)]
+    return units, work, f"{len(chosen)} of {p.S} slices ({total} listed rows, pages quantised beforehand)"
+
+
 def oracle_rate(p, units, work, procs: int, min_seconds: float = 0.0, max_passes: int = 1):
     """Work per second of the oracle over ``units``: whole passes over them,
     repeated until ``min_seconds`` have elapsed (at most ``max_passes``)."""
@@ -246,6 +306,26 @@ def oracle_rate(p, units, work, procs: int, min_seconds: float = 0.0, max_passes
             if dt >= min_seconds or passes >= max_passes:
                 break
     return passes * sum(work) / dt, dt, passes
+
+
+def cpu_leg(p, workload: str, procs: int, min_seconds: float):
+    """The oracle, as it stands, on the host cores over a bounded sample of the
+    workload: whole passes over its units for about ``min_seconds``."""
+    global _PAGED
+    prefill = workload.startswith("prefill")
+    unit, div = ("TFLOP/s", 1e12) if prefill else ("GB/s", 1e9)
+    if p.kv_rows is None:
+        units, work, what = paged_oracle_units(p, quant_of(workload))
+    else:
+        units, work = oracle_units(p, prefill)
+        what = f"{len(units)} (slice, KV head) units" + (
+            f" x {len(units[0][2])} query rows" if prefill else " (whole workload)")
+    try:
+        v, dt, passes = oracle_rate(p, units, work, procs, min_seconds=min_seconds, max_passes=1000)
+    finally:
+        _PAGED = None
+    return {"value": round(v / div, 6), "unit": unit, "cores": procs, "kind": "oracle",
+            "sample": f"{what} x {passes} passes, {dt:.1f} s wall"}
 
 
 # ---------------------------------------------------------------------------
@@ -307,14 +387,30 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 
+# The configurations measured beside the headline decode in a default run
+# (one GPU): the small fp16 decode, the prefill chunk in its ubatch-run layout
+# and fully shuffled, the paged INT8 decode and the sparse long-context decode.
+CONFIG_WORKLOADS = ["decode_f16_small", "prefill_bf16", "prefill_bf16_shuffled", "paged_int8", "sparse_bf16"]
+WORKLOAD_CHOICES = ["decode_bf16", "decode_f16_small", "prefill_bf16", "prefill_bf16_shuffled", "prefill_bf16_small",
+                    "paged_int8", "paged_int8_small", "paged_int4", "paged_fp8", "sparse_bf16", "sparse_select_bf16",
+                    "kv_append_int8"]
 
-def build_problem(workload: str):
+
+def build_problem(workload: str, cache=None):
+    cache = {} if cache is None else cache
     if workload == "decode_bf16":
         return synth.decode_bf16_large()
-    if workload == "prefill_bf16":
-        return synth.prefill_bf16()
+    if workload in ("prefill_bf16", "prefill_bf16_shuffled"):
+        if "prefill_bf16" not in cache:
+            cache["prefill_bf16"] = synth.prefill_bf16()
+        p = cache["prefill_bf16"]
+        if workload == "prefill_bf16":
+            return p
+        # the same pool, every listed row at a random slot: all K/V tiles gathered
+        return synth.relabel_rows(p, synth.SEED_BASE + 13,
+                                  p.name.replace("(2048-row runs)", "(rows shuffled over the pool)"))
     if workload in ("paged_int8", "paged_int4", "paged_fp8"):
-        return synth.paged_int8()   # the paged layout; the pool is quantised by the bench
+        return synth.paged_int8()   # the paged layout; the pool is quantised by each side
     if workload == "paged_int8_small":
         # profiling size: 16 sequences of 1k-32k tokens (about 250 MB of codes, above L2)
         return synth.paged_int8(n_seq=16, lo=1024, hi=32768)
@@ -328,7 +424,19 @@ def build_problem(workload: str):
     raise SystemExit(f"unknown workload {workload}")
 
 
-def run_gpu(args, rank, world, p, cpu_baseline):
+def kernel_kind(workload: str) -> str:
+    if workload.startswith("prefill"):
+        return "prefill"
+    return "decode_q" if workload.startswith("paged") else "decode"
+
+
+def measure(args, rank, world, p, workload, cpu_baseline):
+    """Times one workload on this rank's GPU: warm-up, then args.steps steps
+    (replayed CUDA graphs of the step's launches) with CUDA events on the
+    launching stream, clocks sampled meanwhile; then the same call end to end
+    with host inputs.  Returns the result dict on rank 0."""
+    import ctypes
+
     import torch
     import torch.distributed as dist
 
@@ -342,66 +450,64 @@ def run_gpu(args, rank, world, p, cpu_baseline):
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt).to(dev)
 
-    is_prefill = args.workload.startswith("prefill")
-    paged = p.kv_int8
-    quant = {"paged_int4": "int4", "paged_fp8": "fp8"}.get(args.workload, "int8") if paged else None
+    is_prefill = workload.startswith("prefill")
+    paged = p.kv_rows is None
+    quant = quant_of(workload)
     quantise = {"int4": far.fa_kv_quantize_int4, "fp8": far.fa_kv_quantize_fp8}.get(quant, far.fa_kv_quantize_int8)
     q = to_dev(p.q)
-    k0, v0 = to_dev(p.k), to_dev(p.v)
-    scales = None
     if paged:
-        # write path (not timed): quantise the bf16 pool into INT8/INT4 codes + fp16 scales
-        kq, ks = quantise(k0, p.R)
-        vq, vs = quantise(v0, p.R)
-        del k0, v0
+        # write path (not timed): quantise the bf16 pool into codes + fp16 scales
+        kb, vb = to_dev(p.k), to_dev(p.v)
+        kq, ks = quantise(kb, p.R)
+        vq, vs = quantise(vb, p.R)
+        del kb, vb
         torch.cuda.synchronize(dev)
-        k0, v0, scales = kq, vq, (ks, vs)
+        base = (kq, vq, ks, vs)
         pt = torch.from_numpy(p.page_table).to(dev)
         sl = torch.from_numpy(p.seq_len).to(dev)
         rows = torch.empty((p.S, p.L), dtype=torch.int32, device=dev)
     else:
+        base = (to_dev(p.k), to_dev(p.v), None, None)
         rows = torch.from_numpy(p.kv_rows).to(dev)
-    select = args.workload == "sparse_select_bf16"
+    select = workload == "sparse_select_bf16"
     if select:
         # each step builds the list (4 sinks + 1,532 by score + 512 recent) from a
         # seeded fp32 score per position, then decodes over it
         sel_score = torch.from_numpy(synth.rng(9).standard_normal((1, p.R)).astype(np.float32)).to(dev)
         sel_ws = torch.empty(max(far.lib().fa_kv_sparse_rows_workspace_size(1, p.R), 16), dtype=torch.uint8,
                              device=dev)
-    pool_bytes = 2 * k0.numel() * k0.element_size()
+    pool_bytes = sum(t.numel() * t.element_size() for t in base if t is not None)
     # rotate over enough pool copies that each step reads data not left in L2
     n_copies = max(1, min(3, int(math.ceil(3 * 129e6 / pool_bytes)) + 1)) if not is_prefill else 1
-    pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(n_copies - 1)]
+    pools = [base] + [tuple(None if t is None else t.clone() for t in base) for _ in range(n_copies - 1)]
     out = torch.empty((p.S, p.Nq, p.Hq, p.D), dtype=torch.float32, device=dev)
     a_list = []
-    for (k, v) in pools:
+    for (k, v, ksc, vsc) in pools:
         kw = {}
         if paged:
-            kw = dict(k_scale=scales[0], v_scale=scales[1], kv_len=sl, n_valid_hint=p.n_valid())
+            kw = dict(k_scale=ksc, v_scale=vsc, kv_len=sl, n_valid_hint=p.n_valid())
         a, _, _ = far.make_args(q, k, v, rows, p.scale, causal=p.causal, out=out, **kw)
         a_list.append(a)
-    entry = far.lib().fa_rows_prefill if is_prefill else far.lib().fa_rows_decode
+    lib = far.lib()
+    entry = lib.fa_rows_prefill if is_prefill else lib.fa_rows_decode
     need = far.fa_rows_workspace_size(a_list[0], is_prefill)
     ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     sh = stream.cuda_stream
-    import ctypes
 
-    lib = far.lib()
-
-    def step(i, sh=sh):
-        if select:
-            st = lib.fa_kv_sparse_rows(sel_score.data_ptr(), p.R, None, 1, 4, 512, 1532, None, rows.data_ptr(),
-                                       rows.shape[1], sel_ws.data_ptr(), sel_ws.numel(), sh)
-            if st != 0:
-                raise far.FaRowsError(st, far.fa_last_error())
-        if paged:   # page tables -> row lists, then the decode (both kernels of the step)
-            st = lib.fa_kv_page_table_to_rows(pt.data_ptr(), pt.shape[1], sl.data_ptr(), p.S, p.page_size,
-                                              rows.data_ptr(), p.L, sh)
-            if st != 0:
-                raise far.FaRowsError(st, far.fa_last_error())
-        st = entry(ctypes.byref(a_list[i % len(a_list)]), ws.data_ptr(), ws.numel(), sh)
+    def call(st):
         if st != 0:
             raise far.FaRowsError(st, far.fa_last_error())
+
+    def step(i, sh=sh, a=None):
+        if select:
+            call(lib.fa_kv_sparse_rows(sel_score.data_ptr(), p.R, None, 1, 4, 512, 1532, None, rows.data_ptr(),
+                                       rows.shape[1], sel_ws.data_ptr(), sel_ws.numel(), sh))
+        if paged:   # page tables -> row lists, then the decode (both kernels of the step)
+            call(lib.fa_kv_page_table_to_rows(pt.data_ptr(), pt.shape[1], sl.data_ptr(), p.S, p.page_size,
+                                              rows.data_ptr(), p.L, sh))
+        call(entry(ctypes.byref(a_list[i % len(a_list)] if a is None else a), ws.data_ptr(), ws.numel(), sh))
+
+    launches_per_step = 1 + (1 if paged else 0) + (8 if select else 0)
 
     for i in range(args.warmup):
         step(i)
@@ -417,11 +523,10 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             for i in range(len(a_list)):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
-                    cap = torch.cuda.current_stream(dev).cuda_stream
-                    step(i, cap)
+                    step(i, torch.cuda.current_stream(dev).cuda_stream)
                 graphs.append(g)
-            for i in range(len(graphs)):
-                graphs[i].replay()
+            for g in graphs:
+                g.replay()
             torch.cuda.synchronize(dev)
         except Exception as exc:   # fall back to direct launches
             print(f"# CUDA graph capture failed ({exc}); timing direct launches", file=sys.stderr)
@@ -452,31 +557,41 @@ def run_gpu(args, rank, world, p, cpu_baseline):
     total_ms = t0.elapsed_time(t1)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     mean_launch_ms = sum(launch_ms) / len(launch_ms)
+    # a wait that ran out would have made every number above meaningless
+    if far.fa_rows_status(ws, clear=True) & far.FA_WS_WAIT_EXPIRED:
+        raise SystemExit(f"{workload}: a pipeline wait ran out during the timed steps")
 
-    # end to end through the public API: pinned host inputs copied in every step,
-    # the output read back every step
-    hq = torch.from_numpy(np.ascontiguousarray(p.q).view(np.int16)).view(tdt).pin_memory()
-    hk = k0.cpu().pin_memory()
-    hv = v0.cpu().pin_memory()
-    hr = rows.cpu().pin_memory()
+    # end to end through the public API: the step's inputs copied in from
+    # pinned host memory every step (Q, the pool, the lists -- for a paged
+    # pool its codes, scales, page table and lengths), the output read back
+    k0, v0, ks0, vs0 = base
+    host = {"q": q, "k": k0, "v": v0}
+    if paged:
+        host.update(ks=ks0, vs=vs0, pt=pt, sl=sl)
+    else:
+        host["rows"] = rows
+    pinned = {n: t.cpu().pin_memory() for n, t in host.items()}
+    dbuf = {n: torch.empty_like(t) for n, t in host.items()}
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dk, dv, dr = torch.empty_like(q), torch.empty_like(k0), torch.empty_like(v0), torch.empty_like(rows)
+    e_rows = rows if paged else dbuf["rows"]
     kw = {}
     if paged:
-        kw = dict(k_scale=scales[0], v_scale=scales[1], kv_len=sl, n_valid_hint=p.n_valid())
-    a_e2e, _, _ = far.make_args(dq, dk, dv, dr, p.scale, causal=p.causal, out=out, **kw)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hr))
+        kw = dict(k_scale=dbuf["ks"], v_scale=dbuf["vs"], kv_len=dbuf["sl"], n_valid_hint=p.n_valid())
+    a_e2e, _, _ = far.make_args(dbuf["q"], dbuf["k"], dbuf["v"], e_rows, p.scale, causal=p.causal, out=out, **kw)
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = hout.numel() * hout.element_size()
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dr.copy_(hr, non_blocking=True)
-        st = entry(ctypes.byref(a_e2e), ws.data_ptr(), ws.numel(), sh)
-        if st != 0:
-            raise far.FaRowsError(st, far.fa_last_error())
+        for n, t in pinned.items():
+            dbuf[n].copy_(t, non_blocking=True)
+        if select:
+            call(lib.fa_kv_sparse_rows(sel_score.data_ptr(), p.R, None, 1, 4, 512, 1532, None, e_rows.data_ptr(),
+                                       rows.shape[1], sel_ws.data_ptr(), sel_ws.numel(), sh))
+        if paged:
+            call(lib.fa_kv_page_table_to_rows(dbuf["pt"].data_ptr(), pt.shape[1], dbuf["sl"].data_ptr(), p.S,
+                                              p.page_size, e_rows.data_ptr(), p.L, sh))
+        call(entry(ctypes.byref(a_e2e), ws.data_ptr(), ws.numel(), sh))
         hout.copy_(out, non_blocking=True)
 
     e2e_step()
@@ -489,28 +604,35 @@ def run_gpu(args, rank, world, p, cpu_baseline):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if far.fa_rows_status(ws, clear=True) & far.FA_WS_WAIT_EXPIRED:
+        raise SystemExit(f"{workload}: a pipeline wait ran out during the end-to-end steps")
 
     step_ms = total_ms / args.steps
     if world > 1:
         step_ms, e2e_ms, mean_launch_ms = max_over_ranks([step_ms, e2e_ms, mean_launch_ms], dist, dev)
+    launch_mode = "cuda_graph" if graphs is not None else "direct"
+    del graphs, pools, a_list, base, pinned, dbuf
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
     if rank != 0:
         return None
 
     pk, pk_src = peaks()
-    kind = "prefill" if is_prefill else ("decode_q" if paged else "decode")
+    kind = kernel_kind(workload)
     if is_prefill:
         work = prefill_flops(p)
         unit, scale_ = "TFLOP/s", 1e12
-        peak = pk["bf16_tflops_sustained" if args.steps * step_ms > 2000 else "bf16_tflops"]
+        peak_key = "bf16_tflops_sustained" if args.steps * step_ms > 2000 else "bf16_tflops"
         bound = "tensor"
     else:
         work = decode_bytes(p, quant)
         unit, scale_ = "GB/s", 1e9
-        peak = pk["hbm_gbs"]
+        peak_key = "hbm_gbs"
         bound = "hbm"
+    peak = pk[peak_key]
     value = whole_job_rate(world, work, step_ms, scale_)
     achieved = work / (mean_launch_ms * 1e-3) / scale_
-    res = {
+    return {
         "metric": METRIC,
         "value": round(value, 2),
         "unit": unit,
@@ -521,25 +643,25 @@ def run_gpu(args, rank, world, p, cpu_baseline):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": p.dtype,
+        "dtype": quant if paged else p.dtype,
         "data": "synthetic (seeded N(0,1) values, generator shapes of the pages' workloads)",
         "config": {
             "workload": p.name,
-            "kv_rows": f"[{p.S}, {p.L}] int32",
+            "kv_rows": f"[{p.S}, {p.L}] int32" + (" (expanded from page tables each step)" if paged else ""),
             "n_valid_rows": p.n_valid(),
-            "l2": (f"inputs larger than L2: {len(pools)} pool copies of {pool_bytes / 1e6:.0f} MB rotated"
-                   if not is_prefill else f"pool {pool_bytes / 1e9:.2f} GB > L2"),
+            "l2": (f"inputs larger than L2: {n_copies} pool copies of {pool_bytes / 1e6:.0f} MB rotated"
+                   if not is_prefill else f"inputs larger than L2: pool {pool_bytes / 1e9:.2f} GB"),
             "parallelism": f"replicas x{world}",
-            "launch": "cuda_graph" if graphs is not None else "direct",
+            "launch": launch_mode,
         },
         "roofline": {
             "bound": bound,
             "achieved": round(achieved, 2),
             "peak": peak,
-            "peak_source": pk_src,
+            "peak_source": f"{pk_src} {peak_key}",
             "unit": unit,
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(args.workload, kind),
+            "traffic": profiled_traffic(workload, kind),
             "kernel": KERNEL_NAMES[kind],
             "kernel_ms": round(mean_launch_ms, 5),
             "work_per_launch": work,
@@ -551,11 +673,10 @@ def run_gpu(args, rank, world, p, cpu_baseline):
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4),
         },
-        "gpu_launches": args.steps * (2 if (paged or select) else 1),
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
         "cpu_baseline": cpu_baseline,
     }
-    return res
 
 
 # ---------------------------------------------------------------------------
@@ -757,21 +878,67 @@ def run_append(args, rank, world, cpu_baseline):
     }
 
 
+def reference_arm(args, rank, world, procs):
+    """The oracle, as it stands, on the host cores: each step a bounded sample
+    of the workload (the first `procs` units), on this arm's metric."""
+    if rank != 0:
+        return
+    workload = args.workload
+    p = build_problem(workload)
+    prefill = workload.startswith("prefill")
+    unit, div = ("TFLOP/s", 1e12) if prefill else ("GB/s", 1e9)
+    if p.kv_rows is None:
+        units, work, what = paged_oracle_units(p, quant_of(workload))
+    else:
+        units, work = oracle_units(p, prefill)
+        what = None
+    units, work = units[:procs], work[:procs]
+    for _ in range(args.warmup):
+        oracle_rate(p, units[:1], work[:1], 1)
+    t0 = time.perf_counter()
+    done = 0.0
+    for _ in range(args.steps):
+        r, dt, _ = oracle_rate(p, units, work, procs)
+        done += r * dt
+    dt = time.perf_counter() - t0
+    v = done / dt / div
+    if what is None:
+        what = f"{len(units)} of {p.S * p.Hkv} (slice, KV head) units per step" + (
+            f", {len(units[0][2])} query rows each" if prefill else "")
+    sample = f"{what}, fp64 oracle, {procs} processes"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": p.name},
+        "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": procs, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# keys of a configs entry (the rest is the same as the headline line's)
+CONFIG_KEYS = ("value", "unit", "ms_per_step", "dtype", "config", "roofline", "e2e", "gpu_launches", "clocks",
+               "cpu_baseline")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="decode_bf16",
-                    choices=["decode_bf16", "prefill_bf16", "prefill_bf16_small", "paged_int8", "paged_int8_small",
-                             "paged_int4", "paged_fp8",
-                             "sparse_bf16", "sparse_select_bf16", "decode_f16_small", "kv_append_int8"])
+    ap.add_argument("--workload", default=None, choices=WORKLOAD_CHOICES,
+                    help="one workload alone (default: the bf16 decode, plus the other configurations on one GPU)")
+    ap.add_argument("--no-configs", action="store_true", help="the headline workload alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle time per workload (headline: 10 s)")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA-graph replays")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    explicit = args.workload is not None
+    if not explicit:
+        args.workload = "decode_bf16"
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -811,58 +978,40 @@ def main():
         return
 
     if args.impl == "reference":
-        if rank != 0:
-            return
-        p = build_problem(args.workload)
-        prefill = args.workload.startswith("prefill")
-        unit, div = ("TFLOP/s", 1e12) if prefill else ("GB/s", 1e9)
-        units, work = oracle_units(p, prefill)
-        units, work = units[:procs], work[:procs]
-        for _ in range(args.warmup):
-            oracle_rate(p, units[:1], work[:1], 1)
-        t0 = time.perf_counter()
-        done = 0.0
-        for _ in range(args.steps):
-            r, dt, _ = oracle_rate(p, units, work, procs)
-            done += r * dt
-        dt = time.perf_counter() - t0
-        v = done / dt / div
-        what = "query rows" if prefill else "rows"
-        sample = (f"{len(units)} of {p.S * p.Hkv} (slice, KV head) units per step"
-                  + (f", {len(units[0][2])} {what} each" if prefill else "") + f", fp64 oracle, {procs} processes")
-        print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": p.name},
-            "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": procs, "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        }))
+        reference_arm(args, rank, world, procs)
         return
 
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    p = build_problem(args.workload)
-    cpu_baseline = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and p.kv_rows is not None:
-        # bounded sample of the same workload: whole passes over its units
-        # (prefill: a few query rows per unit) for about 10 s of CPU work
-        prefill = args.workload.startswith("prefill")
-        units, work = oracle_units(p, prefill)
-        v, dt, passes = oracle_rate(p, units, work, procs, min_seconds=10.0, max_passes=1000)
-        unit, div = ("TFLOP/s", 1e12) if prefill else ("GB/s", 1e9)
-        cpu_baseline = {"value": round(v / div, 6), "unit": unit, "cores": procs, "kind": "oracle",
-                        "sample": f"{len(units)} (slice, KV head) units"
-                                  + (f" x {len(units[0][2])} query rows" if prefill else " (whole workload)")
-                                  + f" x {passes} passes, {dt:.1f} s wall"}
-    res = run_gpu(args, rank, world, p, cpu_baseline)
+    # every problem is built and every oracle leg timed before the first CUDA
+    # call (the oracle's worker pool is forked)
+    names = [args.workload]
+    if not explicit and world == 1 and not args.no_configs:
+        names += CONFIG_WORKLOADS
+    cache = {}
+    problems = {n: build_problem(n, cache) for n in names}
+    baselines = {}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        for n in names:
+            if n == "sparse_select_bf16":
+                baselines[n] = None
+                continue
+            secs = 10.0 if n == names[0] else args.cpu_seconds
+            baselines[n] = cpu_leg(problems[n], n, procs, secs)
+    res = measure(args, rank, world, problems[names[0]], names[0], baselines.get(names[0]))
+    configs = {}
+    for n in names[1:]:
+        r = measure(args, rank, world, problems[n], n, baselines.get(n))
+        if r is not None:
+            configs[n] = {k: r[k] for k in CONFIG_KEYS}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     if res is not None:
+        if configs:
+            res["configs"] = configs
         print(json.dumps(res))
 
 

@@ -21,6 +21,13 @@
  *  - Row indices are NOT range-checked by the attention calls (that would cost
  *    a pass over the lists); fa_rows_validate() checks them on the device and
  *    reports through a status word, without trapping.
+ *  - Every wait inside the tensor-core kernels is bounded in time (1 s by
+ *    default, see fa_set_wait_limit_ns).  A wait that runs out is treated as a
+ *    hang: the kernel leaves its pipeline, lets its own copies and MMAs drain,
+ *    frees its tensor memory and sets FA_WS_WAIT_EXPIRED in the status word of
+ *    the call's workspace (fa_rows_status reads it).  That call's outputs are
+ *    then invalid; the call itself has already returned FA_OK, since the wait
+ *    runs on the GPU after the launch.
  */
 #ifndef FA_ROWS_H
 #define FA_ROWS_H
@@ -40,8 +47,15 @@ typedef enum fa_status {
   FA_ERR_UNSUPPORTED = 2,  /* valid but outside the shapes/dtypes built here   */
   FA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required        */
   FA_ERR_INDEX_OOB = 4,    /* reported by fa_rows_validate through its status   */
-  FA_ERR_CUDA = 5          /* a CUDA launch or runtime call failed              */
+  FA_ERR_CUDA = 5,         /* a CUDA launch or runtime call failed              */
+  FA_ERR_WAIT_EXPIRED = 6  /* not returned by a launch: the code to report when
+                            * a workspace status word holds FA_WS_WAIT_EXPIRED */
 } fa_status;
+
+/* Bits of the workspace status word (the first uint32 of every decode and
+ * prefill workspace).  Sticky: set by any call on that workspace, cleared only
+ * by fa_rows_workspace_init or fa_rows_status(..., clear = 1). */
+#define FA_WS_WAIT_EXPIRED 1u  /* a bounded pipeline wait ran out; that call's outputs are invalid */
 
 typedef enum fa_dtype { FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2, FA_I8 = 3, FA_I4 = 4, FA_F8E4M3 = 5 } fa_dtype;
 
@@ -106,15 +120,40 @@ typedef struct fa_rows_args {
 } fa_rows_args;
 
 /*
- * Bytes of scratch that fa_rows_decode / fa_rows_prefill need for these
- * arguments (0 when none).  The decode scratch holds per-split partial results
- * and one arrival counter per (slice, KV head); it must be ZERO-FILLED once
- * after allocation (fa_rows_workspace_init) — every call leaves the counters
- * at zero again.  One workspace must not be used by two calls that can run at
- * the same time.  Returns 0 and sets fa_last_error() on invalid arguments.
+ * Bytes of scratch (a device buffer, 256-byte aligned) that fa_rows_decode /
+ * fa_rows_prefill need for these arguments; at least 256.  Layout: bytes
+ * [0, 256) are the status block, whose first uint32 is the status word
+ * (FA_WS_WAIT_EXPIRED); decode then holds one arrival counter per (slice, KV
+ * head) and, when the list is split over several CTAs, the per-split partial
+ * results.  The buffer must be ZERO-FILLED once after allocation
+ * (fa_rows_workspace_init); every call leaves the counters at zero again, an
+ * aborted one included.  One workspace must not be used by two calls that can
+ * run at the same time.  Returns 0 and sets fa_last_error() on invalid
+ * arguments.
  */
 size_t fa_rows_workspace_size(const fa_rows_args* a, int is_prefill);
 fa_status fa_rows_workspace_init(void* ws, size_t ws_bytes, fa_stream_t stream);
+
+/*
+ * Enqueues on `stream` a copy of the workspace's status word into *d_status
+ * (a device uint32) and, if `clear` is non-zero, then zeroes the word.  The
+ * caller reads d_status once the stream has reached this point; a non-zero
+ * FA_WS_WAIT_EXPIRED bit means a call on this workspace since the word was
+ * last cleared had a pipeline wait run out, so its outputs are invalid.
+ * ws_bytes must be at least 256.  No counterpart on the pages: the pages
+ * describe no failure path.
+ */
+fa_status fa_rows_status(void* ws, size_t ws_bytes, uint32_t* d_status, int clear, fa_stream_t stream);
+
+/*
+ * Diagnostic: the time limit, in nanoseconds, of every bounded pipeline wait
+ * in kernels launched after this call by any thread of the process (0 restores
+ * the default of 1 s).  Lowering it to a few nanoseconds makes waits run out
+ * on purpose, which exercises the abort path and the status word in tests.
+ * The drain waits of an aborting kernel keep the 1 s default.
+ * No counterpart on the pages.
+ */
+fa_status fa_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
  * Decode: few query rows per slice (Nq * Hq/Hkv <= 32).  Split-KV over the
@@ -144,7 +183,9 @@ fa_status fa_rows_decode_static(const fa_rows_args* a, fa_stream_t stream);
 /*
  * Prefill: many query rows per slice.  QK^T and PV on the tensor cores
  * (tcgen05, accumulators in tensor memory), K/V tiles gathered by row index.
- * D = 128, FA_BF16 or FA_F16 for q and the pool; Nq >= 1.
+ * D = 128, FA_BF16 or FA_F16 for q and the pool; Nq >= 1.  The workspace
+ * (fa_rows_workspace_size(a, 1) = 256 bytes, zero-filled once) is required:
+ * it holds the status word; a NULL ws is rejected with FA_ERR_WORKSPACE.
  */
 fa_status fa_rows_prefill(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_stream_t stream);
 

@@ -15,7 +15,14 @@ Readings (the pages are silent on each):
 * dequantisation is ``float32(q) * float32(s)``, which is exact in fp32 (an
   8-bit by 11-bit significand product), so bit-exact agreement is well defined;
 * scales are stored per 64-row page and KV head, 64 to a run:
-  ``scale[r // 64, g, r % 64]``.
+  ``scale[r // 64, g, r % 64]``;
+* non-finite inputs (the pages say nothing of them): a (row, head) with a NaN
+  anywhere among its D values keeps the NaN -- its scale is stored as the
+  fp16 quiet NaN 0x7E00 and every code is 0 (INT8, INT4) or the E4M3 NaN
+  code 0x7F (FP8), so its dequantised values are all NaN, as a 16-bit pool
+  would hold a NaN; a +-Inf element (with no NaN in its row) needs no extra
+  rule: amax = Inf gives s = 65504 by the clamp above, the Inf quotient
+  saturates to the largest code and the finite quotients round to nearly 0.
 """
 from __future__ import annotations
 
@@ -52,6 +59,24 @@ def widen(bits: np.ndarray, fmt: str) -> np.ndarray:
 # INT8 codec
 
 
+def _row_scale(x32: np.ndarray, top: float):
+    """The fp16 scale of each (row, head) for a codec whose largest code is
+    ``top``, and which rows hold a NaN.
+
+    s = fp16_rne(min(amax / top, 65504)) with amax / top one correctly rounded
+    fp32 division (amax = +Inf gives 65504); a row with a NaN gets the fp16
+    quiet NaN 0x7E00, written out explicitly rather than left to numpy's NaN
+    propagation.
+    """
+    nan_row = np.isnan(x32).any(axis=-1)
+    amax = np.max(np.abs(np.where(np.isnan(x32), np.float32(0), x32)), axis=-1)   # exact
+    ratio = amax / np.float32(top)                                                # fp32, correctly rounded
+    s16 = np.minimum(ratio, np.float32(65504.0)).astype(np.float16)               # nearest-even into fp16
+    bits = s16.view(np.uint16).copy()
+    bits[nan_row] = 0x7E00
+    return bits.view(np.float16), nan_row
+
+
 def quantize_int8(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     """Symmetric INT8 per (row, head) over the last axis.
 
@@ -59,14 +84,12 @@ def quantize_int8(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     Returns (q int8 [N, H, D], s float16 [N, H]).
     """
     x32 = np.asarray(x, dtype=np.float32)
-    amax = np.max(np.abs(x32), axis=-1)                       # exact
-    ratio = amax / np.float32(127.0)                          # fp32, correctly rounded
-    s16 = np.minimum(ratio, np.float32(65504.0)).astype(np.float16)   # nearest-even into fp16
+    s16, nan_row = _row_scale(x32, 127.0)
     s32 = s16.astype(np.float32)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
         quot = x32 / s32                                      # fp32, correctly rounded
-    qv = np.clip(np.rint(quot), -127, 127)                    # rint: ties to even
-    qv = np.where(s32 == 0, 0, qv)
+    qv = np.clip(np.rint(quot), -127, 127)                    # rint: ties to even; +-Inf -> +-127
+    qv = np.where((s32 == 0) | nan_row[..., None], 0, qv)     # zero rows and NaN rows: code 0
     return qv.astype(np.int8), s16
 
 
@@ -101,14 +124,12 @@ def quantize_int4(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     Returns (packed uint8 [N, H, D/2], s float16 [N, H]).
     """
     x32 = np.asarray(x, dtype=np.float32)
-    amax = np.max(np.abs(x32), axis=-1)
-    ratio = amax / np.float32(7.0)
-    s16 = np.minimum(ratio, np.float32(65504.0)).astype(np.float16)
+    s16, nan_row = _row_scale(x32, 7.0)
     s32 = s16.astype(np.float32)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
         quot = x32 / s32
     qv = np.clip(np.rint(quot), -7, 7)
-    qv = np.where(s32 == 0, 0, qv).astype(np.int64)
+    qv = np.where((s32 == 0) | nan_row[..., None], 0, qv).astype(np.int64)
     nib = (qv & 0xF).astype(np.uint8)
     packed = nib[..., 0::2] | (nib[..., 1::2] << np.uint8(4))
     return packed.astype(np.uint8), s16
@@ -190,7 +211,9 @@ def append_rows(pool: np.ndarray, new: np.ndarray, dst_rows: np.ndarray,
 # * code = E4M3(x / s): x / s one fp32 division, then round to nearest even on
 #   the E4M3 grid (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
 #   subnormal step 2^-9, largest finite 448, no infinities), saturating to
-#   +-448; a NaN quotient gives the NaN code 0x7f;
+#   +-448 (an Inf element of a NaN-free row therefore codes as +-448); a row
+#   holding a NaN gets the NaN scale 0x7E00 and the NaN code 0x7f throughout
+#   (the non-finite reading above);
 # * dequantisation is float32(E4M3 value) * float32(s), exact in fp32 (a 4-bit
 #   by 11-bit significand product).
 
@@ -235,14 +258,13 @@ def e4m3_encode(y: np.ndarray) -> np.ndarray:
 def quantize_fp8(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     """FP8 E4M3 per (row, head) with an fp16 scale; returns (codes uint8 [N, H, D], s float16 [N, H])."""
     x32 = np.asarray(x, dtype=np.float32)
-    amax = np.max(np.abs(x32), axis=-1)
-    ratio = amax / np.float32(E4M3_MAX)
-    s16 = np.minimum(ratio, np.float32(65504.0)).astype(np.float16)
+    s16, nan_row = _row_scale(x32, E4M3_MAX)
     s32 = s16.astype(np.float32)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
         quot = x32 / s32
-    codes = e4m3_encode(quot)
+    codes = e4m3_encode(np.where(nan_row[..., None], np.float32(0), quot))
     codes = np.where(s32 == 0, np.uint8(0), codes)
+    codes = np.where(nan_row[..., None], np.uint8(0x7F), codes)   # NaN rows: the E4M3 NaN code
     return codes.astype(np.uint8), s16
 
 

@@ -21,6 +21,7 @@ import torch
 
 __all__ = [
     "FaRowsError", "lib", "library_path", "fa_rows_args", "fa_rows_workspace_size", "fa_rows_workspace_init",
+    "fa_rows_status", "fa_set_wait_limit_ns", "default_workspace", "FA_WS_WAIT_EXPIRED",
     "fa_rows_decode", "fa_rows_prefill", "fa_rows_validate", "fa_kv_page_table_to_rows", "fa_kv_quantize_int8",
     "fa_kv_dequantize_int8", "fa_kv_quantize_int4", "fa_kv_dequantize_int4", "fa_kv_quantize_fp8", "fa_kv_dequantize_fp8", "fa_kv_sparse_rows_workspace_size", "fa_kv_sparse_rows", "fa_kv_append", "fa_status_string", "fa_last_error", "fa_version",
     "FA_F16", "FA_BF16", "FA_F32", "FA_I8", "FA_I4", "FA_F8E4M3", "FA_MASK_NONE", "FA_MASK_DENSE", "FA_MASK_CAUSAL",
@@ -29,7 +30,9 @@ __all__ = [
 FA_F16, FA_BF16, FA_F32, FA_I8, FA_I4, FA_F8E4M3 = 0, 1, 2, 3, 4, 5
 FA_MASK_NONE, FA_MASK_DENSE, FA_MASK_CAUSAL = 0, 1, 2
 _STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_WORKSPACE",
-           4: "FA_ERR_INDEX_OOB", 5: "FA_ERR_CUDA"}
+           4: "FA_ERR_INDEX_OOB", 5: "FA_ERR_CUDA", 6: "FA_ERR_WAIT_EXPIRED"}
+FA_ERR_WAIT_EXPIRED = 6
+FA_WS_WAIT_EXPIRED = 1   # bit of the workspace status word (first uint32 of a workspace)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libfa_rows.so")
@@ -66,6 +69,8 @@ _P = ctypes.c_void_p
 _SIGS = {
     "fa_rows_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(fa_rows_args), ctypes.c_int]),
     "fa_rows_workspace_init": (ctypes.c_int, [_P, ctypes.c_size_t, _P]),
+    "fa_rows_status": (ctypes.c_int, [_P, ctypes.c_size_t, _P, ctypes.c_int, _P]),
+    "fa_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "fa_rows_decode": (ctypes.c_int, [ctypes.POINTER(fa_rows_args), _P, ctypes.c_size_t, _P]),
     "fa_rows_prefill": (ctypes.c_int, [ctypes.POINTER(fa_rows_args), _P, ctypes.c_size_t, _P]),
     "fa_rows_decode_static": (ctypes.c_int, [ctypes.POINTER(fa_rows_args), _P]),
@@ -151,7 +156,7 @@ def _stream(stream, device) -> int:
 
 
 class _Workspace:
-    """Caller-side scratch for the decode merge: grown on demand, zeroed once."""
+    """Caller-side scratch (status word, split counters, partials): grown on demand, zeroed once."""
 
     def __init__(self):
         self.buf: Optional[torch.Tensor] = None
@@ -168,11 +173,18 @@ class _Workspace:
 _workspaces = {}
 
 
-def _default_ws(device, stream_handle) -> _Workspace:
-    key = (str(device), stream_handle)
+def _default_ws(device, stream_handle, is_prefill: bool) -> _Workspace:
+    """The binding's own workspace for calls without one: one per (device, stream, decode or prefill)."""
+    key = (str(device), stream_handle, bool(is_prefill))
     if key not in _workspaces:
         _workspaces[key] = _Workspace()
     return _workspaces[key]
+
+
+def default_workspace(device=None, stream=None, is_prefill: bool = False) -> Optional[torch.Tensor]:
+    """The workspace tensor the binding uses for calls made without one (None before the first such call)."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return _default_ws(device, _stream(stream, device), is_prefill).buf
 
 
 def make_args(q, k, v, kv_rows, scale, *, kv_len=None, mask=None, causal=False, k_scale=None, v_scale=None,
@@ -227,15 +239,37 @@ def fa_rows_workspace_init(ws: torch.Tensor, stream=None):
     _check(lib().fa_rows_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream, ws.device)))
 
 
-def _attend(entry: str, is_prefill: bool, q, k, v, kv_rows, scale, *, workspace=None, stream=None, **kw):
+def fa_rows_status(ws: torch.Tensor, clear: bool = False, stream=None) -> int:
+    """The workspace's status word (FA_WS_WAIT_EXPIRED set: a call on it had a
+    pipeline wait run out).  Synchronises the stream to read it."""
+    sh = _stream(stream, ws.device)
+    word = torch.empty(1, dtype=torch.int32, device=ws.device)
+    _check(lib().fa_rows_status(_ptr(ws), ws.numel() * ws.element_size(), word.data_ptr(), int(clear), sh))
+    return int(word.item()) & 0xffffffff
+
+
+def fa_set_wait_limit_ns(limit_ns: int):
+    """Limit of every bounded pipeline wait in kernels launched afterwards (0 = the 1 s default)."""
+    _check(lib().fa_set_wait_limit_ns(int(limit_ns)))
+
+
+def _attend(entry: str, is_prefill: bool, q, k, v, kv_rows, scale, *, workspace=None, stream=None,
+            check_status=False, **kw):
     a, out, lse = make_args(q, k, v, kv_rows, scale, **kw)
     sh = _stream(stream, q.device)
     need = fa_rows_workspace_size(a, is_prefill)
     if workspace is None:
-        wptr, wbytes = _default_ws(q.device, sh).get(need, q.device, sh)
+        wsobj = _default_ws(q.device, sh, is_prefill)
+        wptr, wbytes = wsobj.get(need, q.device, sh)
+        wtensor = wsobj.buf
     else:
         wptr, wbytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+        wtensor = workspace
     _check(getattr(lib(), entry)(ctypes.byref(a), wptr, wbytes, sh))
+    if check_status and wtensor is not None:
+        word = fa_rows_status(wtensor, clear=True, stream=stream)
+        if word & FA_WS_WAIT_EXPIRED:
+            raise FaRowsError(FA_ERR_WAIT_EXPIRED, f"{entry}: a pipeline wait ran out; the outputs are invalid")
     return out, lse
 
 
@@ -244,7 +278,9 @@ def fa_rows_decode(q, k, v, kv_rows, scale, **kw):
 
     Keyword args: kv_len, mask (fp32 [S,Nq,L]), causal, k_scale/v_scale (int8
     pool, fp16 [R/64,Hkv,64]), out, lse, out_dtype, want_lse, n_valid_hint,
-    workspace (zero-initialised uint8 tensor), stream.
+    workspace (zero-initialised uint8 tensor), stream, check_status (read the
+    workspace status word after the call -- this synchronises -- and raise
+    FA_ERR_WAIT_EXPIRED if a pipeline wait ran out, clearing the word).
     """
     return _attend("fa_rows_decode", False, q, k, v, kv_rows, scale, **kw)
 

@@ -14,6 +14,15 @@ namespace {
 
 thread_local char g_err[512] = "";
 
+// Limit of a pipeline wait in the tensor-core kernels launched from now on
+// (0 = the kernels' default).
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+
+unsigned long long wait_limit() {
+  const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : 1000ull * 1000ull * 1000ull;
+}
+
 fa_status fail(fa_status st, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -97,17 +106,16 @@ struct DecodePlan {
   bool tc = false;   // tensor-core kernel (either of the two below)
   bool tcq = false;  // the quantised-pool tensor-core kernel
   int qvp = 0, rows = 0, chunk = 0, nsplit = 0;
-  size_t ws = 0;     // workspace bytes
-  size_t off_err = 0, off_ml = 0, off_o = 0;
+  size_t ws = 0;     // workspace bytes: status block, counters, partials
+  size_t off_cnt = 0, off_ml = 0, off_o = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kMaxSplits = far::kDecodeMaxSplits;
 
-// The prefill workspace holds one error word: non-zero after a call whose
-// pipeline waits expired (its output is then invalid).
-constexpr size_t kPrefillWorkspace = 256;
+// The prefill workspace is the status block alone.
+constexpr size_t kPrefillWorkspace = far::kStatusBytes;
 
 // Chooses the kernel and how the list is cut into per-CTA chunks.  Cost model
 // in units of rows streamed by one CTA: waves * (chunk + fixed cost) + merge
@@ -145,9 +153,11 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
     chunk_max = far::kDecodeChunkMax;
   }
   const int L = a->list_len;
+  pl->off_cnt = far::kStatusBytes;
   if ((long long)a->S * a->Nq == 0 || L == 0) {
     pl->chunk = 0;
     pl->nsplit = 1;
+    pl->ws = far::kStatusBytes;
     return FA_OK;
   }
   int occ = 0;
@@ -190,18 +200,16 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   }
   pl->chunk = (int)round_up((L + best_ns - 1) / best_ns, align);
   pl->nsplit = (L + pl->chunk - 1) / pl->chunk;
+  // [status block][counters][(max, sum) partials][O partials]
   const size_t nunit = (size_t)units;
   const size_t cnt_bytes = round_up(nunit * sizeof(unsigned int), 256);
-  pl->off_err = cnt_bytes;
-  const size_t err_bytes = pl->tc ? 256 : 0;
+  pl->ws = pl->off_cnt + cnt_bytes;
   if (pl->nsplit > 1) {
     const size_t ml_bytes = round_up(nunit * pl->nsplit * pl->rows * 2 * sizeof(float), 256);
     const size_t o_bytes = nunit * pl->nsplit * pl->rows * (size_t)a->D * sizeof(float);
-    pl->off_ml = cnt_bytes + err_bytes;
+    pl->off_ml = pl->ws;
     pl->off_o = pl->off_ml + ml_bytes;
     pl->ws = pl->off_o + o_bytes;
-  } else if (pl->tc) {
-    pl->ws = cnt_bytes + err_bytes;
   }
   return FA_OK;
 }
@@ -222,6 +230,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
     case FA_ERR_INDEX_OOB: return "FA_ERR_INDEX_OOB";
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_WAIT_EXPIRED: return "FA_ERR_WAIT_EXPIRED";
   }
   return "FA_ERR_UNKNOWN";
 }
@@ -247,6 +256,23 @@ fa_status fa_rows_workspace_init(void* ws, size_t ws_bytes, fa_stream_t stream) 
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "workspace init");
 }
 
+fa_status fa_rows_status(void* ws, size_t ws_bytes, uint32_t* d_status, int clear, fa_stream_t stream) {
+  g_err[0] = 0;
+  if (!ws || ws_bytes < far::kStatusBytes || !aligned(ws, 4))
+    return fail(FA_ERR_WORKSPACE, "a workspace of at least %zu bytes is required", far::kStatusBytes);
+  if (!d_status || !aligned(d_status, 4)) return fail(FA_ERR_INVALID_ARG, "d_status must be a device uint32");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(d_status, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), st);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "status copy");
+}
+
+fa_status fa_set_wait_limit_ns(uint64_t limit_ns) {
+  g_err[0] = 0;
+  g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  return FA_OK;
+}
+
 fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_stream_t stream) {
   g_err[0] = 0;
   fa_status st = check_common(a);
@@ -255,7 +281,7 @@ fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_st
   st = plan_decode(a, &pl);
   if (st != FA_OK) return st;
   if ((long long)a->S * a->Nq == 0) return FA_OK;
-  if (pl.ws > 0 && (!ws || ws_bytes < pl.ws || !aligned(ws, 256)))
+  if (!ws || ws_bytes < pl.ws || !aligned(ws, 256))
     return fail(FA_ERR_WORKSPACE, "decode needs %zu bytes of 256-byte aligned, zero-initialised workspace (got %zu)",
                 pl.ws, ws_bytes);
   far::DecodeParams p;
@@ -270,11 +296,13 @@ fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_st
   p.mask = a->mask;
   p.out = a->out;
   p.lse = a->lse;
-  if (pl.ws > 0) {
+  {
     char* w = static_cast<char*>(ws);
-    p.counters = reinterpret_cast<unsigned int*>(w);
-    p.part_ml = reinterpret_cast<float*>(w + pl.off_ml);
-    p.part_o = reinterpret_cast<float*>(w + pl.off_o);
+    p.counters = reinterpret_cast<unsigned int*>(w + pl.off_cnt);
+    if (pl.nsplit > 1) {
+      p.part_ml = reinterpret_cast<float*>(w + pl.off_ml);
+      p.part_o = reinterpret_cast<float*>(w + pl.off_o);
+    }
   }
   p.R = a->n_pool_rows;
   p.S = a->S;
@@ -290,11 +318,12 @@ fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_st
   p.out_dtype = a->out_dtype;
   p.mask_kind = a->mask_kind;
   p.qscale = a->scale * far::kLog2e;
+  p.wait_ns = wait_limit();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;
   const int kind = kv_kind(a->kv_dtype);
   if (pl.tc) {
-    unsigned int* err = pl.ws > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + pl.off_err) : nullptr;
+    unsigned int* err = static_cast<unsigned int*>(ws);   // the status word
     e = pl.tcq ? far::decode_tcq_launch(p, kind, err, s) : far::decode_tc_launch(p, a->D, kind, err, s);
   } else if (kind == far::KV_BF16) {
     e = far::decode_launch_bf16(p, a->D, pl.qvp, s);
@@ -317,9 +346,10 @@ fa_status fa_rows_prefill(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_s
   if (!aligned(a->q, 16)) return fail(FA_ERR_INVALID_ARG, "prefill needs 16-byte aligned q");
   if ((a->out_dtype == FA_F32 && !aligned(a->out, 16)) || !aligned(a->out, 8))
     return fail(FA_ERR_INVALID_ARG, "prefill needs a 16-byte aligned out");
-  if (ws && (ws_bytes < kPrefillWorkspace || !aligned(ws, 16)))
-    return fail(FA_ERR_WORKSPACE, "prefill workspace must be NULL or %zu bytes", kPrefillWorkspace);
   if ((long long)a->S * a->Nq == 0) return FA_OK;
+  if (!ws || ws_bytes < kPrefillWorkspace || !aligned(ws, 16))
+    return fail(FA_ERR_WORKSPACE, "prefill needs a zero-initialised workspace of %zu bytes, 16-byte aligned (it holds "
+                                  "the status word)", kPrefillWorkspace);
   far::PrefillParams p;
   memset(&p, 0, sizeof(p));
   p.q = a->q;
@@ -341,7 +371,8 @@ fa_status fa_rows_prefill(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_s
   p.mask_kind = a->mask_kind;
   p.is_bf16 = a->q_dtype == FA_BF16;
   p.qscale = a->scale * far::kLog2e;
-  p.err = static_cast<unsigned int*>(ws);
+  p.err = static_cast<unsigned int*>(ws);   // the status word
+  p.wait_ns = wait_limit();
   cudaError_t e = far::prefill_launch(p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "prefill launch");
 }

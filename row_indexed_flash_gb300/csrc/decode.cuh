@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) fa_rows_decode_kernel(const
   __shared__ int am_last;
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) am_last = (atomicAdd(p.counters + unit, 1u) == (unsigned)(p.nsplit - 1));
+  if (threadIdx.x == 0) am_last = split_arrive_last(p.counters + unit, p.nsplit, false);
   __syncthreads();
   if (!am_last) return;
   __threadfence();

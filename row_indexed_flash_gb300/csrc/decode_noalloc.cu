@@ -17,6 +17,8 @@
 // race on it and must be serialised by the caller.
 #include <stdio.h>
 
+#include <atomic>
+
 #include "fa_internal.cuh"
 
 namespace far {
@@ -31,25 +33,27 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBy
 
 // Device address of the scratch array for the current device, looked up once
 // per device.  In host code the array's name is only a host-side stand-in, so
-// the address must come from the runtime.
+// the address must come from the runtime.  The cache is atomic: two host
+// threads making their first call at once both look the address up and store
+// the same value.
 void* scratch_address(int* err) {
-  static void* addr[64] = {nullptr};
+  static std::atomic<void*> addr[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) {
     *err = e == cudaSuccess ? (int)cudaErrorInvalidDevice : (int)e;
     return nullptr;
   }
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess || !p) {
-      *err = e == cudaSuccess ? (int)cudaErrorInvalidSymbol : (int)e;
-      return nullptr;
-    }
-    addr[dev] = p;
+  void* cached = addr[dev].load(std::memory_order_relaxed);
+  if (cached) return cached;
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_scratch);
+  if (e != cudaSuccess || !p) {
+    *err = e == cudaSuccess ? (int)cudaErrorInvalidSymbol : (int)e;
+    return nullptr;
   }
-  return addr[dev];
+  addr[dev].store(p, std::memory_order_relaxed);
+  return p;
 }
 
 }  // namespace
@@ -77,7 +81,7 @@ fa_status fa_rows_decode_static(const fa_rows_args* a, fa_stream_t stream) {
     far::set_last_error(msg);
     return FA_ERR_CUDA;
   }
-  if (need > 0) {
+  if (need > 0) {   // the status word, the split counters and the partials start from zero
     const fa_status st = fa_rows_workspace_init(ws, need, stream);
     if (st != FA_OK) return st;
   }

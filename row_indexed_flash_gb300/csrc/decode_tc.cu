@@ -133,6 +133,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
   using Sh = DkShape<D, QVP, KQ, NS>;
   using namespace dk;
   const float NEG_INF = __int_as_float(0xff800000);
+  const unsigned long long wait_ns = p.wait_ns;
   const int lane = threadIdx.x & 31;
   const int G = p.G, QV = p.QV;
   const bool bf16 = p.q_bf16 != 0;
@@ -193,7 +194,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
       nx0 = entry((j + 2) * BN + lane);
       nx1 = entry((j + 2) * BN + lane + 32);
       const int jb = j0 + j * BN;   // list position of column 0
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag, wait_ns)))) break;
       tc_fence_after();
       {
         uint32_t sr[2][32];
@@ -246,7 +247,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
         if (j > 0) {
           // O row r (tensor-memory lane r) is rescaled by the lane that owns it
           const float a_r = __shfl_sync(0xffffffffu, alpha, (lane % qvp) * LPR);
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (j - 1) & 1, abort_flag)))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (j - 1) & 1, abort_flag, wait_ns)))) break;
           tc_fence_after();
 #pragma unroll
           for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -334,7 +335,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
     // drain barrier, one phase) after issuing the last one.  o_ready cannot
     // serve here: the last S only implies PV of tile T-3, so that barrier may
     // be two phases behind, where a parity wait cannot tell the phases apart.
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag));
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag, wait_ns));
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   using namespace dk;
   constexpr int NST = NS;   // stages of this instance
   const DecodeParams& p = kp.a;
-  const float NEG_INF = __int_as_float(0xff800000);
+  const unsigned long long wait_ns = p.wait_ns;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::OFF_BAR);
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       int nrow1 = lane + 32 < cnt ? __ldg(rows_g + lane + 32) : -1;
       for (int j = 0; j < T; ++j) {
         const int st = j % NST, u = j / NST;
-        if (!__all_sync(0xffffffffu, mbar_wait(empty + st, (u & 1) ^ 1, abort_flag))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(empty + st, (u & 1) ^ 1, abort_flag, wait_ns))) break;
         int rows[2] = {nrow0, nrow1};
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -590,7 +591,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
           publish(j - (NST - 1));
           published = j - (NST - 1) + 1;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(v_empty + st, (u & 1) ^ 1, abort_flag))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(v_empty + st, (u & 1) ^ 1, abort_flag, wait_ns))) break;
         int rows[2] = {nrow0, nrow1};
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -633,7 +634,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       const uint32_t id_pv = make_idesc_f16(128, D, bf16, true);
       const uint32_t sQ = smem_u32(sm + Sh::OFF_Q), sK = smem_u32(sm + Sh::OFF_K), sV = smem_u32(sm + Sh::OFF_V);
       const uint32_t tO = tbase + Sh::COL_O;
-      bool ok = mbar_wait(q_full, 0, abort_flag);
+      bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
       // Event-driven issue: QK of the next tile as soon as its K/V have landed
       // (and its S buffer is free: at most one tile ahead of the PVs), PV of
@@ -685,7 +686,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
           t_idle = globaltimer();
         } else if (*abort_flag) {
           ok = false;
-        } else if (globaltimer() - t_idle > kWaitLimitNs) {
+        } else if (globaltimer() - t_idle > wait_ns) {
           *abort_flag = 1;
           ok = false;
         }
@@ -706,16 +707,16 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
     tc_fence_after();
     tmem_dealloc(tbase, Sh::TMEM_COLS);
   }
-  if (*abort_flag) {
-    if (threadIdx.x == 0 && kp.err) atomicOr(kp.err, 1u);
-    return;
-  }
+  // An expired wait marks the workspace status word; the CTA still arrives
+  // on its split counter (marked as aborted) so the counter ends at zero.
+  const bool aborted = *abort_flag != 0;
+  if (aborted && threadIdx.x == 0 && kp.err) atomicOr(kp.err, FA_WS_WAIT_EXPIRED);
   if (p.nsplit == 1) return;
 
   // ---- cross-split merge by the last CTA of this (slice, KV head)
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *am_last = (atomicAdd(p.counters + unit, 1u) == (unsigned)(p.nsplit - 1));
+  if (threadIdx.x == 0) *am_last = split_arrive_last(p.counters + unit, p.nsplit, aborted);
   __syncthreads();
   if (!*am_last) return;
   __threadfence();

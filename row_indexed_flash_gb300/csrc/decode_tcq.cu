@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   using namespace dq;
   constexpr int NC = Sh::NC;
   const DecodeParams& p = kp.a;
+  const unsigned long long wait_ns = p.wait_ns;
   const float NEG_INF = __int_as_float(0xff800000);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     unsigned tma_pend = 0, tma_par = 0;                    // stages with a TMA load issued, and its phase parity
     for (int j = 0; j < T; ++j) {
       const int c = j % NC, u = j / NC;
-      if (!__all_sync(0xffffffffu, mbar_wait(code_empty + c, (u & 1) ^ 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(code_empty + c, (u & 1) ^ 1, abort_flag, wait_ns))) break;
       const int r0 = valid(nrow0) ? nrow0 : -1, r1 = valid(nrow1) ? nrow1 : -1;
       nrow0 = entry((j + 1) * BN + lane);
       nrow1 = entry((j + 1) * BN + lane + 32);
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       const uint32_t id_qk = make_idesc_f16(128, BN, bf16, false);
       const uint32_t id_pv = make_idesc_f16(128, D, bf16, true);
       const uint32_t sQ = smem_u32(sm + Sh::OFF_Q), sB = smem_u32(sm + Sh::OFF_B);
-      bool ok = mbar_wait(q_full, 0, abort_flag);
+      bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
       int nqk = 0, npv = 0;
       unsigned long long t_idle = 0;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
           t_idle = globaltimer();
         } else if (*abort_flag) {
           ok = false;
-        } else if (globaltimer() - t_idle > kWaitLimitNs) {
+        } else if (globaltimer() - t_idle > wait_ns) {
           *abort_flag = 1;
           ok = false;
         }
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     // this row's logit scale (written by the gather warp before q_full)
     float c = 0.f;
     if (T > w) {
-      if (!__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag))) ok = false;
+      if (!__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, wait_ns))) ok = false;
       c = row_ok ? reinterpret_cast<const float*>(sm + Sh::OFF_QS)[row] : 0.f;
     }
     float m_used = NEG_INF, l = 0.f;
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       // this warp's k-th tile is j = w + 2k; it uses S buffer j % NS
       const int sb = j % NS;
       const uint32_t tS = tbase + Sh::COL_S + sb * BN;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (j / NS) & 1, abort_flag)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (j / NS) & 1, abort_flag, wait_ns)))) break;
       tc_fence_after();
       {
         uint32_t sr[2][32];
@@ -459,7 +460,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
           // wait for the PV of this stream's previous tile (the one before it
           // is implied by the S wait: it was issued before this tile's QK)
           const float a_r = __shfl_sync(0xffffffffu, alpha, (lane % QVP) * LPR);
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready + w, (k - 1) & 1, abort_flag)))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready + w, (k - 1) & 1, abort_flag, wait_ns)))) break;
           tc_fence_after();
 #pragma unroll
           for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     // writes O columns [64w, 64w + 64)
     const float m_r = __shfl_sync(0xffffffffu, m_used, (lane % QVP) * LPR);
     const float l_r = __shfl_sync(0xffffffffu, l, (lane % QVP) * LPR);
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag));
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag, wait_ns));
     float2* X = reinterpret_cast<float2*>(sm + Sh::OFF_X);
     if (lane < QROWS) X[w * QROWS + lane] = make_float2(m_r, l_r);
     named_barrier(1, 64);   // both softmax warps, always reached exactly once
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       re2 = re3;
       re3 = ventry(j + 8);
       const int c = j % NC, u = j / NC, b = j % NB, ub = j / NB;
-      if (!__all_sync(0xffffffffu, mbar_wait(code_full + c, u & 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(code_full + c, u & 1, abort_flag, wait_ns))) break;
       const unsigned char* Kc = sm + Sh::OFF_C + c * 2 * Sh::CODES;
       const unsigned char* Vc = Kc + Sh::CODES;
       uint4 ck[NIT], cvv[NIT];
@@ -604,7 +605,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(code_empty + c);   // the codes are in registers
-      if (!__all_sync(0xffffffffu, mbar_wait(buf_empty + b, (ub & 1) ^ 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(buf_empty + b, (ub & 1) ^ 1, abort_flag, wait_ns))) break;
       unsigned char* Kb = sm + Sh::OFF_B + b * 2 * Sh::TILE;
 #pragma unroll
       for (int mat = 0; mat < 2; ++mat) {
@@ -662,16 +663,16 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     tc_fence_after();
     tmem_dealloc(tbase, Sh::TMEM_COLS);
   }
-  if (*abort_flag) {
-    if (threadIdx.x == 0 && kp.err) atomicOr(kp.err, 1u);
-    return;
-  }
+  // An expired wait marks the workspace status word; the CTA still arrives
+  // on its split counter (marked as aborted) so the counter ends at zero.
+  const bool aborted = *abort_flag != 0;
+  if (aborted && threadIdx.x == 0 && kp.err) atomicOr(kp.err, FA_WS_WAIT_EXPIRED);
   if (p.nsplit == 1) return;
 
   // ---- cross-split merge by the last CTA of this (slice, KV head)
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *am_last = (atomicAdd(p.counters + unit, 1u) == (unsigned)(p.nsplit - 1));
+  if (threadIdx.x == 0) *am_last = split_arrive_last(p.counters + unit, p.nsplit, aborted);
   __syncthreads();
   if (!*am_last) return;
   __threadfence();

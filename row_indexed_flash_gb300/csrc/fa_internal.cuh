@@ -27,6 +27,17 @@ constexpr int kDecodeWarps = 4;
 // (max, sum) for up to 32 rows in shared memory (64 KB at this cap).
 constexpr int kDecodeMaxSplits = 256;
 
+// Every decode and prefill workspace starts with a status block of this many
+// bytes; its first word is the status word (FA_WS_WAIT_EXPIRED when a
+// bounded pipeline wait ran out).  Decode's split counters follow it.
+constexpr size_t kStatusBytes = 256;
+// A CTA whose pipeline was aborted still arrives on its (slice, KV head)
+// split counter, adding this much more than a normal arrival (the low 16 bits
+// count arrivals, splits <= 256): the last arrival then knows that a split's
+// partial result is invalid, skips the merge and leaves the counter at zero
+// as every call must.
+constexpr unsigned int kAbortArrival = 1u << 16;
+
 struct DecodeParams {
   const void* q;
   const void* k;
@@ -47,6 +58,7 @@ struct DecodeParams {
   int out_dtype;            // fa_dtype of out
   int mask_kind;            // fa_mask_kind
   float qscale;             // scale * log2(e), folded into Q
+  unsigned long long wait_ns;   // limit of a pipeline wait (tensor-core kernels)
 };
 
 struct DecodeConfig {
@@ -95,7 +107,8 @@ struct PrefillParams {
   int mask_kind;
   int is_bf16;
   float qscale;         // scale * log2(e)
-  unsigned int* err;    // set non-zero if a pipeline wait expired (may be NULL)
+  unsigned int* err;    // the workspace status word: FA_WS_WAIT_EXPIRED is or-ed in when a wait expires
+  unsigned long long wait_ns;   // limit of a pipeline wait
 };
 cudaError_t prefill_launch(const PrefillParams& p, cudaStream_t st);
 bool prefill_supported(int D, int kind);

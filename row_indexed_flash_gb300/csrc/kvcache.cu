@@ -11,6 +11,15 @@
 
 namespace far {
 
+// Scale of one (row, head) for a codec whose largest code is `top`:
+// fp16_rne(min(amax/top, 65504)) with one fp32 division (amax = +Inf gives
+// 65504).  A row holding a NaN keeps it: the fp16 quiet NaN 0x7E00, and the
+// caller writes NaN codes (0 for the integer codecs, 0x7f for E4M3).
+__device__ __forceinline__ unsigned short row_scale_bits(float amax, bool has_nan, float top) {
+  if (has_nan) return 0x7E00u;
+  return __half_as_ushort(__float2half_rn(fminf(__fdiv_rn(amax, top), 65504.0f)));
+}
+
 // kv_rows[s, j] = page_table[s, j/page]*page + j%page for j < seq_len[s], else -1.
 // One thread writes four consecutive positions.
 __global__ void page_table_to_rows_kernel(const int32_t* __restrict__ pt, int max_pages,
@@ -55,7 +64,8 @@ cudaError_t launch_page_table_to_rows(const int32_t* pt, int max_pages, const in
   return cudaGetLastError();
 }
 
-// One warp per (source row, head): amax over D, fp16 scale, int8 codes.
+// One warp per (source row, head): amax over D, fp16 scale, int8 codes (a row
+// holding a NaN: scale 0x7E00, codes 0).
 __global__ void quantize_int8_kernel(const uint16_t* __restrict__ x, int x_bf16, long long n_rows, int Hkv, int D,
                                      const int32_t* __restrict__ dst_rows, int8_t* __restrict__ q,
                                      uint16_t* __restrict__ scale, long long R) {
@@ -69,6 +79,7 @@ __global__ void quantize_int8_kernel(const uint16_t* __restrict__ x, int x_bf16,
     const uint16_t* src = x + (size_t)w * D;
     float vals[8];   // D <= 256
     float amax = 0.f;
+    bool nan = false;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int d = lane + 32 * u;
@@ -78,23 +89,25 @@ __global__ void quantize_int8_kernel(const uint16_t* __restrict__ x, int x_bf16,
         f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
       }
       vals[u] = f;
-      amax = fmaxf(amax, fabsf(f));
+      amax = fmaxf(amax, fabsf(f));   // fmaxf skips NaN: tracked separately
+      nan |= f != f;
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const __half sh = __float2half_rn(fminf(__fdiv_rn(amax, 127.0f), 65504.0f));
-    const float sf = __half2float(sh);
+    const bool has_nan = __any_sync(0xffffffffu, nan);
+    const unsigned short sb = row_scale_bits(amax, has_nan, 127.0f);
+    const float sf = __half2float(__ushort_as_half(sb));
     int8_t* qd = q + ((size_t)dst * Hkv + g) * D;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int d = lane + 32 * u;
       if (d < D) {
         int c = 0;
-        if (sf != 0.f) c = min(max(__float2int_rn(__fdiv_rn(vals[u], sf)), -127), 127);
+        if (sf != 0.f && !has_nan) c = min(max(__float2int_rn(__fdiv_rn(vals[u], sf)), -127), 127);
         qd[d] = (int8_t)c;
       }
     }
-    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = __half_as_ushort(sh);
+    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = sb;
   }
 }
 
@@ -130,6 +143,7 @@ __global__ void quantize_int8_vec_kernel(const uint16_t* __restrict__ x, int x_b
     const long long dst = dst_rows ? (long long)__ldg(dst_rows + i) : i;
     float vals[EPL];
     float amax = 0.f;
+    bool nan = false;
 #pragma unroll
     for (int k = 0; k < EPL / 2; ++k) {
 #pragma unroll
@@ -137,19 +151,21 @@ __global__ void quantize_int8_vec_kernel(const uint16_t* __restrict__ x, int x_b
         const uint32_t b = e ? (raw[k] >> 16) : (raw[k] & 0xffffu);
         const float f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
         vals[2 * k + e] = f;
-        amax = fmaxf(amax, fabsf(f));
+        amax = fmaxf(amax, fabsf(f));   // fmaxf skips NaN: tracked separately
+        nan |= f != f;
       }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const bool has_nan = __any_sync(0xffffffffu, nan);
     if (dst < 0 || dst >= R) continue;   // the same for every lane of the warp
-    const __half sh = __float2half_rn(fminf(__fdiv_rn(amax, 127.0f), 65504.0f));
-    const float sf = __half2float(sh);
+    const unsigned short sb = row_scale_bits(amax, has_nan, 127.0f);
+    const float sf = __half2float(__ushort_as_half(sb));
     uint32_t packed[(EPL + 3) / 4] = {};
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       int c = 0;
-      if (sf != 0.f) c = min(max(__float2int_rn(__fdiv_rn(vals[e], sf)), -127), 127);
+      if (sf != 0.f && !has_nan) c = min(max(__float2int_rn(__fdiv_rn(vals[e], sf)), -127), 127);
       packed[e / 4] |= ((uint32_t)c & 0xffu) << (8 * (e % 4));
     }
     int8_t* qd = q + ((size_t)dst * Hkv + g) * D + lane * EPL;
@@ -160,7 +176,7 @@ __global__ void quantize_int8_vec_kernel(const uint16_t* __restrict__ x, int x_b
     } else {
       *reinterpret_cast<uint2*>(qd) = make_uint2(packed[0], packed[1]);
     }
-    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = __half_as_ushort(sh);
+    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = sb;
   }
 }
 
@@ -200,6 +216,7 @@ __global__ void quantize_int4_kernel(const uint16_t* __restrict__ x, int x_bf16,
     const uint16_t* src = x + (size_t)w * D;
     float vals[8];
     float amax = 0.f;
+    bool nan = false;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int d = 2 * (lane + 32 * u);
@@ -211,27 +228,29 @@ __global__ void quantize_int4_kernel(const uint16_t* __restrict__ x, int x_bf16,
           f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
         }
         vals[2 * u + e] = f;
-        amax = fmaxf(amax, fabsf(f));
+        amax = fmaxf(amax, fabsf(f));   // fmaxf skips NaN: tracked separately
+        nan |= f != f;
       }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const __half sh = __float2half_rn(fminf(__fdiv_rn(amax, 7.0f), 65504.0f));
-    const float sf = __half2float(sh);
+    const bool has_nan = __any_sync(0xffffffffu, nan);
+    const unsigned short sb = row_scale_bits(amax, has_nan, 7.0f);
+    const float sf = __half2float(__ushort_as_half(sb));
     uint8_t* qd = q + ((size_t)dst * Hkv + g) * (D / 2);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int t = lane + 32 * u;   // byte t holds elements 2t, 2t+1
       if (2 * t < D) {
         int c0 = 0, c1 = 0;
-        if (sf != 0.f) {
+        if (sf != 0.f && !has_nan) {
           c0 = min(max(__float2int_rn(__fdiv_rn(vals[2 * u], sf)), -7), 7);
           c1 = min(max(__float2int_rn(__fdiv_rn(vals[2 * u + 1], sf)), -7), 7);
         }
         qd[t] = (uint8_t)((c0 & 0xF) | ((c1 & 0xF) << 4));
       }
     }
-    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = __half_as_ushort(sh);
+    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = sb;
   }
 }
 
@@ -277,7 +296,7 @@ cudaError_t launch_dequantize_int4(const uint8_t* q, const uint16_t* scale, long
 
 // One warp per (source row, head), FP8 E4M3: s = fp16(min(amax/448, 65504)),
 // code = the saturating round-to-nearest-even E4M3 of x/s (one fp32 division);
-// s = 0 gives code 0.
+// s = 0 gives code 0; a row holding a NaN gets scale 0x7E00 and code 0x7f.
 __global__ void quantize_fp8_kernel(const uint16_t* __restrict__ x, int x_bf16, long long n_rows, int Hkv, int D,
                                     const int32_t* __restrict__ dst_rows, uint8_t* __restrict__ q,
                                     uint16_t* __restrict__ scale, long long R) {
@@ -291,6 +310,7 @@ __global__ void quantize_fp8_kernel(const uint16_t* __restrict__ x, int x_bf16, 
     const uint16_t* src = x + (size_t)w * D;
     float vals[8];
     float amax = 0.f;
+    bool nan = false;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int d = lane + 32 * u;
@@ -300,20 +320,24 @@ __global__ void quantize_fp8_kernel(const uint16_t* __restrict__ x, int x_bf16, 
         f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
       }
       vals[u] = f;
-      amax = fmaxf(amax, fabsf(f));
+      amax = fmaxf(amax, fabsf(f));   // fmaxf skips NaN: tracked separately
+      nan |= f != f;
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const __half sh = __float2half_rn(fminf(__fdiv_rn(amax, 448.0f), 65504.0f));
-    const float sf = __half2float(sh);
+    const bool has_nan = __any_sync(0xffffffffu, nan);
+    const unsigned short sb = row_scale_bits(amax, has_nan, 448.0f);
+    const float sf = __half2float(__ushort_as_half(sb));
     uint8_t* qd = q + ((size_t)dst * Hkv + g) * D;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int d = lane + 32 * u;
       if (d < D)
-        qd[d] = sf != 0.f ? (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(vals[u], sf), __NV_SATFINITE, __NV_E4M3) : 0;
+        qd[d] = has_nan ? (uint8_t)0x7f
+                        : sf != 0.f ? (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(vals[u], sf), __NV_SATFINITE, __NV_E4M3)
+                                    : (uint8_t)0;
     }
-    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = __half_as_ushort(sh);
+    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = sb;
   }
 }
 

@@ -16,6 +16,22 @@
 
 namespace far {
 
+// Arrival of a finished split CTA (thread 0) on its (slice, KV head) counter.
+// True for the last arrival when no split of the unit was aborted: that CTA
+// merges, then resets the counter.  An aborted split arrives with
+// kAbortArrival added; when the unit's last arrival sees one (or is one), it
+// resets the counter itself and nothing is merged, so the counter is zero
+// again for the next call whatever happened in this one.
+__device__ __forceinline__ bool split_arrive_last(unsigned int* counter, int nsplit, bool aborted) {
+  const unsigned int old = atomicAdd(counter, aborted ? kAbortArrival + 1u : 1u);
+  if ((old & (kAbortArrival - 1u)) != (unsigned int)(nsplit - 1)) return false;
+  if (aborted || old >= kAbortArrival) {
+    *counter = 0u;
+    return false;
+  }
+  return true;
+}
+
 // part_ml / part_o rows are indexed (unit * nsplit + k) * rows + r.
 // scratch: at least 2 * nsplit * QV + 2 * QV floats of shared memory.
 template <int D>

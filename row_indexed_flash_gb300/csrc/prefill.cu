@@ -21,8 +21,11 @@
 //   softmax warpgroup t (one thread per S row)
 //                  loads S_t, masks, keeps a running max that is only moved
 //                  when it grows by more than 2^8 (then O_t is rescaled in
-//                  place), writes P_t = exp2(S*c - m) as 16-bit pairs over the
-//                  first 64 columns of S_t, and finally normalises O_t.
+//                  place), writes P_t = exp2(S*c - m) over S_t as 16-bit
+//                  values (bf16: the pair P_hi = rn(P), P_lo = rn(P - P_hi),
+//                  which keeps about 16 significant bits of P where one bf16
+//                  rounding keeps 8; f16: rn(P) alone, 11 bits), and finally
+//                  normalises O_t.
 //
 // Tensor memory: S0 | S1 | O0 | O1, 128 columns each (all 512).  The two
 // warpgroups ping-pong: while one computes softmax, the tensor core runs the
@@ -109,6 +112,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
                            const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
   using namespace pf;
   const PrefillParams& p = kp.a;
+  const unsigned long long wait_ns = p.wait_ns;
   const float NEG_INF = __int_as_float(0xff800000);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
     const char* vb = static_cast<const char*>(p.v);
     for (int j = 0; j < T; ++j) {
       const int st = j % NST, u = j / NST;
-      if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag, wait_ns))) break;
       pend &= ~(1u << st);
       int rows[4];
       bool contig = true;
@@ -265,27 +269,40 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
                  kk > 0);
         }
       };
+      // P of keys 16kk..16kk+15 (8 packed columns): f16 at column 8kk; bf16
+      // P_hi at 64(kk/4) + 8(kk%4) and P_lo 32 columns after it, each
+      // multiplied by the same V rows
       auto pv = [&](int qt, int st, bool acc) {
         const uint32_t d = tbase + COL_O + qt * 128;
         const uint32_t a = tbase + COL_S + qt * 128;
+        if (bf16) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(d, a + kk * 8, sdesc_sw128(sV + st * TILE + kk * 2048, HALF, 1024), id_pv, acc || kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t vd = sdesc_sw128(sV + st * TILE + kk * 2048, HALF, 1024);
+            const uint32_t ah = a + (kk >> 2) * 64 + (kk & 3) * 8;
+            mma_ts(d, ah, vd, id_pv, acc || kk > 0);
+            mma_ts(d, ah + 32, vd, id_pv, 1);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(d, a + kk * 8, sdesc_sw128(sV + st * TILE + kk * 2048, HALF, 1024), id_pv, acc || kk > 0);
+        }
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag);
+      bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
       // Issue order per KV tile j: [PV_0(j-1), QK_0(j)], [PV_1(j-1), QK_1(j)],
       // so each tile's QK follows the PV that read its S buffer (the tensor
       // pipe runs one thread's MMAs in order).
       for (int j = 0; ok && j < T; ++j) {
         const int st = j % NST, u = j / NST;
-        if (!(ok = mbar_wait(k_full + st, u & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(k_full + st, u & 1, abort_flag, wait_ns))) break;
         tc_fence_after();
         for (int qt = 0; qt < 2 && ok; ++qt) {
           if (j > 0) {
             const int pj = j - 1, pst = pj % NST, pu = pj / NST;
-            if (qt == 0 && !(ok = mbar_wait(v_full + pst, pu & 1, abort_flag))) break;
-            if (!(ok = mbar_wait(p_full + qt, pj & 1, abort_flag))) break;
+            if (qt == 0 && !(ok = mbar_wait(v_full + pst, pu & 1, abort_flag, wait_ns))) break;
+            if (!(ok = mbar_wait(p_full + qt, pj & 1, abort_flag, wait_ns))) break;
             tc_fence_after();
             pv(qt, pst, pj > 0);
             if (qt == 1) tc_commit(kv_empty + pst);
@@ -296,9 +313,9 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       }
       if (ok) {
         const int pj = T - 1, pst = pj % NST, pu = pj / NST;
-        ok = mbar_wait(v_full + pst, pu & 1, abort_flag);
+        ok = mbar_wait(v_full + pst, pu & 1, abort_flag, wait_ns);
         for (int qt = 0; qt < 2 && ok; ++qt) {
-          if (!(ok = mbar_wait(p_full + qt, pj & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(p_full + qt, pj & 1, abort_flag, wait_ns))) break;
           tc_fence_after();
           pv(qt, pst, pj > 0);
           tc_commit(o_final + qt);
@@ -335,7 +352,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       }
       const bool all_valid = (vbits[0] & vbits[1] & vbits[2] & vbits[3]) == 0xffffffffu;
       // warp-uniform: the tcgen05 loads below need every lane of the warp
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + qt, j & 1, abort_flag)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + qt, j & 1, abort_flag, wait_ns)))) break;
       tc_fence_after();
       const bool need_mask = !all_valid || j * BN + BN - 1 > lim;
       // pass 1: the row maximum of the logits S*c (c = scale*log2e), taken on
@@ -384,50 +401,55 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
           }
         }
       }
-      // pass 2: P = exp2(S*c - m) as 16-bit pairs, invisible columns 0; half h
-      // of P (32 columns) overwrites S columns 32h..32h+31, already read here
+      // pass 2: P = exp2(S*c - m) as 16-bit pairs, invisible columns 0.  The
+      // 64 S columns of half hh are read before anything is written over
+      // them: f16 P of those keys goes to columns 32hh..32hh+31; bf16 P_hi to
+      // 64hh..64hh+31 and P_lo = rn(P - P_hi) to 64hh+32..64hh+63
       const float nmu = (m_used == NEG_INF) ? 0.f : -m_used;
       const float2 c2v = make_float2(c, c), nmu2 = make_float2(nmu, nmu);
       float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pk[32];
+        uint32_t pk[32], pl[32];
         uint32_t ra[32], rb[32];
         load_s64(ra, rb, tS, hh * 64);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int c0 = hh * 64 + cc * 32;
-          float x[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(cc == 0 ? ra[k] : rb[k]);
-          if (need_mask) {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), c2v, nmu2);
-              float2 pr = make_float2(fast_ex2(t.x), fast_ex2(t.y));
+          for (int k = 0; k < 16; ++k) {
+            const float x0 = __uint_as_float(cc == 0 ? ra[2 * k] : rb[2 * k]);
+            const float x1 = __uint_as_float(cc == 0 ? ra[2 * k + 1] : rb[2 * k + 1]);
+            const float2 t = __ffma2_rn(make_float2(x0, x1), c2v, nmu2);
+            float2 pr = make_float2(fast_ex2(t.x), fast_ex2(t.y));
+            if (need_mask) {
               if (!col_visible(c0 + 2 * k, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) pr.x = 0.f;
               if (!col_visible(c0 + 2 * k + 1, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) pr.y = 0.f;
-              sum2 = __fadd2_rn(sum2, pr);
-              pk[cc * 16 + k] = pack2(pr.x, pr.y, bf16);
             }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float2 t = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), c2v, nmu2);
-              const float2 pr = make_float2(fast_ex2(t.x), fast_ex2(t.y));
-              sum2 = __fadd2_rn(sum2, pr);
-              pk[cc * 16 + k] = pack2(pr.x, pr.y, bf16);
+            sum2 = __fadd2_rn(sum2, pr);
+            const uint32_t hi = pack2(pr.x, pr.y, bf16);
+            pk[cc * 16 + k] = hi;
+            if (bf16) {
+              const float2 rem =
+                  __fadd2_rn(pr, make_float2(-__uint_as_float(hi << 16), -__uint_as_float(hi & 0xffff0000u)));
+              pl[cc * 16 + k] = pack2(rem.x, rem.y, true);
             }
           }
         }
-        tmem_st32(tS + hh * 32, pk);
+        if (bf16) {
+          tmem_st32_nowait(tS + hh * 64, pk);
+          tmem_st32_nowait(tS + hh * 64 + 32, pl);
+          tmem_wait_st();
+        } else {
+          tmem_st32(tS + hh * 32, pk);
+        }
       }
       const float sum = sum2.x + sum2.y;
       l += sum;
       tc_fence_before();
       mbar_arrive(p_full + qt);
     }
-    if (ok && T > 0) ok = mbar_wait(o_final + qt, 0, abort_flag);
+    if (ok && T > 0) ok = mbar_wait(o_final + qt, 0, abort_flag, wait_ns);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
@@ -476,7 +498,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
-  if (threadIdx.x == 0 && *abort_flag && p.err) atomicOr(p.err, 1u);
+  if (threadIdx.x == 0 && *abort_flag && p.err) atomicOr(p.err, FA_WS_WAIT_EXPIRED);
 }
 
 // ---------------------------------------------------------------------------

@@ -24,10 +24,13 @@ constexpr int kSelBins = 2048;
 constexpr int kSelCopies = 16;   // histogram copies: two warps share one
 constexpr size_t kSelSmem = (size_t)kSelCopies * kSelBins * sizeof(int);
 
-// Larger float -> larger key; NaN -> 0, below every number (-inf -> 0x007fffff).
+// Larger float -> larger key; NaN -> 0, below every number (-inf -> 0x007fffff);
+// -0.0 and +0.0 compare equal as numbers, so both take +0.0's key and a tie
+// between them goes to the smaller position like any other tie.
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x);
   if (x != x) return 0u;
+  if (x == 0.f) return 0x80000000u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

@@ -9,8 +9,11 @@
 
 namespace far {
 
-// A wait that has not completed after this long is treated as a hang: the
-// kernel records an error and leaves its pipeline.
+// Default limit of a pipeline wait: one that has not completed after this
+// long is treated as a hang, and the kernel records an error and leaves its
+// pipeline (the launch parameters carry the limit in force, which a
+// diagnostic call may lower).  Waits for a CTA's own copies and MMAs to drain
+// before it exits always use this default.
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -68,16 +71,17 @@ __device__ __forceinline__ void named_barrier(int id, int n) {
 }
 
 // Waits for the phase with the given parity.  Gives up (returning false and
-// raising *abort) after kWaitLimitNs, or as soon as another role of the CTA
-// has raised *abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort) {
+// raising *abort) after limit_ns, or as soon as another role of the CTA has
+// raised *abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait(b, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(b, parity)) return true;
     if ((it & 15u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }

@@ -45,18 +45,38 @@ def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
 
 
+PARALLEL_CHUNK = 1 << 24
+
+
 def normal_bits(g: np.random.Generator, shape, dtype: str, chunk: int = 1 << 26) -> np.ndarray:
     """N(0,1) float32 samples rounded into ``dtype`` ('bf16' or 'f16'), as uint16 bits.
 
-    Drawn in chunks so that multi-GB pools do not need a float32 copy of the
-    whole tensor at once.
+    Small tensors are drawn from ``g`` directly.  Tensors of at least
+    ``chunk`` elements are drawn in blocks of PARALLEL_CHUNK elements: one
+    64-bit key is taken from ``g`` and block i comes from Philox(key) jumped
+    i + 1 times (independent streams), so the bytes depend on the seed alone
+    while the blocks are generated on a thread pool and no float32 copy of the
+    whole tensor is ever held.
     """
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
     conv = f32_to_bf16_bits if dtype == "bf16" else f32_to_f16_bits
-    for i in range(0, n, chunk):
-        m = min(chunk, n - i)
-        out[i:i + m] = conv(g.standard_normal(m, dtype=np.float32))
+    if n < chunk:
+        out[:] = conv(g.standard_normal(n, dtype=np.float32))
+        return out.reshape(shape)
+    key = int(g.integers(0, 1 << 63))
+    base = np.random.Philox(key=key)
+    blocks = range(0, n, PARALLEL_CHUNK)
+
+    def fill(i):
+        m = min(PARALLEL_CHUNK, n - i)
+        gi = np.random.Generator(base.jumped(i // PARALLEL_CHUNK + 1))
+        out[i:i + m] = conv(gi.standard_normal(m, dtype=np.float32))
+
+    import concurrent.futures as cf
+    import os
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1))) as ex:
+        list(ex.map(fill, blocks))
     return out.reshape(shape)
 
 
@@ -170,10 +190,11 @@ def prefill_runs_layout(n_seq: int, seq_rows: int, run: int) -> np.ndarray:
 
 def prefill_bf16(seed: int = SEED_BASE + 3, n_seq: int = 4, seq_rows: int = 99936, pool_rows: int = 400000,
                  n_query: int = 2048, run: int = 2048, Hq: int = 32, Hkv: int = 8, D: int = 128,
-                 shuffled: bool = False) -> Problem:
-    """Prefill chunk, bf16: n_seq sequences of seq_rows prompt tokens in a
-    pool_rows unified pool; one ubatch of n_query query rows per sequence at the
-    prompt's end, causal within each sequence's rows (bottom-right aligned).
+                 shuffled: bool = False, dtype: str = "bf16") -> Problem:
+    """Prefill chunk (bf16 unless ``dtype`` says f16): n_seq sequences of
+    seq_rows prompt tokens in a pool_rows unified pool; one ubatch of n_query
+    query rows per sequence at the prompt's end, causal within each sequence's
+    rows (bottom-right aligned).
 
     The pool is written in ``run``-row ubatch runs, round-robin across
     sequences; with ``shuffled`` every row is placed at a random pool slot.
@@ -185,11 +206,22 @@ def prefill_bf16(seed: int = SEED_BASE + 3, n_seq: int = 4, seq_rows: int = 9993
         rows = perm.reshape(n_seq, seq_rows)
     else:
         rows = prefill_runs_layout(n_seq, seq_rows, run)
-    q = normal_bits(g, (n_seq, n_query, Hq, D), "bf16")
-    k = normal_bits(g, (pool_rows, Hkv, D), "bf16")
-    v = normal_bits(g, (pool_rows, Hkv, D), "bf16")
-    return Problem(f"prefill-bf16 {n_seq}x{seq_rows} in {pool_rows}, {n_query} q rows, GQA {Hq}/{Hkv}, D{D}",
-                   "bf16", q, k, v, rows, 1.0 / math.sqrt(D), causal=True)
+    q = normal_bits(g, (n_seq, n_query, Hq, D), dtype)
+    k = normal_bits(g, (pool_rows, Hkv, D), dtype)
+    v = normal_bits(g, (pool_rows, Hkv, D), dtype)
+    layout = "shuffled" if shuffled else f"{run}-row runs"
+    return Problem(f"prefill-{dtype} {n_seq}x{seq_rows} in {pool_rows} ({layout}), {n_query} q rows, "
+                   f"GQA {Hq}/{Hkv}, D{D}", dtype, q, k, v, rows, 1.0 / math.sqrt(D), causal=True)
+
+
+def relabel_rows(p: Problem, seed: int, name: str) -> Problem:
+    """The same problem with every listed row moved to a random pool slot: a
+    seeded permutation of the pool applied to ``kv_rows`` (padding stays -1).
+    The pool bytes are shared, so a fully shuffled variant of a large pool
+    costs no second draw."""
+    perm = rng(seed).permutation(p.R).astype(np.int32)
+    rows = np.where(p.kv_rows >= 0, perm[np.maximum(p.kv_rows, 0)], p.kv_rows).astype(np.int32)
+    return dataclasses.replace(p, kv_rows=rows, name=name)
 
 
 def paged_int8(seed: int = SEED_BASE + 4, n_seq: int = 32, lo: int = 1024, hi: int = 131072,

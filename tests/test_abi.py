@@ -101,3 +101,21 @@ def test_kv_helpers_reject_bad_sizes(lib):
     assert lib.fa_kv_page_table_to_rows(4096, 4, 4096, 2, 0, 4096, 256, None) == 1
     assert lib.fa_kv_append(4096, far.FA_BF16, 4, 1, 4, 4096, 4096, 8, None) == 2    # 8-byte rows
     assert lib.fa_rows_validate(None, 4096, None) == 1
+
+
+def test_status_word_calls_check_their_arguments_on_the_host(lib):
+    assert far.fa_status_string(6) == "FA_ERR_WAIT_EXPIRED"
+    assert lib.fa_rows_status(None, 256, 4096, 0, None) == 3          # no workspace
+    assert lib.fa_rows_status(4096, 128, 4096, 0, None) == 3          # shorter than the status block
+    assert lib.fa_rows_status(4096, 256, None, 0, None) == 1          # no destination word
+    assert lib.fa_set_wait_limit_ns(1000) == 0
+    assert lib.fa_set_wait_limit_ns(0) == 0                           # back to the default
+
+
+def test_every_workspace_starts_with_the_status_block(lib):
+    a = _args(list_len=0)
+    assert lib.fa_rows_workspace_size(ctypes.byref(a), 0) == 256      # decode of empty lists: status block only
+    a = _args()
+    assert lib.fa_rows_workspace_size(ctypes.byref(a), 1) == 256      # prefill: the status block
+    st = lib.fa_rows_prefill(ctypes.byref(a), None, 0, None)
+    assert st == 3 and "status word" in far.fa_last_error()           # refused before anything is launched

@@ -37,6 +37,50 @@ def test_int8_quantise_and_dequantise_are_bit_exact(dtype, D):
     assert np.array_equal(deq.view(np.uint32), oracle.dequantize_int8(qo, so).view(np.uint32))
 
 
+_NONFINITE = {"bf16": (0x7FC0, 0xFFC0, 0x7F80, 0xFF80), "f16": (0x7E00, 0xFE00, 0x7C00, 0xFC00)}
+
+
+@pytest.mark.parametrize("codec,dtype,D", [("int8", "bf16", 128), ("int8", "f16", 96), ("int8", "bf16", 256),
+                                           ("int4", "bf16", 128), ("int4", "f16", 64), ("fp8", "bf16", 128),
+                                           ("fp8", "f16", 96)])
+def test_quantisers_keep_nan_and_saturate_inf_like_the_oracle(codec, dtype, D):
+    """The non-finite reading: a (row, head) holding a NaN gets scale 0x7E00
+    and NaN codes (0, or 0x7f for E4M3); an Inf element gives scale 65504 and
+    saturates.  Codes and scales bit-exact, dequantised values equal (NaN
+    where the oracle has NaN)."""
+    g = synth.rng(80)
+    R, H = 128, 4
+    bits = synth.normal_bits(g, (R, H, D), dtype)
+    qnan, nnan, pinf, ninf = _NONFINITE[dtype]
+    bits[1, 0, 5] = qnan                 # one NaN
+    bits[2, 3, D - 1] = nnan             # a negative NaN at the last element
+    bits[3, 2, 0] = pinf                 # +Inf at the first element
+    bits[4, 1, 7] = ninf                 # -Inf
+    bits[5, 0, 9], bits[5, 0, 10] = pinf, ninf       # both infinities
+    bits[6, 2, 3], bits[6, 2, 4] = pinf, qnan        # Inf and NaN: the NaN decides
+    bits[7, 3] = qnan                    # every element NaN
+    x = dev_bits(bits, dtype)
+    xo = oracle.widen(bits, dtype).astype(np.float32)
+    quant, deq_gpu, quant_o, deq_o = {
+        "int8": (far.fa_kv_quantize_int8, far.fa_kv_dequantize_int8, oracle.quantize_int8, oracle.dequantize_int8),
+        "int4": (far.fa_kv_quantize_int4, far.fa_kv_dequantize_int4, oracle.quantize_int4, oracle.dequantize_int4),
+        "fp8": (far.fa_kv_quantize_fp8, far.fa_kv_dequantize_fp8, oracle.quantize_fp8, oracle.dequantize_fp8),
+    }[codec]
+    q, s = quant(x, R)
+    qo, so = quant_o(xo)
+    got_codes = q.cpu().view(torch.uint8).numpy() if codec == "fp8" else q.cpu().numpy()
+    assert np.array_equal(got_codes.view(np.uint8), qo.view(np.uint8))
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), oracle.pack_scales(so).view(np.uint16))
+    nan_rows = [(1, 0), (2, 3), (6, 2), (7, 3)]
+    for r, h in nan_rows:
+        assert s.cpu().numpy().view(np.uint16)[r // 64, h, r % 64] == 0x7E00
+    dg = deq_gpu(q, s).cpu().numpy()
+    do = deq_o(qo, so)
+    assert np.array_equal(np.isnan(dg), np.isnan(do))
+    fin = ~np.isnan(do)
+    assert np.array_equal(dg[fin].view(np.uint32), do[fin].view(np.uint32))
+
+
 def test_int8_append_scatters_into_named_rows():
     g = synth.rng(78)
     R, H, D, n = 256, 2, 128, 40

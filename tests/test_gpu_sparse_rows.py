@@ -13,12 +13,16 @@ from helpers import assert_parity, dev_bits, oracle_for
 pytestmark = pytest.mark.gpu
 
 
-def _scores(seed, S, n, ties=False, nan_frac=0.0):
+def _scores(seed, S, n, ties=False, nan_frac=0.0, signed_zeros=False):
     g = synth.rng(seed)
     if ties:
         sc = g.integers(-3, 4, size=(S, n)).astype(np.float32)
     else:
         sc = g.standard_normal((S, n)).astype(np.float32)
+    if signed_zeros:
+        # mostly zeros of both signs, so the k-th largest score is a zero
+        sc = np.where(g.random((S, n)) < 0.9, np.float32(0.0), sc)
+        sc = np.where((sc == 0) & (g.random((S, n)) < 0.5), np.float32(-0.0), sc)
     if nan_frac:
         sc[g.random((S, n)) < nan_frac] = np.nan
     return sc
@@ -35,10 +39,16 @@ def _scores(seed, S, n, ties=False, nan_frac=0.0):
     dict(S=1, n=1, sinks=4, recent=4, k=4),
     dict(S=3, n=4099, sinks=3, recent=5, k=77, ties=True),           # rows not 16-byte aligned
     dict(S=1, n=70001, sinks=5, recent=7, k=1000, nan_frac=0.01),
+    dict(S=3, n=3000, sinks=4, recent=16, k=500, signed_zeros=True),      # the k-th score is a +-0 tie
+    dict(S=2, n=20000, sinks=1, recent=1, k=4000, signed_zeros=True, ties=True),
 ])
 def test_sparse_rows_match_oracle(case, ws):
     S, n = case["S"], case["n"]
-    sc = _scores(100 + S + n, S, n, case.get("ties", False), case.get("nan_frac", 0.0))
+    sc = _scores(100 + S + n, S, n, case.get("ties", False), case.get("nan_frac", 0.0),
+                 case.get("signed_zeros", False))
+    if case.get("signed_zeros"):
+        # the case must actually mix signs among the zeros it selects from
+        assert (np.signbit(sc) & (sc == 0)).any() and (~np.signbit(sc) & (sc == 0)).any()
     n_len = None
     if case.get("n_len"):
         n_len = synth.rng(5).integers(0, n + 1, size=S).astype(np.int32)

@@ -63,3 +63,21 @@ def test_quantiser_scale_and_exact_dequantisation():
     ok = (np.abs(x) >= s.astype(np.float32)[..., None] * 2.0 ** -6) & (np.abs(x) > 0)
     rel = np.abs(deq - x)[ok] / np.abs(x)[ok]
     assert rel.max() <= 2.0 ** -4 * 1.0001
+
+
+def test_quantiser_non_finite_rows():
+    # the non-finite reading: a NaN anywhere in a (row, head) gives scale
+    # 0x7E00 and the NaN code 0x7f for every element; an Inf element gives
+    # scale 65504 (amax/448 = Inf, clamped) and saturates to +-448 (0x7E /
+    # 0xFE), while the finite elements (|x| <= 5) fall far below the
+    # smallest subnormal step (2^-9 * 65504 = 128) and code as +-0
+    x = np.array([[3.0, np.nan, -1.0, 2.0],
+                  [1.0, np.inf, -3.0, 0.0],
+                  [-np.inf, 5.0, -0.0, 1.0]], np.float32)[:, None, :]
+    q, s = oracle.quantize_fp8(x)
+    bits = s.view(np.uint16)[:, 0].tolist()
+    assert bits == [0x7E00, 0x7BFF, 0x7BFF]
+    assert q[0, 0].tolist() == [0x7F] * 4
+    assert q[1, 0].tolist() == [0x00, 0x7E, 0x80, 0x00]
+    assert q[2, 0].tolist() == [0xFE, 0x00, 0x80, 0x00]
+    assert np.isnan(oracle.dequantize_fp8(q, s)[0]).all()

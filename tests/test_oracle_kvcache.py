@@ -92,6 +92,40 @@ def test_int8_zero_row_and_saturated_scale():
     assert float(s[0, 1]) == 65504.0 and q[0, 1, 3] == 127
 
 
+def _rows_with_non_finite():
+    """Rows [NaN row, +Inf row, -Inf row, finite row], one head, D = 8."""
+    x = np.array([[1.0, 2.0, np.nan, -3.0, 0.5, 0.0, 4.0, -1.0],
+                  [1.0, np.inf, -2.0, 0.25, 0.0, 3.0, -1.0, 2.0],
+                  [-np.inf, 1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0],
+                  [127.0, -63.5, 0.0, 1.0, 2.0, -2.0, 63.5, -127.0]], np.float32)
+    return x[:, None, :]
+
+
+def test_int8_non_finite_rows():
+    # the non-finite reading: a NaN row keeps its NaN (scale 0x7E00, every
+    # code 0, so every dequantised value is NaN); an Inf element makes
+    # amax/127 = Inf, clamped to the largest fp16 65504, and codes as +-127
+    # while the finite elements of its row (|x| <= 7 here) round to 0
+    q, s = oracle.quantize_int8(_rows_with_non_finite())
+    bits = s.view(np.uint16)[:, 0].tolist()
+    assert bits[0] == 0x7E00 and q[0, 0].tolist() == [0] * 8
+    assert np.isnan(oracle.dequantize_int8(q, s)[0]).all()
+    assert bits[1] == 0x7BFF and q[1, 0].tolist() == [0, 127, 0, 0, 0, 0, 0, 0]
+    assert bits[2] == 0x7BFF and q[2, 0].tolist() == [-127, 0, 0, 0, 0, 0, 0, 0]
+    # the finite row is untouched by its neighbours: scale 1.0 exactly (0x3C00), ties to even
+    assert bits[3] == 0x3C00 and q[3, 0].tolist() == [127, -64, 0, 1, 2, -2, 64, -127]
+
+
+def test_int4_non_finite_rows():
+    packed, s = oracle.quantize_int4(_rows_with_non_finite())
+    bits = s.view(np.uint16)[:, 0].tolist()
+    assert bits[0] == 0x7E00 and packed[0, 0].tolist() == [0, 0, 0, 0]
+    assert np.isnan(oracle.dequantize_int4(packed, s)[0]).all()
+    # +Inf -> code 7 in the high nibble of byte 0; -Inf -> code -7 (0x9) in the low nibble
+    assert bits[1] == 0x7BFF and packed[1, 0].tolist() == [0x70, 0, 0, 0]
+    assert bits[2] == 0x7BFF and packed[2, 0].tolist() == [0x09, 0, 0, 0]
+
+
 def test_int8_dequantisation_is_the_exact_product():
     g = np.random.default_rng(3)
     q = g.integers(-127, 128, size=(10, 2, 8)).astype(np.int8)

@@ -25,6 +25,17 @@ def test_ties_go_to_the_smaller_position_and_nan_ranks_last():
     assert oracle.select_rows(score, 1, 1, 5, 7).tolist() == [[0, 1, 2, 3, 4, 5, 6]]
 
 
+def test_signed_zeros_tie_and_go_to_the_smaller_position():
+    # -0.0 and +0.0 are equal numbers: middle 1..2 = [-0.0, +0.0], top-1 -> position 1
+    score = np.array([[9.0, -0.0, 0.0, 9.0]], np.float32)
+    assert oracle.select_rows(score, 1, 1, 1, 3).tolist() == [[0, 1, 3]]
+    score = np.array([[9.0, 0.0, -0.0, 9.0]], np.float32)
+    assert oracle.select_rows(score, 1, 1, 1, 3).tolist() == [[0, 1, 3]]
+    # four zeros of mixed sign below a 1.0: top-3 -> the 1.0 and the first two zeros
+    score = np.array([[0.0, -0.0, 0.0, 1.0, -0.0, 0.0, 0.0]], np.float32)
+    assert oracle.select_rows(score, 0, 0, 3, 3).tolist() == [[0, 1, 3]]
+
+
 def test_short_slices_list_every_position():
     score = np.zeros((3, 8), np.float32)
     got = oracle.select_rows(score, sinks=4, recent=4, k=2, list_len=10, n_len=np.array([3, 8, 0]))

@@ -4,9 +4,10 @@ framework owns every device allocation).  It takes its scratch from a static
 device array in the library instead of a caller workspace.
 
 Collected last on purpose, so that a run stopping at the first failure has
-already run every other test.  Compares against fa_rows_decode, with the
-parity tolerance of the other decode tests, on two calls in a row (the second
-call sees the array as the first call left it)."""
+already run every other test.  Compares both against fa_rows_decode and
+against the fp64 oracle, with the parity tolerance of the other decode tests,
+on two calls in a row (the second call sees the array as the first call left
+it)."""
 import ctypes
 
 import pytest
@@ -14,7 +15,7 @@ import torch
 
 import row_indexed_flash_gb300 as far
 import synth
-from helpers import assert_parity, dev_bits
+from helpers import assert_lse, assert_parity, dev_bits, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -29,6 +30,7 @@ def test_static_scratch_decode_matches_workspace_decode_on_two_calls():
     q, k, v, rows = _device_problem(p)
     ref, ref_lse = far.fa_rows_decode(q, k, v, rows, p.scale, want_lse=True)
     torch.cuda.synchronize()
+    o_ref, o_lse = oracle_for(p)
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):
         a, out, lse = far.make_args(q, k, v, rows, p.scale, want_lse=True)
@@ -37,6 +39,8 @@ def test_static_scratch_decode_matches_workspace_decode_on_two_calls():
         torch.cuda.synchronize()
         assert_parity(out, ref.double().cpu().numpy(), f"static-scratch call {call}")
         assert_parity(lse, ref_lse.double().cpu().numpy(), f"static-scratch lse {call}")
+        assert_parity(out, o_ref, f"static-scratch call {call} against the oracle")
+        assert_lse(lse, o_lse, f"static-scratch lse {call} against the oracle")
 
 
 def test_static_scratch_decode_rejects_plans_larger_than_the_array():
