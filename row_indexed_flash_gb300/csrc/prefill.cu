@@ -53,25 +53,28 @@ constexpr int HD = 128;                    // head dim
 constexpr int NST = 2;                     // K/V stages
 constexpr int TILE = BM * HD * 2;          // one 128 x 128 16-bit tile: 32 KB
 constexpr int HALF = TILE / 2;             // one 64-column half: 16 KB
-// warps 0-3: softmax of Q tile 0, 4-7: Q tile 1, 8: producer (TMA, Q, gather),
-// 9: MMA issuer, 10-11: gather producers
-constexpr int NWARP = 12;
-constexpr int W_PROD = 8, W_MMA = 9;
+// warps 0-15: softmax, four warpgroups (Q tile 0 columns 0-63, Q tile 0
+// columns 64-127, then the same for Q tile 1); 16: producer (TMA, Q,
+// gather); 17: MMA issuer; 18-19: gather producers
+constexpr int NWARP = 20;
+constexpr int NSMX = 16;                   // softmax warps
+constexpr int W_PROD = 16, W_MMA = 17;
 constexpr int NPROD = 3;                   // warps that gather K/V rows
-// registers per thread: the block is launched with 384 x 168; the producer
-// and MMA warpgroup keeps 64 and the two softmax warpgroups take 216 each
-// (128 x 64 + 256 x 216 = 63,488 <= 64,512 = 384 x 168)
-constexpr int REG_LAUNCH = 168, REG_LOW = 64, REG_HIGH = 216;
-static_assert(128 * REG_LOW + 256 * REG_HIGH <= NWARP * 32 * REG_LAUNCH, "register split");
+// 640 threads: at most 96 registers each (enough for every role: a softmax
+// thread holds 32 S values at a time)
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = 2 * TILE;
 constexpr int OFF_V = OFF_K + NST * TILE;
 constexpr int OFF_BAR = OFF_V + NST * TILE;
-// q_full, k_full[NST], v_full[NST], kv_empty[NST], s_full[2], p_full[2], o_final[2], drain
-constexpr int NBAR = 1 + 3 * NST + 2 + 2 + 2 + 1;
+// q_full, k_full[NST], v_full[NST], k_empty[NST], v_empty[NST], s_full[2],
+// p_full[2], o_final[2], drain, pair[8] (the two warps that share a Q tile's rows)
+constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 1 + 8;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int OFF_IDX = OFF_MISC + 16;     // [NPROD][BN] list entries of the tile each gather warp is on
-constexpr int SMEM_USED = OFF_IDX + NPROD * BN * 4;
+// [2 tile parities][2 Q tiles][2 column halves][128 rows] partial row maxima, then
+// [2 Q tiles][2 column halves][128 rows] partial row sums
+constexpr int OFF_X = OFF_IDX + NPROD * BN * 4;
+constexpr int SMEM_USED = OFF_X + (8 + 4) * BM * 4;
 constexpr int SMEM = SMEM_USED + 1024;     // slack for 1024-byte alignment
 constexpr uint32_t COL_S = 0, COL_O = 256;
 static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -123,11 +126,13 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + NST;
-  uint64_t* kv_empty = v_full + NST;
-  uint64_t* s_full = kv_empty + NST;
+  uint64_t* k_empty = v_full + NST;    // a K stage is free once both Q tiles' QK have read it
+  uint64_t* v_empty = k_empty + NST;   // a V stage once both PV have
+  uint64_t* s_full = v_empty + NST;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_final = p_full + 2;
   uint64_t* drain = o_final + 2;
+  uint64_t* pair = drain + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
 
@@ -151,14 +156,16 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       // its gathered copies land, or plain next to the TMA byte count
       mbar_init(k_full + i, NPROD * 32);
       mbar_init(v_full + i, NPROD * 32);
-      mbar_init(kv_empty + i, 1);
+      mbar_init(k_empty + i, 1);
+      mbar_init(v_empty + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
+      mbar_init(p_full + i, 256);   // both column halves of the tile's 128 rows
       mbar_init(o_final + i, 1);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(pair + i, 64);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -171,10 +178,8 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
 
-  if (warp >= 8) {
-    // the producer / MMA warpgroup gives registers to the softmax warpgroups
-    regs_release<REG_LOW>();
-    if (warp == W_PROD || warp >= 10) {
+  if (warp >= NSMX) {
+    if (warp == W_PROD || warp > W_MMA) {
       // ------------------------------------------------------------ producers
       // Per KV tile: one TMA tile load per 64-column half and matrix when the
       // 128 listed rows are one contiguous pool run (warp 8, lane 0), else a
@@ -182,11 +187,11 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       // split over the three warps (padding rows zero-filled).  Every lane of
       // the three warps arrives once per stage and matrix; gather copies arrive
       // by themselves when they land, so no warp waits for its own loads.
-      static_assert(NST == 2, "the producer tracks two stages in scalars");
-      const int pi = warp == W_PROD ? 0 : warp - 9;   // 0, 1, 2
+      const int pi = warp == W_PROD ? 0 : warp - W_MMA;   // 0, 1, 2
       const bool lead = pi == 0 && lane == 0;
-      unsigned pend = 0;       // bit st: a TMA load into stage st may still be in flight
-      int iss0 = 0, iss1 = 0;  // use count of the last TMA load into stage 0 / 1
+      // TMA loads that may still be in flight: bit st for K stage st, bit
+      // NST + st for V stage st, with the phase parity of each
+      unsigned tma_pend = 0, tma_par = 0;
       bool q_pending = false;
       if (lead && T > 0) {
         tma_prefetch_desc(&tq);
@@ -203,9 +208,35 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       int32_t* idx = reinterpret_cast<int32_t*>(sm + OFF_IDX) + pi * BN;
       // this warp's row pairs of a gathered tile: [it_lo, it_hi) of the 64
       const int it_lo = pi * 22, it_hi = min(BN / 2, it_lo + 22);
+      const int c = lane & 15;
       int nxt[4];
       #pragma unroll
       for (int t = 0; t < 4; ++t) nxt[t] = lane + 32 * t < n_s ? __ldg(rows_g + lane + 32 * t) : -1;
+      // one matrix of tile j into stage st: TMA tile loads for a contiguous
+      // run, else this warp's share of the gather; every lane arrives once
+      auto load = [&](bool contig, int r0, unsigned char* dst, const void* tmap, const char* src, uint64_t* full,
+                      int bit, int u) {
+        if (contig) {
+          if (lead) {
+            mbar_arrive_expect_tx(full, TILE);
+            tma_load_3d(dst, tmap, 0, g, r0, full);
+            tma_load_3d(dst + HALF, tmap, 64, g, r0, full);
+            tma_pend |= 1u << bit;
+            tma_par = (tma_par & ~(1u << bit)) | ((unsigned)(u & 1) << bit);
+          } else {
+            mbar_arrive(full);
+          }
+        } else {
+          for (int it = it_lo; it < it_hi; ++it) {
+            const int e = 2 * it + (lane >> 4);
+            const int r = idx[e];
+            const bool ok = r >= 0;
+            const size_t go = ((size_t)(ok ? r : 0) * p.Hkv + g) * (HD * 2) + c * 16;
+            cp_async16(dst + (c >> 3) * HALF + e * 128 + (((c & 7) ^ (e & 7)) << 4), src + go, ok);
+          }
+          cp_async_mbar_arrive_noinc(full);
+        }
+      };
       for (int j = 0; j < T; ++j) {
         const int st = j % NST, u = j / NST;
         int rows[4];
@@ -216,61 +247,34 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
           const int pos = (j + 1) * BN + lane + 32 * t;
           nxt[t] = pos < n_s ? __ldg(rows_g + pos) : -1;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(kv_empty + st, (u & 1) ^ 1, abort_flag, wait_ns))) break;
-        if (lead) pend &= ~(1u << st);
         const int r0 = __shfl_sync(0xffffffffu, rows[0], 0);
         bool contig = true;
         #pragma unroll
         for (int t = 0; t < 4; ++t) contig = contig && rows[t] >= 0 && rows[t] == r0 + lane + 32 * t;
         contig = __all_sync(0xffffffffu, contig) && kp.tma_kv;
-        unsigned char* Ks = sm + OFF_K + st * TILE;
-        unsigned char* Vs = sm + OFF_V + st * TILE;
-        if (contig) {
-          if (lead) {
-            mbar_arrive_expect_tx(k_full + st, TILE);
-            tma_load_3d(Ks, &tk, 0, g, r0, k_full + st);
-            tma_load_3d(Ks + HALF, &tk, 64, g, r0, k_full + st);
-            mbar_arrive_expect_tx(v_full + st, TILE);
-            tma_load_3d(Vs, &tv, 0, g, r0, v_full + st);
-            tma_load_3d(Vs + HALF, &tv, 64, g, r0, v_full + st);
-            pend |= 1u << st;
-            if (st == 0) iss0 = u; else iss1 = u;
-          } else {
-            mbar_arrive(k_full + st);
-            mbar_arrive(v_full + st);
-          }
-        } else {
+        if (!contig) {
           // this warp's entries of the tile, for any lane to read (the region
           // is this warp's alone: another warp may already be on the next tile)
           __syncwarp();
           #pragma unroll
           for (int t = 0; t < 4; ++t) idx[lane + 32 * t] = rows[t];
           __syncwarp();
-          const int c = lane & 15;
-          for (int it = it_lo; it < it_hi; ++it) {
-            const int e = 2 * it + (lane >> 4);
-            const int r = idx[e];
-            const bool ok = r >= 0;
-            const size_t go = ((size_t)(ok ? r : 0) * p.Hkv + g) * (HD * 2) + c * 16;
-            const uint32_t so = (c >> 3) * HALF + e * 128 + (((c & 7) ^ (e & 7)) << 4);
-            cp_async16(Ks + so, kb + go, ok);
-            cp_async16(Vs + so, vb + go, ok);
-          }
-          cp_async_mbar_arrive_noinc(k_full + st);
-          cp_async_mbar_arrive_noinc(v_full + st);
         }
+        // K as soon as both QKs of tile j - NST have read the stage, V once both PVs have
+        if (!__all_sync(0xffffffffu, mbar_wait(k_empty + st, (u & 1) ^ 1, abort_flag, wait_ns))) break;
+        if (lead) tma_pend &= ~(1u << st);
+        load(contig, r0, sm + OFF_K + st * TILE, &tk, kb, k_full + st, st, u);
+        if (!__all_sync(0xffffffffu, mbar_wait(v_empty + st, (u & 1) ^ 1, abort_flag, wait_ns))) break;
+        if (lead) tma_pend &= ~(1u << (NST + st));
+        load(contig, r0, sm + OFF_V + st * TILE, &tv, vb, v_full + st, NST + st, u);
       }
       cp_async_wait_all();
       // bulk copies still in flight must land before the CTA can exit
-      if (lead) {
-        if (q_pending && *abort_flag) mbar_wait_drain(q_full, 0);
-        if ((pend & 1u) && *abort_flag) {
-          mbar_wait_drain(k_full, iss0 & 1);
-          mbar_wait_drain(v_full, iss0 & 1);
-        }
-        if ((pend & 2u) && *abort_flag) {
-          mbar_wait_drain(k_full + 1, iss1 & 1);
-          mbar_wait_drain(v_full + 1, iss1 & 1);
+      if (lead && *abort_flag) {
+        if (q_pending) mbar_wait_drain(q_full, 0);
+        for (int st = 0; st < NST; ++st) {
+          if ((tma_pend >> st) & 1u) mbar_wait_drain(k_full + st, (tma_par >> st) & 1u);
+          if ((tma_pend >> (NST + st)) & 1u) mbar_wait_drain(v_full + st, (tma_par >> (NST + st)) & 1u);
         }
       }
     } else if (warp == W_MMA) {
@@ -288,8 +292,8 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
                    kk > 0);
           }
         };
-        // P of keys 16kk..16kk+15 (8 packed columns): f16 at column 8kk; bf16
-        // P_hi at 16kk and P_lo at 16kk + 8, each multiplied by the same V rows
+        // P of keys 16kk..16kk+15 (8 packed columns) at column 16kk; bf16
+        // also P_lo at 16kk + 8, multiplied by the same V rows
         auto pv = [&](int qt, int st, bool acc) {
           const uint32_t d = tbase + COL_O + qt * 128;
           const uint32_t a = tbase + COL_S + qt * 128;
@@ -300,47 +304,63 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
               mma_ts(d, a + kk * 16, vd, id_pv, acc || kk > 0);
               mma_ts(d, a + kk * 16 + 8, vd, id_pv, 1);
             } else {
-              mma_ts(d, a + kk * 8, vd, id_pv, acc || kk > 0);
+              mma_ts(d, a + kk * 16, vd, id_pv, acc || kk > 0);
             }
           }
         };
         bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
         tc_fence_after();
-        // Issue order per KV tile j: [PV_0(j-1), QK_0(j)], [PV_1(j-1), QK_1(j)],
-        // so each tile's QK follows the PV that read its S buffer (the tensor
-        // pipe runs one thread's MMAs in order).  Gathered stages were written
-        // by cp.async copies that arrived on their barrier by themselves: a
-        // proxy fence orders them before the tensor core's reads.
-        for (int j = 0; ok && j < T; ++j) {
-          const int st = j % NST, u = j / NST;
-          if (!(ok = mbar_wait(k_full + st, u & 1, abort_flag, wait_ns))) break;
-          tc_fence_after();
-          fence_proxy_async_smem();
-          for (int qt = 0; qt < 2 && ok; ++qt) {
-            if (j > 0) {
-              const int pj = j - 1, pst = pj % NST, pu = pj / NST;
-              if (qt == 0) {
-                if (!(ok = mbar_wait(v_full + pst, pu & 1, abort_flag, wait_ns))) break;
+        // Event-driven issue, per Q tile: QK(j), then once its P is written
+        // PV(j), then QK(j + 1) into the same S buffer (the tensor pipe runs
+        // one thread's MMAs in order, so a QK never overwrites P before the
+        // PV that reads it).  Each operation goes out as soon as its own
+        // inputs are ready; neither Q tile waits for the other, and no PV
+        // waits for the next tile's loads.  A K stage is released after both
+        // Q tiles' QK of its tile, a V stage after both PV.  Gathered stages
+        // were written by cp.async copies that arrived on their barrier by
+        // themselves: a proxy fence orders them before the tensor core's reads.
+        int nq[2] = {0, 0}, np[2] = {0, 0};   // next tile of QK / PV per Q tile
+        unsigned long long t_idle = 0;
+        while (ok && (np[0] < T || np[1] < T)) {
+          bool progressed = false;
+          #pragma unroll
+          for (int qt = 0; qt < 2; ++qt) {
+            if (np[qt] < nq[qt]) {
+              const int j = np[qt], st = j % NST;
+              if (mbar_test_wait(p_full + qt, j & 1) && mbar_test_wait(v_full + st, (j / NST) & 1)) {
+                tc_fence_after();
                 fence_proxy_async_smem();
+                pv(qt, st, j > 0);
+                ++np[qt];
+                if (np[qt ^ 1] > j) tc_commit(v_empty + st);   // both PV of tile j issued
+                if (np[qt] == T) tc_commit(o_final + qt);
+                progressed = true;
               }
-              if (!(ok = mbar_wait(p_full + qt, pj & 1, abort_flag, wait_ns))) break;
-              tc_fence_after();
-              pv(qt, pst, pj > 0);
-              if (qt == 1) tc_commit(kv_empty + pst);
             }
-            qk(qt, st);
-            tc_commit(s_full + qt);
+            if (nq[qt] < T && nq[qt] == np[qt]) {
+              const int j = nq[qt], st = j % NST;
+              if (mbar_test_wait(k_full + st, (j / NST) & 1)) {
+                tc_fence_after();
+                fence_proxy_async_smem();
+                qk(qt, st);
+                tc_commit(s_full + qt);
+                ++nq[qt];
+                if (nq[qt ^ 1] > j) tc_commit(k_empty + st);   // both QK of tile j issued
+                progressed = true;
+              }
+            }
           }
-        }
-        if (ok) {
-          const int pj = T - 1, pst = pj % NST, pu = pj / NST;
-          ok = mbar_wait(v_full + pst, pu & 1, abort_flag, wait_ns);
-          fence_proxy_async_smem();
-          for (int qt = 0; qt < 2 && ok; ++qt) {
-            if (!(ok = mbar_wait(p_full + qt, pj & 1, abort_flag, wait_ns))) break;
-            tc_fence_after();
-            pv(qt, pst, pj > 0);
-            tc_commit(o_final + qt);
+          if (progressed) {
+            t_idle = 0;
+            continue;
+          }
+          if (t_idle == 0) {
+            t_idle = globaltimer();
+          } else if (*abort_flag) {
+            ok = false;
+          } else if (globaltimer() - t_idle > wait_ns) {
+            *abort_flag = 1;
+            ok = false;
           }
         }
         tc_commit(drain);
@@ -348,19 +368,24 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       }
     }
   } else {
-    regs_acquire<REG_HIGH>();
     // ------------------------------------------------------------ softmax
-    // One thread per S row; the whole 128-column row of a tile is loaded from
-    // tensor memory once and kept in registers.
-    const int qt = warp >> 2, quad = warp & 3;
+    // Two threads per S row, one per 64-column half: each reads its half of
+    // a tile's row from tensor memory in two 32-column chunks, once for the
+    // row maximum and once to turn it into P.  The two halves' maxima are
+    // exchanged through shared memory and a bounded pair barrier, so both
+    // apply the same reference max; their sums are added at the end.
+    const int qt = warp >> 3, half = (warp >> 2) & 1, quad = warp & 3;
     const int m = quad * 32 + lane;
     const int i = i0 + qt * PT + m / G;
     const int h = g * G + m % G;
     const bool row_ok = (m < PT * G) && (i < p.Nq);
     const int lim = causal ? n_s - p.Nq + i : n_s - 1;
     const uint32_t lane_sel = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tbase + lane_sel + COL_S + qt * 128;
-    const uint32_t tO = tbase + lane_sel + COL_O + qt * 128;
+    const uint32_t tS = tbase + lane_sel + COL_S + qt * 128 + half * 64;
+    const uint32_t tO = tbase + lane_sel + COL_O + qt * 128 + half * 64;
+    uint64_t* pb = pair + qt * 4 + quad;
+    float* xmax = reinterpret_cast<float*>(sm + OFF_X);                   // [parity][qt][half][row]
+    float* xsum = xmax + 8 * BM;                                            // [qt][half][row]
     // c = scale * log2(e); a zero scale is replaced by the smallest normal
     // float, which leaves every logit 0 to within 2^-100 (so P = 1 exactly)
     // while a masked column's infinite fill still maps to -inf
@@ -369,72 +394,78 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
     const uint32_t fill = c > 0.f ? 0xff800000u : 0x7f800000u;
     float m_used = NEG_INF, l = 0.f;
     bool ok = true;
-    // list entries of the next tile, loaded one tile ahead of their use
-    int nxt[4];
+    // this half's list entries of the next tile, loaded one tile ahead
+    const int c0 = half * 64;   // first column of this half within a tile
+    int nxt[2];
     #pragma unroll
-    for (int t = 0; t < 4; ++t) nxt[t] = lane + 32 * t < n_s ? __ldg(rows_g + lane + 32 * t) : -1;
-    for (int j = 0; j < T; ++j) {
-      unsigned vbits[4];
+    for (int t = 0; t < 2; ++t) nxt[t] = c0 + lane + 32 * t < n_s ? __ldg(rows_g + c0 + lane + 32 * t) : -1;
+    int j = 0;
+    for (; j < T; ++j) {
+      unsigned vbits[2];
       #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < 2; ++t) {
         vbits[t] = __ballot_sync(0xffffffffu, nxt[t] >= 0 && (long long)nxt[t] < p.R);
-        const int pos = (j + 1) * BN + lane + 32 * t;
+        const int pos = (j + 1) * BN + c0 + lane + 32 * t;
         nxt[t] = pos < n_s ? __ldg(rows_g + pos) : -1;
       }
-      const bool all_valid = (vbits[0] & vbits[1] & vbits[2] & vbits[3]) == 0xffffffffu;
       // warp-uniform: the tcgen05 loads below need every lane of the warp
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + qt, j & 1, abort_flag, wait_ns)))) break;
       tc_fence_after();
-      uint32_t s0[32], s1[32], s2[32], s3[32];
-      tmem_ld32_nowait(tS, s0);
-      tmem_ld32_nowait(tS + 32, s1);
-      tmem_ld32_nowait(tS + 64, s2);
-      tmem_ld32_nowait(tS + 96, s3);
-      tmem_wait_ld_tied(s0);
-      tmem_wait_ld_tied(s1);
-      tmem_wait_ld_tied(s2);
-      tmem_wait_ld_tied(s3);
-      if (!all_valid || j * BN + BN - 1 > lim) {
-        #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (!col_visible(k, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) s0[k] = fill;
-          if (!col_visible(32 + k, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) s1[k] = fill;
-          if (!col_visible(64 + k, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) s2[k] = fill;
-          if (!col_visible(96 + k, vbits[0], vbits[1], vbits[2], vbits[3], j * BN, lim)) s3[k] = fill;
+      // pass 1: the row extreme of raw S over this half, 32 columns at a time
+      // (max for c > 0, min for c < 0: the logits' max is then ext * c;
+      // masked columns take the fill)
+      const int jb = j * BN + c0;   // list position of this half's first column
+      const bool masked = (vbits[0] & vbits[1]) != 0xffffffffu || jb + 63 > lim;
+      auto load_chunk = [&](uint32_t (&sv)[32], int q) {
+        tmem_ld32(tS + q * 32, sv);
+        if (masked) {
+          #pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (!(((vbits[q] >> k) & 1u) && jb + 32 * q + k <= lim)) sv[k] = fill;
         }
-      }
-      // the row maximum of the logits S*c (c = scale*log2e), taken on raw S:
-      // max(S)*c for c > 0, min(S)*c for c < 0 (masked columns hold the fill)
+      };
       float e[4];
-      if (c > 0.f) {
-        #pragma unroll
-        for (int u = 0; u < 4; ++u) e[u] = __uint_as_float(fill);
-        #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          e[0] = fmaxf(e[0], fmaxf(__uint_as_float(s0[k]), __uint_as_float(s0[k + 1])));
-          e[1] = fmaxf(e[1], fmaxf(__uint_as_float(s1[k]), __uint_as_float(s1[k + 1])));
-          e[2] = fmaxf(e[2], fmaxf(__uint_as_float(s2[k]), __uint_as_float(s2[k + 1])));
-          e[3] = fmaxf(e[3], fmaxf(__uint_as_float(s3[k]), __uint_as_float(s3[k + 1])));
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) e[u] = __uint_as_float(fill);
+      #pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t sv[32];
+        load_chunk(sv, q);
+        if (c > 0.f) {
+          #pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            e[0] = fmaxf(e[0], fmaxf(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])));
+            e[1] = fmaxf(e[1], fmaxf(__uint_as_float(sv[k + 2]), __uint_as_float(sv[k + 3])));
+            e[2] = fmaxf(e[2], fmaxf(__uint_as_float(sv[k + 4]), __uint_as_float(sv[k + 5])));
+            e[3] = fmaxf(e[3], fmaxf(__uint_as_float(sv[k + 6]), __uint_as_float(sv[k + 7])));
+          }
+        } else {
+          #pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            e[0] = fminf(e[0], fminf(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])));
+            e[1] = fminf(e[1], fminf(__uint_as_float(sv[k + 2]), __uint_as_float(sv[k + 3])));
+            e[2] = fminf(e[2], fminf(__uint_as_float(sv[k + 4]), __uint_as_float(sv[k + 5])));
+            e[3] = fminf(e[3], fminf(__uint_as_float(sv[k + 6]), __uint_as_float(sv[k + 7])));
+          }
         }
-        e[0] = fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]));
-      } else {
-        #pragma unroll
-        for (int u = 0; u < 4; ++u) e[u] = __uint_as_float(fill);
-        #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          e[0] = fminf(e[0], fminf(__uint_as_float(s0[k]), __uint_as_float(s0[k + 1])));
-          e[1] = fminf(e[1], fminf(__uint_as_float(s1[k]), __uint_as_float(s1[k + 1])));
-          e[2] = fminf(e[2], fminf(__uint_as_float(s2[k]), __uint_as_float(s2[k + 1])));
-          e[3] = fminf(e[3], fminf(__uint_as_float(s3[k]), __uint_as_float(s3[k + 1])));
-        }
-        e[0] = fminf(fminf(e[0], e[1]), fminf(e[2], e[3]));
       }
-      const float mx = (__float_as_uint(e[0]) == fill) ? NEG_INF : e[0] * c;
+      e[0] = c > 0.f ? fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3])) : fminf(fminf(e[0], e[1]), fminf(e[2], e[3]));
+      // exchange with the other half of the row (slots alternate with the
+      // tile parity, so the partner's next write cannot overwrite a slot this
+      // thread has yet to read)
+      float* xm = xmax + (((j & 1) * 2 + qt) * 2) * BM + m;
+      xm[half * BM] = e[0];
+      mbar_arrive(pb);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(pb, j & 1, abort_flag, wait_ns)))) break;
+      const float eo = xm[(half ^ 1) * BM];
+      const float ext = c > 0.f ? fmaxf(e[0], eo) : fminf(e[0], eo);
+      const float mx = (__float_as_uint(ext) == fill) ? NEG_INF : ext * c;
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + 8.f;
       if (__any_sync(0xffffffffu, need)) {
-        // rare: move the reference max and rescale O in place (PV of the
-        // previous tile has completed: it was issued before this tile's QK)
+        // rare: move the reference max and rescale this half of O in place
+        // (PV of the previous tile has completed: it was issued before this
+        // tile's QK)
         const float alpha = need ? fast_ex2(m_used - m_new) : 1.f;
         if (need) {
           l *= alpha;
@@ -442,7 +473,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
         }
         if (j > 0) {
           #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c4 = 0; c4 < 2; ++c4) {
             uint32_t r[32];
             tmem_ld32(tO + c4 * 32, r);
             #pragma unroll
@@ -451,21 +482,22 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
           }
         }
       }
-      // P = exp2(S*c - m), written over S (all of which is in registers), 16
-      // keys at a time: keys 16kk..16kk+15 as f16 P to columns 8kk..8kk+7, or
-      // as bf16 P_hi = rn(P) to 16kk..16kk+7 and P_lo = rn(P - P_hi) to
-      // 16kk+8..16kk+15; a masked column's fill gives exp2(-inf) = 0
+      // P = exp2(S*c - m), written over this half's S columns (in registers),
+      // 16 keys at a time: keys 16kk..16kk+15 of the tile to columns
+      // 16kk..16kk+7 (f16 P, or bf16 P_hi = rn(P)) and, for bf16, P_lo =
+      // rn(P - P_hi) to 16kk+8..16kk+15; a masked column's fill gives 0
       const float nmu = (m_used == NEG_INF) ? 0.f : -m_used;
       const float2 c2v = make_float2(c, c), nmu2 = make_float2(nmu, nmu);
-      float2 sum[4];
+      float2 acc = make_float2(0.f, 0.f);
       auto emit = [&](const uint32_t (&sv)[32], int q) {
-        float2 acc = make_float2(0.f, 0.f);
         #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t w[16];   // bf16: 8 P_hi words then 8 P_lo words; f16: 8 P words
+        for (int o = 0; o < 4; ++o) {
+          // keys 8o..8o+7 of this 32-column chunk: 4 P (or P_hi) words, and
+          // for bf16 4 P_lo words
+          uint32_t w[8];
           #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int x = 16 * h + 2 * k;
+          for (int k = 0; k < 4; ++k) {
+            const int x = 8 * o + 2 * k;
             const float2 t =
                 __ffma2_rn(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), c2v, nmu2);
             const float2 pr = make_float2(fast_ex2(t.x), fast_ex2(t.y));
@@ -475,26 +507,24 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
             if constexpr (BF16) {
               const float2 rem =
                   __fadd2_rn(pr, make_float2(-__uint_as_float(hi << 16), -__uint_as_float(hi & 0xffff0000u)));
-              w[8 + k] = pack2(rem.x, rem.y, true);
+              w[4 + k] = pack2(rem.x, rem.y, true);
             }
           }
-          const int kk = 2 * q + h;
-          if constexpr (BF16) {
-            tmem_st16_nowait(tS + kk * 16, w);
-          } else {
-            tmem_st8_nowait(tS + kk * 8, w);
-          }
+          // this half's keys 32q + 8o ..: column 16 * (2q + o/2) + 4 * (o%2) of its 64
+          const uint32_t col = tS + (2 * q + (o >> 1)) * 16 + (o & 1) * 4;
+          tmem_st4_nowait(col, w[0], w[1], w[2], w[3]);
+          if constexpr (BF16) tmem_st4_nowait(col + 8, w[4], w[5], w[6], w[7]);
         }
-        sum[q] = acc;
       };
-      emit(s0, 0);
-      emit(s1, 1);
-      emit(s2, 2);
-      emit(s3, 3);
+      // pass 2: the same 32-column chunks read again, turned into P
+      #pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t sv[32];
+        load_chunk(sv, q);
+        emit(sv, q);
+      }
       tmem_wait_st();
-      const float2 s01 = __fadd2_rn(sum[0], sum[1]), s23 = __fadd2_rn(sum[2], sum[3]);
-      const float2 st = __fadd2_rn(s01, s23);
-      l += st.x + st.y;
+      l += acc.x + acc.y;
       tc_fence_before();
       mbar_arrive(p_full + qt);
     }
@@ -502,10 +532,17 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const size_t orow = (((size_t)s * p.Nq + i) * p.Hq + h) * HD;
+      // the row sum is the two halves' sums (added in the same order by both)
+      xsum[(qt * 2 + half) * BM + m] = l;
+      mbar_arrive(pb);
+      ok = __all_sync(0xffffffffu, mbar_wait(pb, T & 1, abort_flag, wait_ns));
+    }
+    if (ok) {
+      const float lt = xsum[(qt * 2) * BM + m] + xsum[(qt * 2 + 1) * BM + m];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const size_t orow = (((size_t)s * p.Nq + i) * p.Hq + h) * HD + half * 64;
       #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c4 = 0; c4 < 2; ++c4) {
         uint32_t r[32];
         if (T > 0) {
           tmem_ld32(tO + c4 * 32, r);
@@ -525,18 +562,18 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
             uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow + c4 * 32);
             #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              uint4 w;
-              w.x = pack2(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv, ob);
-              w.y = pack2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv, ob);
-              w.z = pack2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv, ob);
-              w.w = pack2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv, ob);
-              o4[k] = w;
+              uint4 wv;
+              wv.x = pack2(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv, ob);
+              wv.y = pack2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv, ob);
+              wv.z = pack2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv, ob);
+              wv.w = pack2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv, ob);
+              o4[k] = wv;
             }
           }
         }
       }
-      if (row_ok && p.lse)
-        p.lse[((size_t)s * p.Nq + i) * p.Hq + h] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : NEG_INF;
+      if (row_ok && half == 0 && p.lse)
+        p.lse[((size_t)s * p.Nq + i) * p.Hq + h] = lt > 0.f ? (m_used + __log2f(lt)) * kLn2 : NEG_INF;
     }
   }
 

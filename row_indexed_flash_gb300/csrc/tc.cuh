@@ -259,6 +259,13 @@ __device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t (
                : "memory");
 }
 
+// Stores 4 consecutive 32-bit columns of this thread's lane, without the wait.
+__device__ __forceinline__ void tmem_st4_nowait(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
 // Register budget of the calling warpgroup (all four of its warps execute it):
 // give registers back to the block's pool, or take them from it.
 template <int N>
