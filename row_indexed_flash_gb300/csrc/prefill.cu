@@ -282,14 +282,18 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       if (lane == 0 && T > 0) {
         const uint32_t id_qk = make_idesc_f16(128, 128, BF16, false);
         const uint32_t id_pv = make_idesc_f16(128, 128, BF16, true);
-        const uint32_t sQ = smem_u32(sm + OFF_Q), sK = smem_u32(sm + OFF_K), sV = smem_u32(sm + OFF_V);
+        // operand descriptors built once; each MMA only adds a constant offset
+        static_assert(NST == 2, "two K and V stages");
+        const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + OFF_Q), 16, 1024), dQ1 = sdesc_at(dQ0, TILE);
+        const uint64_t dK0 = sdesc_sw128(smem_u32(sm + OFF_K), 16, 1024), dK1 = sdesc_at(dK0, TILE);
+        const uint64_t dV0 = sdesc_sw128(smem_u32(sm + OFF_V), HALF, 1024), dV1 = sdesc_at(dV0, TILE);
         auto qk = [&](int qt, int st) {
           const uint32_t d = tbase + COL_S + qt * 128;
+          const uint64_t a = qt ? dQ1 : dQ0, b = st ? dK1 : dK0;
           #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-            mma_ss(d, sdesc_sw128(sQ + qt * TILE + off, 16, 1024), sdesc_sw128(sK + st * TILE + off, 16, 1024), id_qk,
-                   kk > 0);
+            mma_ss(d, sdesc_at(a, off), sdesc_at(b, off), id_qk, kk > 0);
           }
         };
         // P of keys 16kk..16kk+15 (8 packed columns) at column 16kk; bf16
@@ -297,9 +301,10 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
         auto pv = [&](int qt, int st, bool acc) {
           const uint32_t d = tbase + COL_O + qt * 128;
           const uint32_t a = tbase + COL_S + qt * 128;
+          const uint64_t vb = st ? dV1 : dV0;
           #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t vd = sdesc_sw128(sV + st * TILE + kk * 2048, HALF, 1024);
+            const uint64_t vd = sdesc_at(vb, kk * 2048);
             if constexpr (BF16) {
               mma_ts(d, a + kk * 16, vd, id_pv, acc || kk > 0);
               mma_ts(d, a + kk * 16 + 8, vd, id_pv, 1);

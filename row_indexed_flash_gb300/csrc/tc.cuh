@@ -186,6 +186,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of the same operand layout `byte_off` bytes (a multiple of
+// 16) further on: the start address sits in the descriptor's low 14 bits as
+// address / 16, and a shared-memory address below 256 KB never carries out of
+// them.  Building a stage's descriptor once and stepping it this way keeps the
+// MMA issuing thread's per-instruction work to an add.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t d, uint32_t byte_off) { return d + (uint64_t)(byte_off >> 4); }
+
 // 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape), then
 // wait for the load; the wait is in the same statement so that no use of the
 // registers can be scheduled before it.
