@@ -313,9 +313,14 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && T > 0) {
-      const uint32_t id_qk = make_idesc_f16(128, BN, bf16, false);
+      // With at most 16 query vectors their S rows fit an M = 64 product
+      // (rows 0-15 land in tensor-memory lanes 0-15); PV stays at M = 128.
+      const uint32_t id_qk = make_idesc_f16(QVP <= 16 ? 64 : 128, BN, bf16, false);
       const uint32_t id_pv = make_idesc_f16(128, D, bf16, true);
-      const uint32_t sQ = smem_u32(sm + Sh::OFF_Q), sB = smem_u32(sm + Sh::OFF_B);
+      // operand descriptors built once; each MMA only adds a constant offset
+      const uint64_t dQ = sdesc_sw128(smem_u32(sm + Sh::OFF_Q), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(sm + Sh::OFF_B), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_B + Sh::TILE), Sh::KV_ATOM, 1024);
       bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
       int nqk = 0, npv = 0;
@@ -326,11 +331,11 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
         if (npv < nqk && mbar_test_wait(p_full + npv % NS, (npv / NS) & 1)) {
           const int b = npv % NB, sb = npv % NS;
           tc_fence_after();
-          const uint32_t vtile = sB + b * 2 * Sh::TILE + Sh::TILE;
+          const uint64_t vb = sdesc_at(dV, b * 2 * Sh::TILE);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tbase + Sh::COL_O + (npv & 1) * D, tbase + Sh::COL_S + sb * BN + kk * 8,
-                   sdesc_sw128(vtile + kk * 2048, Sh::KV_ATOM, 1024), id_pv, npv > 1 || kk > 0);
+            mma_ts(tbase + Sh::COL_O + (npv & 1) * D, tbase + Sh::COL_S + sb * BN + kk * 8, sdesc_at(vb, kk * 2048),
+                   id_pv, npv > 1 || kk > 0);
           tc_commit(buf_empty + b);
           tc_commit(o_ready + (npv & 1));
           ++npv;
@@ -341,12 +346,12 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
         if (nqk < T && nqk < npv + NS && mbar_test_wait(buf_full + nqk % NB, (nqk / NB) & 1)) {
           const int b = nqk % NB, sb = nqk % NS;
           tc_fence_after();
+          const uint64_t kbd = sdesc_at(dK, b * 2 * Sh::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t a_off = (kk >> 2) * Sh::QATOM + (kk & 3) * 32;
             const uint32_t b_off = (kk >> 2) * Sh::KV_ATOM + (kk & 3) * 32;
-            mma_ss(tbase + Sh::COL_S + sb * BN, sdesc_sw128(sQ + a_off, 16, 1024),
-                   sdesc_sw128(sB + b * 2 * Sh::TILE + b_off, 16, 1024), id_qk, kk > 0);
+            mma_ss(tbase + Sh::COL_S + sb * BN, sdesc_at(dQ, a_off), sdesc_at(kbd, b_off), id_qk, kk > 0);
           }
           tc_commit(s_full + sb);
           ++nqk;
@@ -356,7 +361,6 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
           t_idle = 0;
           continue;
         }
-        __nanosleep(32);
         if (t_idle == 0) {
           t_idle = globaltimer();
         } else if (*abort_flag) {
