@@ -137,7 +137,7 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   pl->rows = pl->tc ? (int)qv : qvp;
   int align = 0, chunk_max = 0;
   if (pl->tc) {
-    align = far::decode_tc_tile();
+    align = pl->tcq ? far::decode_tcq_tile() : far::decode_tc_tile();
     chunk_max = 1 << 30;
   } else {
     far::DecodeConfig cfg;

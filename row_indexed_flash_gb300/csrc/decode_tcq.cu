@@ -8,40 +8,46 @@
 // KV): codes x = q * s per (row, head), the fp16 scales laid out
 // [R/64][Hkv][64].
 //
-// A quantised tile carries half (INT8) or a quarter (INT4) of the bytes of a
-// 16-bit tile, so keeping HBM busy takes many tiles in flight per SM, and the
-// codes must be widened before the tensor core can use them.  One CTA per SM,
-// each (slice, KV head, split) item streamed in tiles of 64 list entries:
-//   gather warp      the listed rows' codes into a ring of NC code stages:
-//                    one TMA tile load per matrix when the 64 rows are one
-//                    contiguous run (a 64-token page), else cp.async gathers;
-//                    it never waits for its copies: they arrive on the
-//                    stage's barrier when they land.  It also stages Q as
-//                    f16, each query vector times a power of two that puts
-//                    its largest element in [2^13, 2^14) (exact for every
-//                    element within 2^-29 of the largest; the factor is taken
-//                    back out of the logit scale).
-//   4 widen warps    16 rows each: codes -> f16 in the MMA's 128-byte-swizzled
-//                    layout, into one of NB working buffers: K codes exactly
-//                    (|code| <= 127), V as rn_f16(code * s_v) (one rounding,
-//                    2^-12 relative); the code stage is released as soon as
-//                    its codes are in registers.
-//   MMA warp         S = Q K^T into one of NS buffers, O += P V (f16, P from
-//                    tensor memory, V MN-major); even tiles accumulate into
-//                    O_A, odd tiles into O_B.
-//   2 softmax warps  one per parity of the tile index, each with its own
-//                    running max/sum and its own O accumulator (warps 0 and
-//                    4: both address tensor-memory lanes 0-31, where the
-//                    query vectors' rows live).  The K scale is folded into
-//                    the logit; P = exp2(x - m) <= 2^8 is rounded once to
-//                    f16 (2^-12 relative).  At the end the two streams are
-//                    merged like two splits.
+// Keys ride in the MMA's M dimension and the query vectors of the KV head (at
+// most 32) in N, so a 128-key tile costs 16 small MMAs and the softmax is one
+// thread per key.  Per tile of 128 list entries (two 64-row halves, a page
+// each):
+//   gather warp      the listed rows' K and V codes into a ring of code
+//                    stages (128-byte rows swizzled, 64-byte INT4 rows plain):
+//                    one TMA tile load per half and matrix when the half is
+//                    one contiguous pool run, else cp.async gathers; the
+//                    copies arrive on the stage's barrier by themselves.  It
+//                    also stages Q^T: the query vectors as f16 rows, each
+//                    times a power of two that puts its largest element in
+//                    [2^13, 2^14) (exact for every element within 2^-29 of the
+//                    largest), taken back out of its logit scale.
+//   K warps (4)      one thread per key: its codes widened exactly to f16 and
+//                    stored into a K tile in tensor memory (lane = key).
+//   V warps (4)      one thread per key: its codes widened exactly to f16 into
+//                    a V buffer in shared memory (rows = keys).
+//   MMA warp         S^T = K Q^T (A = the K tile in tensor memory, B = Q^T),
+//                    then O^T += V^T P^T (A = the V buffer read MN-major, B =
+//                    P^T in shared memory); O^T holds a lane per head
+//                    dimension and a column per query vector.
+//   softmax (4)      one thread per key: its logits (the K scale folded in),
+//                    P = exp2(logit - m) against a reference max m per query
+//                    vector that moves only when a logit exceeds it by more
+//                    than 2^8 -- detected by each thread and agreed across the
+//                    four warps at one bounded barrier per tile, followed only
+//                    in that rare case by a maximum over the tile's keys and a
+//                    rescale of O^T -- then the O weight P * s_v as f16 into
+//                    P^T, kept below 2^8 by a second lazy reference of the
+//                    same kind over logit + log2|s_v|.
+//                    Each thread keeps partial row sums; they are added at the
+//                    end, when the same warps (now one thread per head
+//                    dimension) normalise O^T.
 // The last CTA to finish a (slice, KV head) merges the splits.  Every wait is
-// bounded in time and reported through an error word.
+// bounded in time and reported through the workspace status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "merge.cuh"
@@ -53,76 +59,68 @@ namespace far {
 
 namespace dq {
 constexpr int D = 128;
-constexpr int BN = 64;        // list entries per tile
-constexpr int QROWS = 32;     // query-vector rows kept in shared memory
-constexpr int NB = 4;         // 16-bit working buffers (K and V tiles)
-constexpr int NS = 4;         // S/P buffers in tensor memory: two per softmax warp
-constexpr int NCONV = 4;      // widen warps per group (16 rows each); two groups take alternate tiles
-constexpr int NWARP = 12;
-// warp roles: 0 softmax (even tiles), 1 MMA, 2 gather, 4 softmax (odd
-// tiles), widen group 0: 3, 5, 6, 8; group 1: 7, 9, 10, 11 -- the two softmax
-// warps share a scheduler (both address tensor-memory lanes 0-31), each widen
-// group spans all four
-constexpr int W_SMX0 = 0, W_MMA = 1, W_GATHER = 2, W_SMX1 = 4;
-// widen warp -> (group << 2) | index within the group
-__device__ __forceinline__ int widen_slot(int warp) {
-  switch (warp) {
-    case 3: return 0;
-    case 5: return 1;
-    case 6: return 2;
-    case 8: return 3;
-    case 7: return 4;
-    case 9: return 5;
-    case 10: return 6;
-    default: return 7;   // 11
-  }
-}
+constexpr int BN = 128;       // list entries per tile
+constexpr int HB = 64;        // rows per half tile (a 64-token page)
+constexpr int QROWS = 32;     // query vectors per KV head, at most
+constexpr int NKT = 4;        // K tiles in tensor memory
+constexpr int NS = 2;         // S^T buffers in tensor memory
+constexpr int NVB = 2;        // widened V buffers
+constexpr int NPB = 2;        // P^T buffers
+constexpr int NWARP = 14;
+// warps 0-3: softmax and epilogue (tensor-memory lane quarter = warp);
+// 4-7: K widen (lane quarter = warp - 4); 8: gather; 9: MMA; 10-13: V widen
+constexpr int W_K0 = 4, W_GATHER = 8, W_MMA = 9, W_V0 = 10;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_K = 0;                  // NKT K tiles of 64 columns (128 f16 per key)
+constexpr uint32_t COL_S = NKT * 64;           // NS S^T buffers of NQ columns
 }  // namespace dq
 
 // KQ: 1 = INT8 codes, 2 = INT4 codes (two per byte), 3 = FP8 E4M3 codes.
 template <int QVP, int KQ>
 struct DqShape {
+  static constexpr int NQ = QVP < 16 ? 16 : QVP;            // MMA N: query vectors, padded
   static constexpr int CB = KQ == 2 ? dq::D / 2 : dq::D;   // code bytes of one (row, head)
   static constexpr int CPR = CB / 16;                      // their 16-byte chunks
-  static constexpr int QATOM = dq::QROWS * 128;
-  static constexpr int Q_BYTES = 2 * QATOM;
-  static constexpr int KV_ATOM = dq::BN * 128;
-  static constexpr int TILE = 2 * KV_ATOM;                 // one 16-bit K (or V) tile
+  static constexpr int WPC = 64 / CPR;                     // widened f16 pairs per chunk
   static constexpr int CODES = dq::BN * CB;                // one tile's K (or V) codes
-  static constexpr int LPR = 32 / QVP;                     // softmax lanes per query vector
-  static constexpr int SSTR = dq::BN + (2 * LPR) % 32;     // padded S row stride (floats)
-  static constexpr int SPP = dq::BN + LPR % 32;            // padded P row stride (words)
-  static constexpr int SROW = SSTR > SPP ? SSTR : SPP;
-  static constexpr int STAGE_SM = ((QVP * SROW * 4 + 2 * dq::BN * 4 + 127) / 128) * 128;   // S/P rows + scales
+  static constexpr int STAGE = 2 * CODES;
+  static constexpr int QATOM = NQ * 128;                   // Q^T: NQ rows x 128 B per 64 dimensions
+  static constexpr int PATOM = NQ * 128;                   // P^T: NQ rows x 128 B per 64 keys
+  static constexpr int PBUF = 2 * PATOM;
+  static constexpr int VATOM = dq::BN * 128;               // V buffer: 128 keys x 128 B per 64 dimensions
+  static constexpr int VBUF = 2 * VATOM;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_B = ((Q_BYTES + 1023) / 1024) * 1024;
-  static constexpr int OFF_C = OFF_B + dq::NB * 2 * TILE;
-  static constexpr int TAIL = 512 + 128 + 2 * STAGE_SM + 3 * dq::QROWS * 8;   // barriers, misc, staging, exchange, scales
+  static constexpr int OFF_P = ((2 * QATOM + 1023) / 1024) * 1024;
+  static constexpr int OFF_V = OFF_P + dq::NPB * PBUF;
+  static constexpr int OFF_C = OFF_V + dq::NVB * VBUF;
+  // barriers, misc words, agreement flags [2][4], per-warp maxima (two
+  // kinds) and sums [3][4][QROWS], per-query-vector logit scales [QROWS],
+  // references [2][3][QROWS]
+  static constexpr int TAIL = 512 + 64 + 64 + 3 * 4 * dq::QROWS * 4 + dq::QROWS * 4 + 6 * dq::QROWS * 4;
   static constexpr int BUDGET = 227 * 1024 - 1024 - OFF_C - TAIL;
-  static constexpr int NC = BUDGET / (2 * CODES) < 8 ? BUDGET / (2 * CODES) : 8;   // code stages
-  static constexpr int OFF_BAR = OFF_C + NC * 2 * CODES;
-  // q_full, code_full[NC], code_empty[NC], buf_full[NB], buf_empty[NB], s_full[NS], p_full[NS], o_ready[2], drain
-  static constexpr int NBAR = 1 + 2 * NC + 2 * dq::NB + 2 * dq::NS + 2 + 1;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // tmem base, abort flag, last-CTA flag
-  static constexpr int OFF_SM = ((OFF_MISC + 16 + 127) / 128) * 128;
-  static constexpr int OFF_X = OFF_SM + 2 * STAGE_SM;      // [2][QROWS] (max, sum) of the two streams
-  static constexpr int OFF_QS = OFF_X + 2 * dq::QROWS * 8; // [QROWS] logit scale of each query vector
-  static constexpr int SMEM_USED = OFF_QS + dq::QROWS * 4;
+  static constexpr int NC = BUDGET / STAGE < 8 ? BUDGET / STAGE : 8;   // code stages
+  static constexpr int OFF_BAR = OFF_C + NC * STAGE;
+  // q_full, code_full[NC], code_empty[NC], kt_full[NKT], kt_empty[NKT], vb_full[NVB],
+  // vb_empty[NVB], s_full[NS], p_full[NPB], p_empty[NPB], o_ready, agree, drain
+  static constexpr int NBAR = 1 + 2 * NC + 2 * dq::NKT + 2 * dq::NVB + dq::NS + 2 * dq::NPB + 3;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag, last-CTA flag
+  static constexpr int OFF_FLAG = OFF_MISC + 16;              // [2][4] int
+  static constexpr int OFF_RED = OFF_FLAG + 32;               // [2][4][QROWS] float: tile maxima
+  static constexpr int OFF_SUM = OFF_RED + 8 * dq::QROWS * 4;  // [4][QROWS] float: final row sums
+  static constexpr int OFF_QS = OFF_SUM + 4 * dq::QROWS * 4;  // [QROWS] float
+  static constexpr int OFF_REF = OFF_QS + dq::QROWS * 4;      // [2][3][QROWS] float: ml, mo, cw
+  static constexpr int SMEM_USED = OFF_REF + 6 * dq::QROWS * 4;
   static constexpr int SMEM = SMEM_USED + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0;                     // S0..S3: 64 columns each
-  static constexpr uint32_t COL_O = dq::NS * dq::BN;       // O_A, O_B: 128 columns each
-  static_assert(COL_O + 2 * dq::D <= TMEM_COLS, "tensor memory");
+  static constexpr uint32_t COL_O = dq::COL_S + dq::NS * NQ;   // O^T: NQ columns
+  static_assert(COL_O + NQ <= dq::TMEM_COLS, "tensor memory");
   static_assert(NC >= 3, "code ring too shallow");
   static_assert(NBAR * 8 <= 512, "barrier area");
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(OFF_B % 1024 == 0 && TILE % 1024 == 0 && OFF_C % 1024 == 0, "tiles must be 1024-byte aligned");
-  static_assert(CODES % 16 == 0 && OFF_SM % 16 == 0 && STAGE_SM % 16 == 0, "16-byte alignment");
-  // the 128-row Q operand reads past the 32 stored rows (results never used):
-  // those reads stay inside the allocation
-  static_assert(OFF_Q + QATOM + 16 * 1024 <= SMEM_USED, "A-operand overrun");
-  // split merge scratch (up to 2 * 256 * 32 + 64 floats) reuses the working buffers and code ring
-  static_assert(OFF_BAR - OFF_B >= (2 * kDecodeMaxSplits * dq::QROWS + 2 * dq::QROWS) * 4, "merge scratch");
+  static_assert(OFF_P % 1024 == 0 && OFF_V % 1024 == 0 && OFF_C % 1024 == 0 && STAGE % 1024 == 0 &&
+                    CODES % 1024 == 0 && QATOM % 1024 == 0 && PATOM % 1024 == 0,
+                "operand tiles and swizzled stages must be 1024-byte aligned");
+  // split merge scratch (up to 2 * 256 * 32 + 64 floats) reuses the code ring
+  static_assert(NC * STAGE >= (2 * kDecodeMaxSplits * dq::QROWS + 2 * dq::QROWS) * 4, "merge scratch");
 };
 
 struct DqParams {
@@ -140,15 +138,47 @@ __device__ __forceinline__ void dq_wait_drain(uint64_t* b, uint32_t parity) {
   }
 }
 
+// Widened f16 pairs of 16-byte code chunk `cw`: INT8 / FP8 chunks hold 16
+// codes (8 words out), INT4 chunks 32 codes (16 words out); word t holds the
+// chunk's elements 2t and 2t + 1.
+template <int KQ>
+__device__ __forceinline__ void widen_chunk(const uint4& cw, uint32_t* w) {
+  if constexpr (KQ == 1) {
+    const uint2 a = widen_i8x4(cw.x, false), b = widen_i8x4(cw.y, false);
+    const uint2 c = widen_i8x4(cw.z, false), d = widen_i8x4(cw.w, false);
+    w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y; w[4] = c.x; w[5] = c.y; w[6] = d.x; w[7] = d.y;
+  } else if constexpr (KQ == 3) {
+    const uint2 a = widen_e4m3x4(cw.x), b = widen_e4m3x4(cw.y), c = widen_e4m3x4(cw.z), d = widen_e4m3x4(cw.w);
+    w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y; w[4] = c.x; w[5] = c.y; w[6] = d.x; w[7] = d.y;
+  } else {
+    const uint32_t v[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint4 h = widen_i4x8(v[t], false);
+      w[4 * t] = h.x; w[4 * t + 1] = h.y; w[4 * t + 2] = h.z; w[4 * t + 3] = h.w;
+    }
+  }
+}
+
+// Byte offset of 16-byte chunk ch of code row k within one matrix of a stage:
+// 128-byte rows in the 128-byte swizzle (what the TMA writes), 64-byte rows plain.
+template <int CB>
+__device__ __forceinline__ uint32_t code_off(int k, int ch) {
+  if constexpr (CB == 128) return (uint32_t)(k * 128 + ((ch ^ (k & 7)) << 4));
+  return (uint32_t)(k * CB + ch * 16);
+}
+
 }  // namespace
 
+// 448 threads: 14 warps put four on some of the SM's four schedulers, whose
+// register files hold 16,384 each, so at most 128 registers per thread
 template <int QVP, int KQ>
 __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     fa_rows_decode_tcq_kernel(const DqParams kp, const __grid_constant__ CUtensorMap tk,
                               const __grid_constant__ CUtensorMap tv) {
   using Sh = DqShape<QVP, KQ>;
   using namespace dq;
-  constexpr int NC = Sh::NC;
+  constexpr int NC = Sh::NC, NQ = Sh::NQ, CB = Sh::CB, CPR = Sh::CPR;
   const DecodeParams& p = kp.a;
   const unsigned long long wait_ns = p.wait_ns;
   const float NEG_INF = __int_as_float(0xff800000);
@@ -158,12 +188,16 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   uint64_t* q_full = bars;
   uint64_t* code_full = q_full + 1;
   uint64_t* code_empty = code_full + NC;
-  uint64_t* buf_full = code_empty + NC;
-  uint64_t* buf_empty = buf_full + NB;
-  uint64_t* s_full = buf_empty + NB;
+  uint64_t* kt_full = code_empty + NC;
+  uint64_t* kt_empty = kt_full + NKT;
+  uint64_t* vb_full = kt_empty + NKT;
+  uint64_t* vb_empty = vb_full + NVB;
+  uint64_t* s_full = vb_empty + NVB;
   uint64_t* p_full = s_full + NS;
-  uint64_t* o_ready = p_full + NS;
-  uint64_t* drain = o_ready + 2;
+  uint64_t* p_empty = p_full + NPB;
+  uint64_t* o_ready = p_empty + NPB;
+  uint64_t* agree = o_ready + 1;
+  uint64_t* drain = agree + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Sh::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::OFF_MISC + 4);
   int* am_last = reinterpret_cast<int*>(sm + Sh::OFF_MISC + 8);
@@ -172,7 +206,6 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int G = p.G, QV = p.QV;
   const bool q_bf16 = p.q_bf16 != 0;
-  constexpr bool bf16 = false;   // every MMA operand is f16 here
   int n_s = p.L;
   if (p.kv_len) n_s = min(max(__ldg(p.kv_len + s), 0), p.L);
   const int j0 = split * p.chunk;
@@ -180,32 +213,49 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   const int T = (cnt + BN - 1) / BN;
   const int32_t* rows_g = p.kv_rows + (size_t)s * p.L + j0;
   const size_t unit = (size_t)s * p.Hkv + g;
-  auto entry = [&](int pos) { return pos < cnt ? __ldg(rows_g + pos) : -1; };
+  // List loads run tiles ahead of their use: each reads a clamped (always
+  // valid) position and returns the raw entry, and the range test is applied
+  // where the value is used, so no instruction waits on the load at issue.
+  const int32_t* rows_safe = cnt > 0 ? rows_g : p.kv_rows;
+  const int pos_max = cnt > 0 ? cnt - 1 : 0;
+  auto entry_raw = [&](int pos) { return __ldg(rows_safe + min(pos, pos_max)); };
+  auto live = [&](int pos, int e) { return pos < cnt ? e : -1; };
   auto valid = [&](int r) { return r >= 0 && (long long)r < p.R; };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < NC; ++i) {
-      mbar_init(code_full + i, 32);   // one asynchronous arrival per gather lane
-      mbar_init(code_empty + i, NCONV);
+      mbar_init(code_full + i, 32);   // one arrival per gather lane
+      mbar_init(code_empty + i, 8);   // one per K warp and per V warp
     }
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(buf_full + i, NCONV);
-      mbar_init(buf_empty + i, 1);
+    for (int i = 0; i < NKT; ++i) {
+      mbar_init(kt_full + i, 4);
+      mbar_init(kt_empty + i, 1);
     }
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 1);
+    for (int i = 0; i < NVB; ++i) {
+      mbar_init(vb_full + i, 4);
+      mbar_init(vb_empty + i, 1);
+    }
+    for (int i = 0; i < NS; ++i) mbar_init(s_full + i, 1);
+    for (int i = 0; i < NPB; ++i) {
+      mbar_init(p_full + i, 4);
+      mbar_init(p_empty + i, 1);
     }
     mbar_init(o_ready, 1);
-    mbar_init(o_ready + 1, 1);
+    mbar_init(agree, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == W_MMA) {
-    tmem_alloc(tmem_holder, Sh::TMEM_COLS);
+    tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
+  }
+  if (warp == 0) {   // the softmax references' first copy: ml = mo = -inf, cw = 0
+    float* refs = reinterpret_cast<float*>(sm + Sh::OFF_REF);
+    refs[lane] = NEG_INF;
+    refs[QROWS + lane] = NEG_INF;
+    refs[2 * QROWS + lane] = 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -217,12 +267,13 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     const char* kb = static_cast<const char*>(p.k);
     const char* vb = static_cast<const char*>(p.v);
     if (T > 0) {
-      // query vectors -> rows 0..QV-1 of the swizzled Q tile, as f16 times
-      // 2^k_r; the row's logit scale becomes qscale * 2^-k_r.  16 lanes per
-      // row, 8 elements (one 16-byte chunk) each.
+      // Q^T: query vector r -> row r of the swizzled tile (two 64-dimension
+      // atoms), as f16 times 2^k_r; the row's logit scale becomes
+      // qscale * 2^-k_r.  Rows QV..NQ-1 are zero.  16 lanes per row, 8
+      // elements (one 16-byte chunk) each.
       const uint16_t* qg = static_cast<const uint16_t*>(p.q);
       float* qs = reinterpret_cast<float*>(sm + Sh::OFF_QS);
-      for (int r = lane / 16; r < ((QV + 1) & ~1); r += 2) {
+      for (int r = lane / 16; r < NQ; r += 2) {
         const int c = lane % 16;
         const bool live = r < QV;
         const int i = r / G, h = g * G + r % G;
@@ -251,59 +302,88 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
         int k2 = 0;
         if (mx > 0.f && mx <= 3.402823e38f) k2 = min(max(140 - (int)((__float_as_uint(mx) >> 23) & 0xff), -126), 126);
         const float up = __int_as_float((127 + k2) << 23), down = __int_as_float((127 - k2) << 23);
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
         if (live) {
-          uint4 o;
           o.x = pack2h(v[0] * up, v[1] * up, false);
           o.y = pack2h(v[2] * up, v[3] * up, false);
           o.z = pack2h(v[4] * up, v[5] * up, false);
           o.w = pack2h(v[6] * up, v[7] * up, false);
-          *reinterpret_cast<uint4*>(sm + Sh::OFF_Q + (c >> 3) * Sh::QATOM + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = o;
           if (c == 0) qs[r] = p.qscale * down;
         }
+        *reinterpret_cast<uint4*>(sm + Sh::OFF_Q + (c >> 3) * Sh::QATOM + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = o;
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
     }
-    int nrow0 = entry(lane), nrow1 = entry(lane + 32);   // the next tile's entries, one tile ahead
-    unsigned tma_pend = 0, tma_par = 0;                    // stages with a TMA load issued, and its phase parity
+    // entries lane + 32t of the next two tiles, loaded two tiles ahead
+    int nx[4], nx2[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      nx[t] = entry_raw(lane + 32 * t);
+      nx2[t] = entry_raw(BN + lane + 32 * t);
+    }
+    unsigned tma_pend = 0, tma_par = 0;   // stages with a TMA load issued, and its phase parity
     for (int j = 0; j < T; ++j) {
       const int c = j % NC, u = j / NC;
+      int r[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int e = live(j * BN + lane + 32 * t, nx[t]);
+        r[t] = valid(e) ? e : -1;
+        nx[t] = nx2[t];
+        nx2[t] = entry_raw((j + 2) * BN + lane + 32 * t);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(code_empty + c, (u & 1) ^ 1, abort_flag, wait_ns))) break;
-      const int r0 = valid(nrow0) ? nrow0 : -1, r1 = valid(nrow1) ? nrow1 : -1;
-      nrow0 = entry((j + 1) * BN + lane);
-      nrow1 = entry((j + 1) * BN + lane + 32);
-      unsigned char* Kc = sm + Sh::OFF_C + c * 2 * Sh::CODES;
+      unsigned char* Kc = sm + Sh::OFF_C + c * Sh::STAGE;
       unsigned char* Vc = Kc + Sh::CODES;
-      const int rbase = __shfl_sync(0xffffffffu, r0, 0);
-      const bool contig =
-          kp.tma && __all_sync(0xffffffffu, r0 >= 0 && r0 == rbase + lane && r1 >= 0 && r1 == rbase + 32 + lane);
-      if (contig) {
-        // one 64-row run: a TMA tile load per matrix (x = 0 is 16-byte aligned)
+      // half h holds entries 64h .. 64h + 63 (lane values r[2h], r[2h + 1]);
+      // a half that is one contiguous pool run goes by TMA
+      bool contig[2];
+      int rb[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        rb[h] = __shfl_sync(0xffffffffu, r[2 * h], 0);
+        contig[h] = kp.tma != 0 && __all_sync(0xffffffffu, r[2 * h] >= 0 && r[2 * h] == rb[h] + lane &&
+                                                               r[2 * h + 1] >= 0 && r[2 * h + 1] == rb[h] + 32 + lane);
+      }
+      if (contig[0] || contig[1]) {
         if (lane == 0) {
-          mbar_arrive_expect_tx(code_full + c, 2 * Sh::CODES);
-          tma_load_3d(Kc, &tk, 0, g, rbase, code_full + c);
-          tma_load_3d(Vc, &tv, 0, g, rbase, code_full + c);
-        } else {
-          mbar_arrive(code_full + c);
+          // the bytes the loads will bring, counted before any arrival
+          mbar_expect_tx(code_full + c, (uint32_t)(((contig[0] ? 1 : 0) + (contig[1] ? 1 : 0)) * 2 * HB * CB));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (!contig[h]) continue;
+            tma_load_3d(Kc + h * HB * CB, &tk, 0, g, rb[h], code_full + c);
+            tma_load_3d(Vc + h * HB * CB, &tv, 0, g, rb[h], code_full + c);
+          }
         }
         tma_pend |= 1u << c;
         tma_par = (tma_par & ~(1u << c)) | ((unsigned)(u & 1) << c);
-        continue;
       }
+      if (!(contig[0] && contig[1])) {
 #pragma unroll
-      for (int it = 0; it < BN * Sh::CPR / 32; ++it) {
-        const int f = it * 32 + lane;
-        const int e = f / Sh::CPR, q = f % Sh::CPR;   // e < 32 exactly for the first half of the iterations
-        const int ra = __shfl_sync(0xffffffffu, r0, e & 31);
-        const int rb = __shfl_sync(0xffffffffu, r1, e & 31);
-        const int r = e < 32 ? ra : rb;
-        const bool okr = r >= 0;
-        const size_t go = ((size_t)(okr ? r : 0) * p.Hkv + g) * Sh::CB + q * 16;
-        cp_async16(Kc + e * Sh::CB + q * 16, kb + go, okr);
-        cp_async16(Vc + e * Sh::CB + q * 16, vb + go, okr);
+        for (int h = 0; h < 2; ++h) {
+          if (contig[h]) continue;
+          // 64 rows x CPR chunks over 32 lanes: row e = f / CPR of the half
+#pragma unroll
+          for (int it = 0; it < HB * CPR / 32; ++it) {
+            const int f = it * 32 + lane;
+            const int e = f / CPR, q = f % CPR;   // e < 32 exactly for the first half of the iterations
+            const int ra = __shfl_sync(0xffffffffu, r[2 * h], e & 31);
+            const int rc = __shfl_sync(0xffffffffu, r[2 * h + 1], e & 31);
+            const int row = e < 32 ? ra : rc;
+            const bool okr = row >= 0;
+            const size_t go = ((size_t)(okr ? row : 0) * p.Hkv + g) * CB + q * 16;
+            const uint32_t so = code_off<CB>(h * HB + e, q);
+            cp_async16(Kc + so, kb + go, okr);
+            cp_async16(Vc + so, vb + go, okr);
+          }
+        }
+        cp_async_mbar_arrive_noinc(code_full + c);
+      } else {
+        mbar_arrive(code_full + c);
       }
-      cp_async_mbar_arrive_noinc(code_full + c);
     }
     cp_async_wait_all();
     if (lane == 0 && *abort_flag) {   // no TMA load may still be writing when the CTA exits
@@ -313,350 +393,350 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && T > 0) {
-      // With at most 16 query vectors their S rows fit an M = 64 product
-      // (rows 0-15 land in tensor-memory lanes 0-15); PV stays at M = 128.
-      const uint32_t id_qk = make_idesc_f16(QVP <= 16 ? 64 : 128, BN, bf16, false);
-      const uint32_t id_pv = make_idesc_f16(128, D, bf16, true);
+      // S^T = K Q^T: M = 128 keys (A in tensor memory), N = NQ, K = 128 dims
+      const uint32_t id_qk = make_idesc_f16_ab(128, NQ, false, false, false);
+      // O^T += V^T P^T: M = 128 dims (A = the V buffer read MN-major), N = NQ, K = 16 keys each
+      const uint32_t id_pv = make_idesc_f16_ab(128, NQ, false, true, false);
       // operand descriptors built once; each MMA only adds a constant offset
       const uint64_t dQ = sdesc_sw128(smem_u32(sm + Sh::OFF_Q), 16, 1024);
-      const uint64_t dK = sdesc_sw128(smem_u32(sm + Sh::OFF_B), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_B + Sh::TILE), Sh::KV_ATOM, 1024);
+      const uint64_t dP = sdesc_sw128(smem_u32(sm + Sh::OFF_P), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_V), Sh::VATOM, 1024);
+      const uint32_t tO = tbase + Sh::COL_O;
       bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
-      int nqk = 0, npv = 0;
-      unsigned long long t_idle = 0;
-      while (ok && npv < T) {
-        bool progressed = false;
-        // PV of the oldest tile once its P is written: O_(tile parity) += P V
-        if (npv < nqk && mbar_test_wait(p_full + npv % NS, (npv / NS) & 1)) {
-          const int b = npv % NB, sb = npv % NS;
+      // step j: QK of tile j, then PV of tile j - 1.  The waits block (the
+      // warp sleeps in them) rather than poll, leaving the issue slots of
+      // this scheduler to the softmax and widen warps that share it.  S^T
+      // buffer j % NS was last read by the softmax of tile j - NS, whose P^T
+      // the PV of step j - NS + 1 <= j - 1 has already waited for.
+      for (int j = 0; ok && j <= T; ++j) {
+        if (j < T) {
+          ok = mbar_wait(kt_full + j % NKT, (j / NKT) & 1, abort_flag, wait_ns);
+          if (!ok) break;
           tc_fence_after();
-          const uint64_t vb = sdesc_at(dV, b * 2 * Sh::TILE);
+          const uint32_t ak = tbase + COL_K + (j % NKT) * 64;
+          const uint32_t dS = tbase + COL_S + (j % NS) * NQ;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts(dS, ak + kk * 8, sdesc_at(dQ, (kk >> 2) * Sh::QATOM + (kk & 3) * 32), id_qk, kk > 0);
+          tc_commit(s_full + j % NS);
+          tc_commit(kt_empty + j % NKT);
+        }
+        if (j >= 1) {
+          const int t = j - 1;
+          ok = mbar_wait(p_full + t % NPB, (t / NPB) & 1, abort_flag, wait_ns) &&
+               mbar_wait(vb_full + t % NVB, (t / NVB) & 1, abort_flag, wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t av = sdesc_at(dV, (t % NVB) * Sh::VBUF);
+          const uint64_t bp = sdesc_at(dP, (t % NPB) * Sh::PBUF);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tbase + Sh::COL_O + (npv & 1) * D, tbase + Sh::COL_S + sb * BN + kk * 8, sdesc_at(vb, kk * 2048),
-                   id_pv, npv > 1 || kk > 0);
-          tc_commit(buf_empty + b);
-          tc_commit(o_ready + (npv & 1));
-          ++npv;
-          progressed = true;
-        }
-        // QK of the next tile once its widened K/V are in a buffer and its S
-        // buffer is free (the PV of the tile NS back has been issued)
-        if (nqk < T && nqk < npv + NS && mbar_test_wait(buf_full + nqk % NB, (nqk / NB) & 1)) {
-          const int b = nqk % NB, sb = nqk % NS;
-          tc_fence_after();
-          const uint64_t kbd = sdesc_at(dK, b * 2 * Sh::TILE);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t a_off = (kk >> 2) * Sh::QATOM + (kk & 3) * 32;
-            const uint32_t b_off = (kk >> 2) * Sh::KV_ATOM + (kk & 3) * 32;
-            mma_ss(tbase + Sh::COL_S + sb * BN, sdesc_at(dQ, a_off), sdesc_at(kbd, b_off), id_qk, kk > 0);
-          }
-          tc_commit(s_full + sb);
-          ++nqk;
-          progressed = true;
-        }
-        if (progressed) {
-          t_idle = 0;
-          continue;
-        }
-        if (t_idle == 0) {
-          t_idle = globaltimer();
-        } else if (*abort_flag) {
-          ok = false;
-        } else if (globaltimer() - t_idle > wait_ns) {
-          *abort_flag = 1;
-          ok = false;
+            mma_ss(tO, sdesc_at(av, kk * 2048), sdesc_at(bp, (kk >> 2) * Sh::PATOM + (kk & 3) * 32), id_pv,
+                   t > 0 || kk > 0);
+          tc_commit(vb_empty + t % NVB);
+          tc_commit(p_empty + t % NPB);
+          tc_commit(o_ready);
         }
       }
       tc_commit(drain);
       dq_wait_drain(drain, 0);
     }
-  } else if (warp == W_SMX0 || warp == W_SMX1) {
-    // ------------------------------------------------------------ softmax (tiles of one parity)
-    const int w = warp == W_SMX1 ? 1 : 0;
-    constexpr int LPR = Sh::LPR, CPL = BN / LPR;   // lanes per row, columns per lane
-    const int row = lane / LPR, part = lane % LPR;
-    const bool row_ok = row < QV;
-    const int lim = (p.mask_kind == FA_MASK_CAUSAL) ? n_s - p.Nq + row / G : n_s - 1;
-    float* sS = reinterpret_cast<float*>(sm + Sh::OFF_SM + w * Sh::STAGE_SM);
-    uint32_t* sP = reinterpret_cast<uint32_t*>(sS);             // replaces S once every lane has read it
-    float* scK = sS + QVP * Sh::SROW;                            // [BN] K scales of the current tile
-    bool ok = true;
-    const uint32_t tO = tbase + Sh::COL_O + w * D;
-    // this row's logit scale (written by the gather warp before q_full)
-    float c = 0.f;
-    if (T > w) {
-      if (!__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, wait_ns))) ok = false;
-      c = row_ok ? reinterpret_cast<const float*>(sm + Sh::OFF_QS)[row] : 0.f;
-    }
-    float m_used = NEG_INF, l = 0.f;
-    auto scale_of = [&](const uint16_t* sc, int r) {
-      return valid(r) ? __ldg(sc + ((size_t)(r >> 6) * p.Hkv + g) * kPage + (r & 63)) : (unsigned short)0;
-    };
-    // entries lane, lane + 32 of this warp's current tile and of its next (two tiles on)
-    int cur0 = entry(w * BN + lane), cur1 = entry(w * BN + lane + 32);
-    int nx0 = entry((w + 2) * BN + lane), nx1 = entry((w + 2) * BN + lane + 32);
-    unsigned short sk0 = scale_of(p.k_scale, cur0), sk1 = scale_of(p.k_scale, cur1);
-    int k = 0;
-    for (int j = w; ok && j < T; j += 2, ++k) {
-      unsigned vb[2];
-      vb[0] = __ballot_sync(0xffffffffu, valid(cur0));
-      vb[1] = __ballot_sync(0xffffffffu, valid(cur1));
-      scK[lane] = __half2float(__ushort_as_half(sk0));
-      scK[lane + 32] = __half2float(__ushort_as_half(sk1));
-      sk0 = scale_of(p.k_scale, nx0);
-      sk1 = scale_of(p.k_scale, nx1);
-      cur0 = nx0;
-      cur1 = nx1;
-      nx0 = entry((j + 4) * BN + lane);
-      nx1 = entry((j + 4) * BN + lane + 32);
-      const int jb = j0 + j * BN;   // list position of column 0
-      // this warp's k-th tile is j = w + 2k; it uses S buffer j % NS
-      const int sb = j % NS;
-      const uint32_t tS = tbase + Sh::COL_S + sb * BN;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (j / NS) & 1, abort_flag, wait_ns)))) break;
+  } else if (warp >= W_K0 && warp < W_K0 + 4) {
+    // ------------------------------------------------------------ K widen: one thread per key
+    const int k = (warp - W_K0) * 32 + lane;   // tensor-memory lane = key within the tile
+    const uint32_t lane_sel = (uint32_t)((warp - W_K0) * 32) << 16;
+    for (int j = 0; j < T; ++j) {
+      const int c = j % NC, u = j / NC, kt = j % NKT;
+      if (!__all_sync(0xffffffffu, mbar_wait(code_full + c, u & 1, abort_flag, wait_ns))) break;
+      const unsigned char* Kc = sm + Sh::OFF_C + c * Sh::STAGE;
+      // dimensions 0..63, then 64..127: half the row's codes and 32 f16 pairs
+      // in registers at a time
+      constexpr int HC = CPR / 2;
+      uint4 ca[HC], cb[HC];
+#pragma unroll
+      for (int ch = 0; ch < HC; ++ch) {
+        ca[ch] = *reinterpret_cast<const uint4*>(Kc + code_off<CB>(k, ch));
+        cb[ch] = *reinterpret_cast<const uint4*>(Kc + code_off<CB>(k, HC + ch));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(code_empty + c);   // the codes are in registers
+      if (!__all_sync(0xffffffffu, mbar_wait(kt_empty + kt, ((j / NKT) & 1) ^ 1, abort_flag, wait_ns))) break;
       tc_fence_after();
       {
-        uint32_t sr[2][32];
-        tmem_ld32_nowait(tS, sr[0]);
-        tmem_ld32_nowait(tS + 32, sr[1]);
-        tmem_wait_ld_tied(sr[0]);
-        tmem_wait_ld_tied(sr[1]);
-        if (lane < QV) {
-          float2* dst = reinterpret_cast<float2*>(sS + lane * Sh::SSTR);
+        uint32_t w[32];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) dst[q] = make_float2(__uint_as_float(sr[0][2 * q]), __uint_as_float(sr[0][2 * q + 1]));
-#pragma unroll
-          for (int q = 0; q < 16; ++q)
-            dst[16 + q] = make_float2(__uint_as_float(sr[1][2 * q]), __uint_as_float(sr[1][2 * q + 1]));
-        }
+        for (int ch = 0; ch < HC; ++ch) widen_chunk<KQ>(ca[ch], w + ch * Sh::WPC);
+        tmem_st32_nowait(tbase + lane_sel + COL_K + kt * 64, w);
       }
-      __syncwarp();
-      // column pairs 2*(part + LPR*kk) of row `row`: logits in log2 units, masked
-      const unsigned long long vbits = ((unsigned long long)vb[1] << 32) | vb[0];
-      float x[CPL];
-      float mx = NEG_INF;
-#pragma unroll
-      for (int kk = 0; kk < CPL / 2; ++kk) {
-        const int col = 2 * (part + LPR * kk);
-        const float2 sv = *reinterpret_cast<const float2*>(sS + row * Sh::SSTR + col);
-        const float2 sk = *reinterpret_cast<const float2*>(scK + col);
-        float v0 = sv.x * (c * sk.x), v1 = sv.y * (c * sk.y);
-        if (!(row_ok && ((vbits >> col) & 1ull) && (jb + col <= lim))) v0 = NEG_INF;
-        if (!(row_ok && ((vbits >> (col + 1)) & 1ull) && (jb + col + 1 <= lim))) v1 = NEG_INF;
-        x[2 * kk] = v0;
-        x[2 * kk + 1] = v1;
-        mx = fmaxf(mx, fmaxf(v0, v1));
-      }
-#pragma unroll
-      for (int sh = 1; sh < LPR; sh <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-      const float m_new = fmaxf(m_used, mx);
-      const bool need = row_ok && m_new > m_used + 8.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? fast_ex2(m_used - m_new) : 1.f;
-        if (need) {
-          l *= alpha;
-          m_used = m_new;
-        }
-        if (k > 0) {
-          // wait for the PV of this stream's previous tile (the one before it
-          // is implied by the S wait: it was issued before this tile's QK)
-          const float a_r = __shfl_sync(0xffffffffu, alpha, (lane % QVP) * LPR);
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready + w, (k - 1) & 1, abort_flag, wait_ns)))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t o[32];
-            tmem_ld32(tO + c4 * 32, o);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * a_r);
-            tmem_st32(tO + c4 * 32, o);
-          }
-        }
-      }
-      const float mu = (m_used == NEG_INF) ? 0.f : m_used;
-      float sum = 0.f;
-      __syncwarp();   // every lane's S reads are done before P overwrites them
-#pragma unroll
-      for (int kk = 0; kk < CPL / 2; ++kk) {
-        const int pp = part + LPR * kk;   // column pair
-        const float p0 = fast_ex2(x[2 * kk] - mu), p1 = fast_ex2(x[2 * kk + 1] - mu);
-        sum += p0 + p1;
-        if (row_ok) sP[row * Sh::SPP + pp] = pack2h(p0, p1, false);
-      }
-#pragma unroll
-      for (int sh = 1; sh < LPR; sh <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
-      l += sum;
-      __syncwarp();
       {
-        uint32_t pk[32];
-        if (lane < QV) {
-          const uint32_t* src = sP + lane * Sh::SPP;
-          if constexpr (Sh::SPP % 4 == 0) {
+        uint32_t w[32];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint4 w4 = reinterpret_cast<const uint4*>(src)[q];
-              pk[4 * q] = w4.x; pk[4 * q + 1] = w4.y; pk[4 * q + 2] = w4.z; pk[4 * q + 3] = w4.w;
-            }
-          } else if constexpr (Sh::SPP % 2 == 0) {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const uint2 w2 = reinterpret_cast<const uint2*>(src)[q];
-              pk[2 * q] = w2.x; pk[2 * q + 1] = w2.y;
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) pk[q] = src[q];
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) pk[q] = 0u;
-        }
-        tmem_st32_nowait(tS, pk);
+        for (int ch = 0; ch < HC; ++ch) widen_chunk<KQ>(cb[ch], w + ch * Sh::WPC);
+        tmem_st32_nowait(tbase + lane_sel + COL_K + kt * 64 + 32, w);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full + sb);
+      if (lane == 0) mbar_arrive(kt_full + kt);
     }
-    // ---- merge the two streams and write this split's result; warp w
-    // writes O columns [64w, 64w + 64)
-    const float m_r = __shfl_sync(0xffffffffu, m_used, (lane % QVP) * LPR);
-    const float l_r = __shfl_sync(0xffffffffu, l, (lane % QVP) * LPR);
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag, wait_ns));
-    float2* X = reinterpret_cast<float2*>(sm + Sh::OFF_X);
-    if (lane < QROWS) X[w * QROWS + lane] = make_float2(m_r, l_r);
-    named_barrier(1, 64);   // both softmax warps, always reached exactly once
-    tc_fence_after();
-    if (ok && !*abort_flag) {
-      const int r = lane;
-      const bool own = r < QV;
-      const float2 a = X[r], b2 = X[QROWS + r];
-      const float M = fmaxf(a.x, b2.x);
-      const float wa = (a.x == NEG_INF) ? 0.f : fast_ex2(a.x - M);
-      const float wb = (b2.x == NEG_INF) ? 0.f : fast_ex2(b2.x - M);
-      const float L = a.y * wa + b2.y * wb;
-      const int i = r / G, h = g * G + r % G;
-      const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
-      const size_t pi = (unit * p.nsplit + split) * QV + r;
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int col = w * (D / 2) + cc * 32;
-        uint32_t oa[32], ob[32];
-        if (T > 0) tmem_ld32(tbase + Sh::COL_O + col, oa);
-        if (T > 1) tmem_ld32(tbase + Sh::COL_O + D + col, ob);
-        float acc[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          float v = 0.f;
-          if (T > 0 && wa != 0.f) v = __uint_as_float(oa[q]) * wa;
-          if (T > 1 && wb != 0.f) v += __uint_as_float(ob[q]) * wb;
-          acc[q] = v;
-        }
-        if (!own) continue;
-        if (p.nsplit == 1) {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) store_out(p.out, oi * D + col + q, acc[q] * inv, p.out_dtype);
-        } else if (M != NEG_INF) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + pi * D + col);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-        }
-      }
-      if (own && w == 0) {
-        if (p.nsplit == 1) {
-          if (p.lse) p.lse[oi] = L > 0.f ? (M + __log2f(L)) * kLn2 : NEG_INF;
-        } else {
-          p.part_ml[pi * 2] = M;
-          p.part_ml[pi * 2 + 1] = L;
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ widen (16 rows each)
-    const int slot = widen_slot(warp);
-    const int grp = slot >> 2, cv = slot & 3;   // this warp widens rows 16*cv.. of tiles grp, grp + 2, ...
-    constexpr int NIT = 16 * Sh::CPR / 32;
-    // V scales of this warp's 16 rows (lane t < 16: row 16*cv + t): each
-    // scale is loaded two of this group's tiles before its use, from an entry
-    // loaded two tiles before that, so neither load's latency lands on a tile
-    auto ventry = [&](int jj) { return lane < 16 ? entry(jj * BN + cv * 16 + lane) : -1; };
-    auto vscale = [&](int r) {
-      return valid(r) ? __ldg(p.v_scale + ((size_t)(r >> 6) * p.Hkv + g) * kPage + (r & 63)) : (unsigned short)0;
-    };
-    unsigned short sv0 = vscale(ventry(grp)), sv1 = vscale(ventry(grp + 2));   // tiles j, j + 2
-    int re2 = ventry(grp + 4), re3 = ventry(grp + 6);                           // entries of tiles j + 4, j + 6
-    for (int j = grp; j < T; j += 2) {
-      const unsigned short sv_here = sv0;
-      sv0 = sv1;
-      sv1 = vscale(re2);
-      re2 = re3;
-      re3 = ventry(j + 8);
-      const int c = j % NC, u = j / NC, b = j % NB, ub = j / NB;
+  } else if (warp >= W_V0) {
+    // ------------------------------------------------------------ V widen: one thread per key
+    const int k = (warp - W_V0) * 32 + lane;
+    for (int j = 0; j < T; ++j) {
+      const int c = j % NC, u = j / NC, b = j % NVB;
       if (!__all_sync(0xffffffffu, mbar_wait(code_full + c, u & 1, abort_flag, wait_ns))) break;
-      const unsigned char* Kc = sm + Sh::OFF_C + c * 2 * Sh::CODES;
-      const unsigned char* Vc = Kc + Sh::CODES;
-      uint4 ck[NIT], cvv[NIT];
+      const unsigned char* Vc = sm + Sh::OFF_C + c * Sh::STAGE + Sh::CODES;
+      constexpr int HC = CPR / 2;
+      uint4 ca[HC], cb[HC];
 #pragma unroll
-      for (int it = 0; it < NIT; ++it) {
-        const int f = it * 32 + lane;
-        const int e = cv * 16 + f / Sh::CPR, q = f % Sh::CPR;
-        ck[it] = *reinterpret_cast<const uint4*>(Kc + e * Sh::CB + q * 16);
-        cvv[it] = *reinterpret_cast<const uint4*>(Vc + e * Sh::CB + q * 16);
+      for (int ch = 0; ch < HC; ++ch) {
+        ca[ch] = *reinterpret_cast<const uint4*>(Vc + code_off<CB>(k, ch));
+        cb[ch] = *reinterpret_cast<const uint4*>(Vc + code_off<CB>(k, HC + ch));
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(code_empty + c);   // the codes are in registers
-      if (!__all_sync(0xffffffffu, mbar_wait(buf_empty + b, (ub & 1) ^ 1, abort_flag, wait_ns))) break;
-      unsigned char* Kb = sm + Sh::OFF_B + b * 2 * Sh::TILE;
+      if (lane == 0) mbar_arrive(code_empty + c);
+      if (!__all_sync(0xffffffffu, mbar_wait(vb_empty + b, ((j / NVB) & 1) ^ 1, abort_flag, wait_ns))) break;
+      // row k of the buffer: dimensions 8t..8t+7 (words 4t..4t+3) in 16-byte
+      // chunk t % 8 of atom t / 8, swizzled by the row; atom a holds
+      // dimensions 64a..64a+63, widened from half a of the codes
+      unsigned char* Vb = sm + Sh::OFF_V + b * Sh::VBUF;
 #pragma unroll
-      for (int mat = 0; mat < 2; ++mat) {
-        unsigned char* tile = Kb + mat * Sh::TILE;
+      for (int a = 0; a < 2; ++a) {
+        uint32_t w[32];
 #pragma unroll
-        for (int it = 0; it < NIT; ++it) {
-          const int f = it * 32 + lane;
-          const int e = cv * 16 + f / Sh::CPR, q = f % Sh::CPR;
-          const uint4 cw = mat ? cvv[it] : ck[it];
-          // V: each value times its row's scale, rounded once to f16
-          const unsigned short svr = (unsigned short)__shfl_sync(0xffffffffu, (int)sv_here, f / Sh::CPR);
-          const __half2 sv2 = __halves2half2(__ushort_as_half(svr), __ushort_as_half(svr));
-          auto vs = [&](uint32_t h2) {
-            if (!mat) return h2;
-            __half2 x2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), sv2);
-            return *reinterpret_cast<uint32_t*>(&x2);
-          };
-          if constexpr (KQ == 1 || KQ == 3) {
-            // 16 codes = columns 16q .. 16q+15: two 16-byte chunks of atom q / 4
-            uint2 a, b1, c2, d;
-            if constexpr (KQ == 1) {
-              a = widen_i8x4(cw.x, bf16), b1 = widen_i8x4(cw.y, bf16);
-              c2 = widen_i8x4(cw.z, bf16), d = widen_i8x4(cw.w, bf16);
-            } else {
-              a = widen_e4m3x4(cw.x), b1 = widen_e4m3x4(cw.y), c2 = widen_e4m3x4(cw.z), d = widen_e4m3x4(cw.w);
-            }
-            unsigned char* rowp = tile + (q / 4) * Sh::KV_ATOM + e * 128;
-            const int k0 = 2 * (q % 4);
-            *reinterpret_cast<uint4*>(rowp + ((k0 ^ (e & 7)) << 4)) = make_uint4(vs(a.x), vs(a.y), vs(b1.x), vs(b1.y));
-            *reinterpret_cast<uint4*>(rowp + (((k0 + 1) ^ (e & 7)) << 4)) =
-                make_uint4(vs(c2.x), vs(c2.y), vs(d.x), vs(d.y));
-          } else {
-            // 32 codes = columns 32q .. 32q+31: four 16-byte chunks of atom q / 2
-            unsigned char* rowp = tile + (q / 2) * Sh::KV_ATOM + e * 128;
-            const int k0 = 4 * (q % 2);
-            const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
+        for (int ch = 0; ch < HC; ++ch) widen_chunk<KQ>(a ? cb[ch] : ca[ch], w + ch * Sh::WPC);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const uint4 h = widen_i4x8(wv[t], bf16);
-              *reinterpret_cast<uint4*>(rowp + (((k0 + t) ^ (e & 7)) << 4)) = make_uint4(vs(h.x), vs(h.y), vs(h.z), vs(h.w));
-            }
-          }
-        }
+        for (int t = 0; t < 8; ++t)
+          *reinterpret_cast<uint4*>(Vb + a * Sh::VATOM + k * 128 + ((t ^ (k & 7)) << 4)) =
+              make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(buf_full + b);
+      if (lane == 0) mbar_arrive(vb_full + b);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax, one thread per key
+    const int k = warp * 32 + lane;
+    const uint32_t lane_sel = (uint32_t)(warp * 32) << 16;
+    int* flags = reinterpret_cast<int*>(sm + Sh::OFF_FLAG);   // [2][4]
+    float* red = reinterpret_cast<float*>(sm + Sh::OFF_RED);  // [4][QROWS] tile maxima
+    // [4][QROWS] row sums: their own slots, since a warp that has left the
+    // loop may write them while another still reads its last tile's maxima
+    float* rsum = reinterpret_cast<float*>(sm + Sh::OFF_SUM);
+    const float* qs = reinterpret_cast<const float*>(sm + Sh::OFF_QS);
+    const bool causal = p.mask_kind == FA_MASK_CAUSAL;
+    bool ok = true;
+    uint32_t ph = 0;   // completed phases of the agreement barrier
+    auto agree_wait = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(agree);
+      const bool r = __all_sync(0xffffffffu, mbar_wait(agree, ph & 1, abort_flag, wait_ns));
+      ++ph;
+      return r;
+    };
+    // Two lazy references per query vector: ml for the row sum l = sum of
+    // 2^(x - ml), and mo for the weights that go into O^T, 2^(x + log2|s_v| - mo)
+    // * sign(s_v), so that every weight sits below 2^8 in magnitude and the
+    // largest ones near the top of the f16 range whatever the V scales are.
+    // cw = 2^(ml - mo) turns a row-sum term into an O weight: w = p * s_v * cw.
+    // The three are the same for every thread and live in shared memory,
+    // two copies that alternate at each move; l is this thread's partial sum.
+    // (copy 0 starts at -inf, -inf, 0: set before the CTA's first barrier)
+    float* refs = reinterpret_cast<float*>(sm + Sh::OFF_REF);   // [2][3][QROWS]
+    int rp = 0;                                                  // current copy
+    float l[QVP];
+#pragma unroll
+    for (int q = 0; q < QVP; ++q) l[q] = 0.f;
+    // the logit scales qs[] are read from shared memory once q_full has completed
+    if (T > 0 && !__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, wait_ns))) ok = false;
+    // this key's list entries three tiles ahead and its raw fp16 scales two
+    // tiles ahead; a scale is read at row 0 for a dead entry and zeroed at use
+    auto scale_raw = [&](const uint16_t* sc, int r) {
+      const int rr = valid(r) ? r : 0;
+      return __ldg(sc + ((size_t)(rr >> 6) * p.Hkv + g) * kPage + (rr & 63));
+    };
+    const bool has_rows = p.R > 0;
+    int e1 = entry_raw(k), e2 = entry_raw(BN + k), e3 = entry_raw(2 * BN + k);
+    int r1 = live(k, e1), r2 = live(BN + k, e2);
+    uint16_t hk1 = 0, hv1 = 0, hk2 = 0, hv2 = 0;
+    if (has_rows) {
+      hk1 = scale_raw(p.k_scale, r1);
+      hv1 = scale_raw(p.v_scale, r1);
+      hk2 = scale_raw(p.k_scale, r2);
+      hv2 = scale_raw(p.v_scale, r2);
+    }
+    for (int j = 0; ok && j < T; ++j) {
+      const int r = valid(r1) ? r1 : -1;
+      const float sk = r >= 0 ? __half2float(__ushort_as_half(hk1)) : 0.f;
+      const float sv = r >= 0 ? __half2float(__ushort_as_half(hv1)) : 0.f;
+      r1 = r2;
+      hk1 = hk2;
+      hv1 = hv2;
+      r2 = live((j + 2) * BN + k, e3);   // loaded an iteration ago
+      e3 = entry_raw((j + 3) * BN + k);
+      if (has_rows) {
+        hk2 = scale_raw(p.k_scale, r2);
+        hv2 = scale_raw(p.v_scale, r2);
+      }
+      const float lsv = __log2f(fabsf(sv));   // -inf for a zero scale
+      const int pos = j0 + j * BN + k;   // list position of this key
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + j % NS, (j / NS) & 1, abort_flag, wait_ns)))) break;
+      tc_fence_after();
+      uint32_t sr[32];
+      if constexpr (NQ == 16) {
+        tmem_ld16(tbase + lane_sel + COL_S + (j % NS) * NQ, *reinterpret_cast<uint32_t(*)[16]>(sr));
+      } else {
+        tmem_ld32(tbase + lane_sel + COL_S + (j % NS) * NQ, sr);
+      }
+      // logits in log2 units with the K scale folded in; masked: -inf
+      float x[QVP];
+      bool exceed = false;
+      const float* ml = refs + rp * 3 * QROWS;
+      const float* mo = ml + QROWS;
+#pragma unroll
+      for (int q = 0; q < QVP; ++q) {
+        const int lim = causal ? n_s - p.Nq + q / G : n_s - 1;
+        const bool vis = q < QV && valid(r) && pos <= lim;
+        x[q] = vis ? __uint_as_float(sr[q]) * (qs[q] * sk) : NEG_INF;
+        exceed = exceed || (x[q] > ml[q] + 8.f) || (x[q] + lsv > mo[q] + 8.f);
+      }
+      // do the four warps agree that no reference has to move?
+      const bool wex = __any_sync(0xffffffffu, exceed);
+      if (lane == 0) flags[(j & 1) * 4 + warp] = wex ? 1 : 0;
+      if (!(ok = agree_wait())) break;
+      const int* fl = flags + (j & 1) * 4;
+      if (fl[0] | fl[1] | fl[2] | fl[3]) {
+        // rare: each query vector's maxima over the tile's keys
+#pragma unroll
+        for (int q = 0; q < QVP; ++q) {
+          float v = x[q], vo = x[q] + lsv;
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) {
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            vo = fmaxf(vo, __shfl_xor_sync(0xffffffffu, vo, o));
+          }
+          if (lane == 0) {
+            red[warp * QROWS + q] = v;
+            red[(4 + warp) * QROWS + q] = vo;
+          }
+        }
+        if (!(ok = agree_wait())) break;
+        // new references into the other copy (warp 0, a lane per query
+        // vector); each thread scales its own partial sums and keeps the O^T
+        // factors
+        float* nref = refs + (rp ^ 1) * 3 * QROWS;
+        float alpha[QVP];
+        bool any_scale = false;
+#pragma unroll
+        for (int q = 0; q < QVP; ++q) {
+          const float* rl = red + q;
+          const float* ro = red + 4 * QROWS + q;
+          const float mt = fmaxf(fmaxf(rl[0], rl[QROWS]), fmaxf(rl[2 * QROWS], rl[3 * QROWS]));
+          const float mto = fmaxf(fmaxf(ro[0], ro[QROWS]), fmaxf(ro[2 * QROWS], ro[3 * QROWS]));
+          float nl = ml[q], no = mo[q];
+          if (mt > nl + 8.f) {
+            l[q] *= nl == NEG_INF ? 0.f : fast_ex2(nl - mt);
+            nl = mt;
+          }
+          alpha[q] = 1.f;
+          if (mto > no + 8.f) {
+            alpha[q] = no == NEG_INF ? 0.f : fast_ex2(no - mto);
+            no = mto;
+            any_scale = true;
+          }
+          if (warp == 0 && lane == q) {
+            nref[q] = nl;
+            nref[QROWS + q] = no;
+            nref[2 * QROWS + q] = no == NEG_INF || nl == NEG_INF ? 0.f : fast_ex2(nl - no);
+          }
+        }
+        // the new copy is complete, and every thread has read the reductions
+        // and the old copy, before any thread goes on
+        if (!(ok = agree_wait())) break;
+        rp ^= 1;
+        if (any_scale && j > 0) {
+          // O^T (this thread's lane = head dimension k) times alpha per query
+          // vector, once the PV of the previous tile has completed
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (j - 1) & 1, abort_flag, wait_ns)))) break;
+          tc_fence_after();
+          uint32_t o[32];
+          if constexpr (NQ == 16) {
+            tmem_ld16(tbase + lane_sel + Sh::COL_O, *reinterpret_cast<uint32_t(*)[16]>(o));
+          } else {
+            tmem_ld32(tbase + lane_sel + Sh::COL_O, o);
+          }
+#pragma unroll
+          for (int q = 0; q < QVP; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha[q]);
+          if constexpr (NQ == 16) {
+            tmem_st16(tbase + lane_sel + Sh::COL_O, *reinterpret_cast<uint32_t(*)[16]>(o));
+          } else {
+            tmem_st32(tbase + lane_sel + Sh::COL_O, o);
+          }
+        }
+      }
+      // P^T row q, key k: the O weight as f16, once the PV that last read this
+      // buffer has completed
+      const int pb = j % NPB;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_empty + pb, ((j / NPB) & 1) ^ 1, abort_flag, wait_ns)))) break;
+      unsigned char* Pb = sm + Sh::OFF_P + pb * Sh::PBUF + (k >> 6) * Sh::PATOM + (k & 7) * 2;
+      const float* mlc = refs + rp * 3 * QROWS;
+      const float* cw = mlc + 2 * QROWS;
+#pragma unroll
+      for (int q = 0; q < QVP; ++q) {
+        const float pq = x[q] == NEG_INF ? 0.f : fast_ex2(x[q] - mlc[q]);
+        l[q] += pq;
+        if (q < QV)
+          *reinterpret_cast<__half*>(Pb + q * 128 + ((((k & 63) >> 3) ^ (q & 7)) << 4)) =
+              __float2half_rn(pq * (sv * cw[q]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full + pb);
+    }
+    // ---- the row sums over all keys, then O^T normalised: this thread's
+    // lane is now head dimension k
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag, wait_ns));
+#pragma unroll
+    for (int q = 0; q < QVP; ++q) {
+      float v = l[q];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) rsum[warp * QROWS + q] = v;
+    }
+    if (ok) ok = agree_wait();
+    tc_fence_after();
+    const float* ml = refs + rp * 3 * QROWS;
+    const float* mo = ml + QROWS;
+    if (ok && !*abort_flag) {
+      uint32_t o[32];
+      if (T > 0) {
+        if constexpr (NQ == 16) {
+          tmem_ld16(tbase + lane_sel + Sh::COL_O, *reinterpret_cast<uint32_t(*)[16]>(o));
+        } else {
+          tmem_ld32(tbase + lane_sel + Sh::COL_O, o);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < QVP; ++q) {
+        if (q >= QV) continue;
+        const float L = rsum[q] + rsum[QROWS + q] + rsum[2 * QROWS + q] + rsum[3 * QROWS + q];
+        // O^T holds the sum of 2^(x - mo) s_v v; relative to ml that is times 2^(mo - ml)
+        const float ov = T > 0 && mo[q] != NEG_INF && ml[q] != NEG_INF ? __uint_as_float(o[q]) * exp2f(mo[q] - ml[q]) : 0.f;
+        const int i = q / G, h = g * G + q % G;
+        const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
+        const size_t pi = (unit * p.nsplit + split) * QV + q;
+        if (p.nsplit == 1) {
+          store_out(p.out, oi * D + k, L > 0.f ? ov / L : 0.f, p.out_dtype);
+          if (k == 0 && p.lse) p.lse[oi] = L > 0.f ? (ml[q] + __log2f(L)) * kLn2 : NEG_INF;
+        } else {
+          if (ml[q] != NEG_INF) p.part_o[pi * D + k] = ov;
+          if (k == 0) {
+            p.part_ml[pi * 2] = ml[q];
+            p.part_ml[pi * 2 + 1] = L;
+          }
+        }
+      }
     }
   }
 
@@ -665,7 +745,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   if (warp == W_MMA) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tbase, Sh::TMEM_COLS);
+    tmem_dealloc(tbase, TMEM_COLS);
   }
   // An expired wait marks the workspace status word; the CTA still arrives
   // on its split counter (marked as aborted) so the counter ends at zero.
@@ -680,7 +760,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   __syncthreads();
   if (!*am_last) return;
   __threadfence();
-  merge_splits<D>(p, unit, QV, QV, s, g, reinterpret_cast<float*>(sm + Sh::OFF_B));
+  merge_splits<D>(p, unit, QV, QV, s, g, reinterpret_cast<float*>(sm + Sh::OFF_C));
   if (threadIdx.x == 0) p.counters[unit] = 0u;
 }
 
@@ -690,27 +770,30 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
 namespace {
 
 // Code pool [R][Hkv][CB bytes] as a 3-D byte tensor; box = CB bytes x one
-// head x 64 rows, unswizzled (the widen warps read it row-major).
+// head x 64 rows, 128-byte swizzled for 128-byte rows (the widen threads each
+// read a row), plain for INT4's 64-byte rows.
 bool dq_map(CUtensorMap* m, const void* base, int CB, int Hkv, long long R) {
   const cuuint64_t dims[3] = {(cuuint64_t)CB, (cuuint64_t)Hkv, (cuuint64_t)R};
   const cuuint64_t strides[2] = {(cuuint64_t)CB, (cuuint64_t)CB * Hkv};
-  const cuuint32_t box[3] = {(cuuint32_t)CB, 1, (cuuint32_t)dq::BN};
-  return tmap_encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  const cuuint32_t box[3] = {(cuuint32_t)CB, 1, (cuuint32_t)dq::HB};
+  return tmap_encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box,
+                        CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <int QVP, int KQ>
 int dq_occupancy() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev] > 0) return cached[dev];
+  const int c = cached[dev].load(std::memory_order_relaxed);
+  if (c > 0) return c;
   using Sh = DqShape<QVP, KQ>;
   auto kern = fa_rows_decode_tcq_kernel<QVP, KQ>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, dq::NWARP * 32, Sh::SMEM) != cudaSuccess) return 0;
   n = n < 1 ? n : 1;   // 512 tensor-memory columns: one CTA per SM
-  cached[dev] = n;
+  if (n > 0) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -724,7 +807,7 @@ cudaError_t dq_launch(const DecodeParams& a, unsigned int* err, cudaStream_t st)
   CUtensorMap tk, tv;
   memset(&tk, 0, sizeof(tk));
   memset(&tv, 0, sizeof(tv));
-  kp.tma = a.R >= dq::BN && dq_map(&tk, a.k, Sh::CB, a.Hkv, a.R) && dq_map(&tv, a.v, Sh::CB, a.Hkv, a.R);
+  kp.tma = a.R >= dq::HB && dq_map(&tk, a.k, Sh::CB, a.Hkv, a.R) && dq_map(&tv, a.v, Sh::CB, a.Hkv, a.R);
   dim3 grid(a.nsplit, a.Hkv, a.S);
   fa_rows_decode_tcq_kernel<QVP, KQ><<<grid, dq::NWARP * 32, Sh::SMEM, st>>>(kp, tk, tv);
   return cudaGetLastError();
@@ -772,6 +855,8 @@ int decode_tcq_occupancy(int kind, int qv) {
   if (kind == KV_F8) return dq_occupancy_q<3>(dq_pow2(qv));
   return dq_occupancy_q<1>(dq_pow2(qv));
 }
+
+int decode_tcq_tile() { return dq::BN; }
 
 cudaError_t decode_tcq_launch(const DecodeParams& a, int kind, unsigned int* err, cudaStream_t st) {
   if (kind == KV_I4) return dq_launch_q<2>(dq_pow2(a.QV), a, err, st);

@@ -87,6 +87,7 @@ cudaError_t decode_tc_launch(const DecodeParams& p, int D, int kind, unsigned in
 // D 128: one CTA per SM with a deep code ring.  Same workspace as above.
 bool decode_tcq_supported(int D, int kind, int qv, int mask_kind);
 int decode_tcq_occupancy(int kind, int qv);
+int decode_tcq_tile();
 cudaError_t decode_tcq_launch(const DecodeParams& p, int kind, unsigned int* err, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
