@@ -129,7 +129,7 @@ template <int D, int QVP, int KQ, int NS>
 __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char* sm, uint64_t* s_full, uint64_t* p_full,
                                            uint64_t* o_ready, uint64_t* o_done, volatile int* abort_flag,
                                            uint32_t tbase, int T, int cnt, int j0, int n_s, const int32_t* rows_g,
-                                           size_t unit, int split, int s, int g) {
+                                           size_t unit, int split, int s, int g, bool single) {
   using Sh = DkShape<D, QVP, KQ, NS>;
   using namespace dk;
   const float NEG_INF = __int_as_float(0xff800000);
@@ -355,7 +355,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
           for (int k = 0; k < 32; ++k) o[k] = 0u;
         }
         if (!own) continue;
-        if (p.nsplit == 1) {
+        if (single) {
 #pragma unroll
           for (int k = 0; k < 32; ++k) store_out(p.out, oi * D + c4 * 32 + k, __uint_as_float(o[k]) * inv, p.out_dtype);
         } else if (m_r != NEG_INF) {
@@ -368,7 +368,7 @@ __device__ __forceinline__ void dk_softmax(const DecodeParams& p, unsigned char*
         }
       }
       if (own) {
-        if (p.nsplit == 1) {
+        if (single) {
           if (p.lse) p.lse[oi] = l_r > 0.f ? (m_r + __log2f(l_r)) * kLn2 : NEG_INF;
         } else {
           p.part_ml[pi * 2] = m_r;
@@ -411,6 +411,10 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   const bool bf16 = p.q_bf16 != 0;
   int n_s = p.L;
   if (p.kv_len) n_s = min(max(__ldg(p.kv_len + s), 0), p.L);
+  // splits past the sequence's last entry do nothing and are not merged; a
+  // sequence that fits one split writes its result directly
+  const int ns_unit = n_s > 0 && p.chunk > 0 ? (n_s + p.chunk - 1) / p.chunk : 1;
+  if (split >= ns_unit) return;
   const int j0 = split * p.chunk;
   const int cnt = max(min(j0 + p.chunk, n_s) - j0, 0);
   const int T = (cnt + BN - 1) / BN;
@@ -697,7 +701,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   } else {
     // ------------------------------------------------------------ softmax (warp 0)
     dk_softmax<D, QVP, KQ, NS>(p, sm, s_full, p_full, o_ready, drain, abort_flag, tbase, T, cnt, j0, n_s, rows_g, unit,
-                           split, s, g);
+                           split, s, g, ns_unit == 1);
   }
 
   tc_fence_before();
@@ -711,16 +715,16 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   // on its split counter (marked as aborted) so the counter ends at zero.
   const bool aborted = *abort_flag != 0;
   if (aborted && threadIdx.x == 0 && kp.err) atomicOr(kp.err, FA_WS_WAIT_EXPIRED);
-  if (p.nsplit == 1) return;
+  if (ns_unit == 1) return;
 
   // ---- cross-split merge by the last CTA of this (slice, KV head)
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *am_last = split_arrive_last(p.counters + unit, p.nsplit, aborted);
+  if (threadIdx.x == 0) *am_last = split_arrive_last(p.counters + unit, ns_unit, aborted);
   __syncthreads();
   if (!*am_last) return;
   __threadfence();
-  merge_splits<D>(p, unit, QV, QV, s, g, reinterpret_cast<float*>(sm + Sh::OFF_K));
+  merge_splits<D>(p, unit, QV, QV, s, g, reinterpret_cast<float*>(sm + Sh::OFF_K), ns_unit);
   if (threadIdx.x == 0) p.counters[unit] = 0u;
 }
 

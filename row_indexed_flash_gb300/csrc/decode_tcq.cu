@@ -21,26 +21,33 @@
 //                    times a power of two that puts its largest element in
 //                    [2^13, 2^14) (exact for every element within 2^-29 of the
 //                    largest), taken back out of its logit scale.
-//   K warps (4)      one thread per key: its codes widened exactly to f16 and
-//                    stored into a K tile in tensor memory (lane = key).
-//   V warps (4)      one thread per key: its codes widened exactly to f16 into
-//                    a V buffer in shared memory (rows = keys).
+//   widen warps (4)  one thread per key: its K codes widened exactly to f16
+//                    into a K tile in tensor memory (lane = key).
 //   MMA warp         S^T = K Q^T (A = the K tile in tensor memory, B = Q^T),
-//                    then O^T += V^T P^T (A = the V buffer read MN-major, B =
-//                    P^T in shared memory); O^T holds a lane per head
+//                    then O^T += V^T P^T (A = the V tile read MN-major, B =
+//                    P^T in shared memory) into the O^T accumulator of the
+//                    tile's softmax group; O^T holds a lane per head
 //                    dimension and a column per query vector.
-//   softmax (4)      one thread per key: its logits (the K scale folded in),
+//   softmax (2 x 4)  two groups of four warps take alternate tiles, each with
+//                    its own references, row sums and O^T, so that one
+//                    group's barriers and waits overlap the other's work; one
+//                    thread per key.  Each tile starts with its V codes,
+//                    widened exactly to f16 in place: the f16 V tile (rows =
+//                    keys) takes the whole code stage once the widen warps
+//                    hold its K codes, and the stage is released when the PV
+//                    that reads it completes.  Then the key's logits (the K
+//                    scale folded in),
 //                    P = exp2(logit - m) against a reference max m per query
 //                    vector that moves only when a logit exceeds it by more
 //                    than 2^8 -- detected by each thread and agreed across the
-//                    four warps at one bounded barrier per tile, followed only
-//                    in that rare case by a maximum over the tile's keys and a
-//                    rescale of O^T -- then the O weight P * s_v as f16 into
-//                    P^T, kept below 2^8 by a second lazy reference of the
-//                    same kind over logit + log2|s_v|.
-//                    Each thread keeps partial row sums; they are added at the
-//                    end, when the same warps (now one thread per head
-//                    dimension) normalise O^T.
+//                    group's four warps at one bounded barrier per tile,
+//                    followed only in that rare case by a maximum over the
+//                    tile's keys and a rescale of the group's O^T -- then the
+//                    O weight P * s_v as f16 into P^T, kept below 2^8 by a
+//                    second lazy reference of the same kind over
+//                    logit + log2|s_v|.  At the end the first group (now one
+//                    thread per head dimension) combines the two groups'
+//                    states and normalises.
 // The last CTA to finish a (slice, KV head) merges the splits.  Every wait is
 // bounded in time and reported through the workspace status word.
 #include <cuda.h>
@@ -63,16 +70,16 @@ constexpr int BN = 128;       // list entries per tile
 constexpr int HB = 64;        // rows per half tile (a 64-token page)
 constexpr int QROWS = 32;     // query vectors per KV head, at most
 constexpr int NKT = 4;        // K tiles in tensor memory
-constexpr int NS = 2;         // S^T buffers in tensor memory
-constexpr int NVB = 2;        // widened V buffers
-constexpr int NPB = 2;        // P^T buffers
+constexpr int NS = 4;         // S^T buffers in tensor memory
+constexpr int NPB = 4;        // P^T buffers (two per softmax group)
 constexpr int NWARP = 14;
-// warps 0-3: softmax and epilogue (tensor-memory lane quarter = warp);
-// 4-7: K widen (lane quarter = warp - 4); 8: gather; 9: MMA; 10-13: V widen
-constexpr int W_K0 = 4, W_GATHER = 8, W_MMA = 9, W_V0 = 10;
+// warps 0-7: softmax, group w / 4 takes the tiles j with j % 2 == w / 4
+// (tensor-memory lane quarter w % 4); 8-11: widen (lane quarter w - 8);
+// 12: gather; 13: MMA
+constexpr int W_WID0 = 8, W_GATHER = 12, W_MMA = 13;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_K = 0;                  // NKT K tiles of 64 columns (128 f16 per key)
-constexpr uint32_t COL_S = NKT * 64;           // NS S^T buffers of NQ columns
+constexpr uint32_t COL_S = NKT * 64;           // NS S^T buffers of NQ columns, then two O^T
 }  // namespace dq
 
 // KQ: 1 = INT8 codes, 2 = INT4 codes (two per byte), 3 = FP8 E4M3 codes.
@@ -83,40 +90,40 @@ struct DqShape {
   static constexpr int CPR = CB / 16;                      // their 16-byte chunks
   static constexpr int WPC = 64 / CPR;                     // widened f16 pairs per chunk
   static constexpr int CODES = dq::BN * CB;                // one tile's K (or V) codes
-  static constexpr int STAGE = 2 * CODES;
+  static constexpr int VATOM = dq::BN * 128;               // f16 V tile: 128 keys x 128 B per 64 dimensions
+  // a stage holds the K codes at 0 and the V codes at VATOM, then the f16 V
+  // tile (atom a at a * VATOM): each key's f16 row covers its own code rows
+  // for 128-byte codes; for INT4 the widen warps agree before writing
+  static constexpr int STAGE = 2 * VATOM;
   static constexpr int QATOM = NQ * 128;                   // Q^T: NQ rows x 128 B per 64 dimensions
   static constexpr int PATOM = NQ * 128;                   // P^T: NQ rows x 128 B per 64 keys
   static constexpr int PBUF = 2 * PATOM;
-  static constexpr int VATOM = dq::BN * 128;               // V buffer: 128 keys x 128 B per 64 dimensions
-  static constexpr int VBUF = 2 * VATOM;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_P = ((2 * QATOM + 1023) / 1024) * 1024;
-  static constexpr int OFF_V = OFF_P + dq::NPB * PBUF;
-  static constexpr int OFF_C = OFF_V + dq::NVB * VBUF;
-  // barriers, misc words, agreement flags [2][4], per-warp maxima (two
-  // kinds) and sums [3][4][QROWS], per-query-vector logit scales [QROWS],
-  // references [2][3][QROWS]
-  static constexpr int TAIL = 512 + 64 + 64 + 3 * 4 * dq::QROWS * 4 + dq::QROWS * 4 + 6 * dq::QROWS * 4;
+  static constexpr int OFF_C = OFF_P + dq::NPB * PBUF;
+  // per group: agreement flags [2][4], tile maxima [2][4][QROWS], row sums
+  // [4][QROWS], references [2][3][QROWS]; logit scales [QROWS]
+  static constexpr int GRP_FLOATS = 8 + 8 * dq::QROWS + 4 * dq::QROWS + 6 * dq::QROWS;
+  static constexpr int TAIL = 512 + 64 + 2 * GRP_FLOATS * 4 + dq::QROWS * 4;
   static constexpr int BUDGET = 227 * 1024 - 1024 - OFF_C - TAIL;
   static constexpr int NC = BUDGET / STAGE < 8 ? BUDGET / STAGE : 8;   // code stages
   static constexpr int OFF_BAR = OFF_C + NC * STAGE;
-  // q_full, code_full[NC], code_empty[NC], kt_full[NKT], kt_empty[NKT], vb_full[NVB],
-  // vb_empty[NVB], s_full[NS], p_full[NPB], p_empty[NPB], o_ready, agree, drain
-  static constexpr int NBAR = 1 + 2 * NC + 2 * dq::NKT + 2 * dq::NVB + dq::NS + 2 * dq::NPB + 3;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base, abort flag, last-CTA flag
-  static constexpr int OFF_FLAG = OFF_MISC + 16;              // [2][4] int
-  static constexpr int OFF_RED = OFF_FLAG + 32;               // [2][4][QROWS] float: tile maxima
-  static constexpr int OFF_SUM = OFF_RED + 8 * dq::QROWS * 4;  // [4][QROWS] float: final row sums
-  static constexpr int OFF_QS = OFF_SUM + 4 * dq::QROWS * 4;  // [QROWS] float
-  static constexpr int OFF_REF = OFF_QS + dq::QROWS * 4;      // [2][3][QROWS] float: ml, mo, cw
-  static constexpr int SMEM_USED = OFF_REF + 6 * dq::QROWS * 4;
+  // q_full, code_full[NC], code_empty[NC], vb_full[NC], kc_read[NC], kt_full[NKT],
+  // kt_empty[NKT], s_full[NS], p_full[NPB], p_empty[NPB], o_ready[2], agree[2], drain
+  static constexpr int NBAR = 1 + 4 * NC + 2 * dq::NKT + dq::NS + 2 * dq::NPB + 5;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base, abort flag, last-CTA flag, final copies [2]
+  static constexpr int OFF_GRP = OFF_MISC + 32;         // [2] groups of GRP_FLOATS words
+  static constexpr int G_FLAG = 0, G_RED = 8, G_SUM = 8 + 8 * dq::QROWS, G_REF = 8 + 12 * dq::QROWS;
+  static constexpr int OFF_QS = OFF_GRP + 2 * GRP_FLOATS * 4;   // [QROWS] float
+  static constexpr int SMEM_USED = OFF_QS + dq::QROWS * 4;
   static constexpr int SMEM = SMEM_USED + 1024;
-  static constexpr uint32_t COL_O = dq::COL_S + dq::NS * NQ;   // O^T: NQ columns
-  static_assert(COL_O + NQ <= dq::TMEM_COLS, "tensor memory");
+  static constexpr uint32_t COL_O = dq::COL_S + dq::NS * NQ;   // O^T of group g: NQ columns at COL_O + g * NQ
+  static_assert(COL_O + 2 * NQ <= dq::TMEM_COLS, "tensor memory");
   static_assert(NC >= 3, "code ring too shallow");
   static_assert(NBAR * 8 <= 512, "barrier area");
+  static_assert(SMEM_USED - OFF_BAR <= TAIL, "tail area");
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(OFF_P % 1024 == 0 && OFF_V % 1024 == 0 && OFF_C % 1024 == 0 && STAGE % 1024 == 0 &&
+  static_assert(OFF_P % 1024 == 0 && OFF_C % 1024 == 0 && STAGE % 1024 == 0 &&
                     CODES % 1024 == 0 && QATOM % 1024 == 0 && PATOM % 1024 == 0,
                 "operand tiles and swizzled stages must be 1024-byte aligned");
   // split merge scratch (up to 2 * 256 * 32 + 64 floats) reuses the code ring
@@ -187,27 +194,32 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* code_full = q_full + 1;
-  uint64_t* code_empty = code_full + NC;
-  uint64_t* kt_full = code_empty + NC;
+  uint64_t* code_empty = code_full + NC;   // the stage's PV has completed
+  uint64_t* vb_full = code_empty + NC;     // the stage holds the f16 V tile
+  uint64_t* kc_read = vb_full + NC;        // the widen warps hold the stage's K codes
+  uint64_t* kt_full = kc_read + NC;
   uint64_t* kt_empty = kt_full + NKT;
-  uint64_t* vb_full = kt_empty + NKT;
-  uint64_t* vb_empty = vb_full + NVB;
-  uint64_t* s_full = vb_empty + NVB;
+  uint64_t* s_full = kt_empty + NKT;
   uint64_t* p_full = s_full + NS;
   uint64_t* p_empty = p_full + NPB;
-  uint64_t* o_ready = p_empty + NPB;
-  uint64_t* agree = o_ready + 1;
-  uint64_t* drain = agree + 1;
+  uint64_t* o_ready = p_empty + NPB;   // [2]: the PV of a group's tile has completed
+  uint64_t* agree = o_ready + 2;       // [2]: a group's four warps
+  uint64_t* drain = agree + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Sh::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::OFF_MISC + 4);
   int* am_last = reinterpret_cast<int*>(sm + Sh::OFF_MISC + 8);
-
+  int* final_copy = reinterpret_cast<int*>(sm + Sh::OFF_MISC + 16);   // [2]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int G = p.G, QV = p.QV;
   const bool q_bf16 = p.q_bf16 != 0;
   int n_s = p.L;
   if (p.kv_len) n_s = min(max(__ldg(p.kv_len + s), 0), p.L);
+  // splits past the sequence's last entry do nothing and are not merged; a
+  // sequence that fits one split writes its result directly
+  const int ns_unit = n_s > 0 && p.chunk > 0 ? (n_s + p.chunk - 1) / p.chunk : 1;
+  if (split >= ns_unit) return;
+  const bool single = ns_unit == 1;
   const int j0 = split * p.chunk;
   const int cnt = max(min(j0 + p.chunk, n_s) - j0, 0);
   const int T = (cnt + BN - 1) / BN;
@@ -221,28 +233,29 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   auto entry_raw = [&](int pos) { return __ldg(rows_safe + min(pos, pos_max)); };
   auto live = [&](int pos, int e) { return pos < cnt ? e : -1; };
   auto valid = [&](int r) { return r >= 0 && (long long)r < p.R; };
+  auto grp_words = [&](int grp) { return reinterpret_cast<float*>(sm + Sh::OFF_GRP) + grp * Sh::GRP_FLOATS; };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < NC; ++i) {
       mbar_init(code_full + i, 32);   // one arrival per gather lane
-      mbar_init(code_empty + i, 8);   // one per K warp and per V warp
+      mbar_init(code_empty + i, 1);
+      mbar_init(vb_full + i, 4);   // the four warps of the tile's softmax group
+      mbar_init(kc_read + i, 4);
     }
     for (int i = 0; i < NKT; ++i) {
       mbar_init(kt_full + i, 4);
       mbar_init(kt_empty + i, 1);
-    }
-    for (int i = 0; i < NVB; ++i) {
-      mbar_init(vb_full + i, 4);
-      mbar_init(vb_empty + i, 1);
     }
     for (int i = 0; i < NS; ++i) mbar_init(s_full + i, 1);
     for (int i = 0; i < NPB; ++i) {
       mbar_init(p_full + i, 4);
       mbar_init(p_empty + i, 1);
     }
-    mbar_init(o_ready, 1);
-    mbar_init(agree, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(o_ready + i, 1);
+      mbar_init(agree + i, 4);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -251,8 +264,8 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 0) {   // the softmax references' first copy: ml = mo = -inf, cw = 0
-    float* refs = reinterpret_cast<float*>(sm + Sh::OFF_REF);
+  if (warp == 0 || warp == 4) {   // each group's first reference copy: ml = mo = -inf, cw = 0
+    float* refs = grp_words(warp >> 2) + Sh::G_REF;
     refs[lane] = NEG_INF;
     refs[QROWS + lane] = NEG_INF;
     refs[2 * QROWS + lane] = 0.f;
@@ -275,11 +288,11 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       float* qs = reinterpret_cast<float*>(sm + Sh::OFF_QS);
       for (int r = lane / 16; r < NQ; r += 2) {
         const int c = lane % 16;
-        const bool live = r < QV;
+        const bool live_r = r < QV;
         const int i = r / G, h = g * G + r % G;
         float v[8];
         float mx = 0.f;
-        if (live) {
+        if (live_r) {
           const uint4 w4 = __ldg(reinterpret_cast<const uint4*>(qg + (((size_t)s * p.Nq + i) * p.Hq + h) * D) + c);
           const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
@@ -303,7 +316,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
         if (mx > 0.f && mx <= 3.402823e38f) k2 = min(max(140 - (int)((__float_as_uint(mx) >> 23) & 0xff), -126), 126);
         const float up = __int_as_float((127 + k2) << 23), down = __int_as_float((127 - k2) << 23);
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (live) {
+        if (live_r) {
           o.x = pack2h(v[0] * up, v[1] * up, false);
           o.y = pack2h(v[2] * up, v[3] * up, false);
           o.z = pack2h(v[4] * up, v[5] * up, false);
@@ -336,7 +349,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       }
       if (!__all_sync(0xffffffffu, mbar_wait(code_empty + c, (u & 1) ^ 1, abort_flag, wait_ns))) break;
       unsigned char* Kc = sm + Sh::OFF_C + c * Sh::STAGE;
-      unsigned char* Vc = Kc + Sh::CODES;
+      unsigned char* Vc = Kc + Sh::VATOM;
       // half h holds entries 64h .. 64h + 63 (lane values r[2h], r[2h + 1]);
       // a half that is one contiguous pool run goes by TMA
       bool contig[2];
@@ -400,16 +413,15 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       // operand descriptors built once; each MMA only adds a constant offset
       const uint64_t dQ = sdesc_sw128(smem_u32(sm + Sh::OFF_Q), 16, 1024);
       const uint64_t dP = sdesc_sw128(smem_u32(sm + Sh::OFF_P), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_V), Sh::VATOM, 1024);
-      const uint32_t tO = tbase + Sh::COL_O;
+      const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_C), Sh::VATOM, 1024);
       bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
-      // step j: QK of tile j, then PV of tile j - 1.  The waits block (the
-      // warp sleeps in them) rather than poll, leaving the issue slots of
-      // this scheduler to the softmax and widen warps that share it.  S^T
-      // buffer j % NS was last read by the softmax of tile j - NS, whose P^T
-      // the PV of step j - NS + 1 <= j - 1 has already waited for.
-      for (int j = 0; ok && j <= T; ++j) {
+      // step j: QK of tile j, then PV of tile j - 2 into the O^T of its
+      // group, so that a tile's S^T is computed while the softmax still
+      // works on earlier tiles.  The waits block (the warp sleeps in them)
+      // rather than poll.  S^T buffer j % NS was last read by the softmax of
+      // tile j - NS, whose P^T the PV of step j - NS + 2 <= j - 2 waited for.
+      for (int j = 0; ok && j <= T + 1; ++j) {
         if (j < T) {
           ok = mbar_wait(kt_full + j % NKT, (j / NKT) & 1, abort_flag, wait_ns);
           if (!ok) break;
@@ -422,46 +434,48 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
           tc_commit(s_full + j % NS);
           tc_commit(kt_empty + j % NKT);
         }
-        if (j >= 1) {
-          const int t = j - 1;
+        if (j >= 2) {
+          const int t = j - 2, c = t % NC;
           ok = mbar_wait(p_full + t % NPB, (t / NPB) & 1, abort_flag, wait_ns) &&
-               mbar_wait(vb_full + t % NVB, (t / NVB) & 1, abort_flag, wait_ns);
+               mbar_wait(vb_full + c, (t / NC) & 1, abort_flag, wait_ns);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t av = sdesc_at(dV, (t % NVB) * Sh::VBUF);
+          const uint64_t av = sdesc_at(dV, c * Sh::STAGE);
           const uint64_t bp = sdesc_at(dP, (t % NPB) * Sh::PBUF);
+          const uint32_t tO = tbase + Sh::COL_O + (t & 1) * NQ;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ss(tO, sdesc_at(av, kk * 2048), sdesc_at(bp, (kk >> 2) * Sh::PATOM + (kk & 3) * 32), id_pv,
-                   t > 0 || kk > 0);
-          tc_commit(vb_empty + t % NVB);
+                   t > 1 || kk > 0);
+          tc_commit(code_empty + c);
           tc_commit(p_empty + t % NPB);
-          tc_commit(o_ready);
+          tc_commit(o_ready + (t & 1));
         }
       }
       tc_commit(drain);
       dq_wait_drain(drain, 0);
     }
-  } else if (warp >= W_K0 && warp < W_K0 + 4) {
-    // ------------------------------------------------------------ K widen: one thread per key
-    const int k = (warp - W_K0) * 32 + lane;   // tensor-memory lane = key within the tile
-    const uint32_t lane_sel = (uint32_t)((warp - W_K0) * 32) << 16;
-    for (int j = 0; j < T; ++j) {
-      const int c = j % NC, u = j / NC, kt = j % NKT;
-      if (!__all_sync(0xffffffffu, mbar_wait(code_full + c, u & 1, abort_flag, wait_ns))) break;
-      const unsigned char* Kc = sm + Sh::OFF_C + c * Sh::STAGE;
-      // dimensions 0..63, then 64..127: half the row's codes and 32 f16 pairs
-      // in registers at a time
-      constexpr int HC = CPR / 2;
+  } else if (warp >= W_WID0) {
+    // ------------------------------------------------------------ widen: one thread per key
+    const int k = (warp - W_WID0) * 32 + lane;   // tensor-memory lane = key within the tile
+    const uint32_t lane_sel = (uint32_t)((warp - W_WID0) * 32) << 16;
+    constexpr int HC = CPR / 2;
+    bool ok = true;
+    for (int j = 0; ok && j < T; ++j) {
+      const int c = j % NC, kt = j % NKT;
+      const unsigned char* stg = sm + Sh::OFF_C + c * Sh::STAGE;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(code_full + c, (j / NC) & 1, abort_flag, wait_ns)))) break;
+      // dimensions 0..63, then 64..127 (half the row's codes and 32 f16
+      // pairs in registers at a time) into K tile kt
       uint4 ca[HC], cb[HC];
 #pragma unroll
       for (int ch = 0; ch < HC; ++ch) {
-        ca[ch] = *reinterpret_cast<const uint4*>(Kc + code_off<CB>(k, ch));
-        cb[ch] = *reinterpret_cast<const uint4*>(Kc + code_off<CB>(k, HC + ch));
+        ca[ch] = *reinterpret_cast<const uint4*>(stg + code_off<CB>(k, ch));
+        cb[ch] = *reinterpret_cast<const uint4*>(stg + code_off<CB>(k, HC + ch));
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(code_empty + c);   // the codes are in registers
-      if (!__all_sync(0xffffffffu, mbar_wait(kt_empty + kt, ((j / NKT) & 1) ^ 1, abort_flag, wait_ns))) break;
+      if (lane == 0) mbar_arrive(kc_read + c);   // the f16 V tile may now cover the K codes
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(kt_empty + kt, ((j / NKT) & 1) ^ 1, abort_flag, wait_ns)))) break;
       tc_fence_after();
       {
         uint32_t w[32];
@@ -480,85 +494,54 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(kt_full + kt);
     }
-  } else if (warp >= W_V0) {
-    // ------------------------------------------------------------ V widen: one thread per key
-    const int k = (warp - W_V0) * 32 + lane;
-    for (int j = 0; j < T; ++j) {
-      const int c = j % NC, u = j / NC, b = j % NVB;
-      if (!__all_sync(0xffffffffu, mbar_wait(code_full + c, u & 1, abort_flag, wait_ns))) break;
-      const unsigned char* Vc = sm + Sh::OFF_C + c * Sh::STAGE + Sh::CODES;
-      constexpr int HC = CPR / 2;
-      uint4 ca[HC], cb[HC];
-#pragma unroll
-      for (int ch = 0; ch < HC; ++ch) {
-        ca[ch] = *reinterpret_cast<const uint4*>(Vc + code_off<CB>(k, ch));
-        cb[ch] = *reinterpret_cast<const uint4*>(Vc + code_off<CB>(k, HC + ch));
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(code_empty + c);
-      if (!__all_sync(0xffffffffu, mbar_wait(vb_empty + b, ((j / NVB) & 1) ^ 1, abort_flag, wait_ns))) break;
-      // row k of the buffer: dimensions 8t..8t+7 (words 4t..4t+3) in 16-byte
-      // chunk t % 8 of atom t / 8, swizzled by the row; atom a holds
-      // dimensions 64a..64a+63, widened from half a of the codes
-      unsigned char* Vb = sm + Sh::OFF_V + b * Sh::VBUF;
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        uint32_t w[32];
-#pragma unroll
-        for (int ch = 0; ch < HC; ++ch) widen_chunk<KQ>(a ? cb[ch] : ca[ch], w + ch * Sh::WPC);
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-          *reinterpret_cast<uint4*>(Vb + a * Sh::VATOM + k * 128 + ((t ^ (k & 7)) << 4)) =
-              make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(vb_full + b);
-    }
-  } else if (warp < 4) {
+  } else {
     // ------------------------------------------------------------ softmax, one thread per key
-    const int k = warp * 32 + lane;
-    const uint32_t lane_sel = (uint32_t)(warp * 32) << 16;
-    int* flags = reinterpret_cast<int*>(sm + Sh::OFF_FLAG);   // [2][4]
-    float* red = reinterpret_cast<float*>(sm + Sh::OFF_RED);  // [4][QROWS] tile maxima
-    // [4][QROWS] row sums: their own slots, since a warp that has left the
-    // loop may write them while another still reads its last tile's maxima
-    float* rsum = reinterpret_cast<float*>(sm + Sh::OFF_SUM);
-    const float* qs = reinterpret_cast<const float*>(sm + Sh::OFF_QS);
-    const bool causal = p.mask_kind == FA_MASK_CAUSAL;
-    bool ok = true;
-    uint32_t ph = 0;   // completed phases of the agreement barrier
-    auto agree_wait = [&]() {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(agree);
-      const bool r = __all_sync(0xffffffffu, mbar_wait(agree, ph & 1, abort_flag, wait_ns));
-      ++ph;
-      return r;
-    };
+    const int grp = warp >> 2, wq = warp & 3;
+    const int k = wq * 32 + lane;
+    const uint32_t lane_sel = (uint32_t)(wq * 32) << 16;
+    float* gw = grp_words(grp);
+    int* flags = reinterpret_cast<int*>(gw + Sh::G_FLAG);   // [2][4]
+    float* red = gw + Sh::G_RED;                            // [2][4][QROWS] tile maxima: logit, logit + log2|s_v|
+    float* rsum = gw + Sh::G_SUM;                           // [4][QROWS] final row sums
     // Two lazy references per query vector: ml for the row sum l = sum of
     // 2^(x - ml), and mo for the weights that go into O^T, 2^(x + log2|s_v| - mo)
     // * sign(s_v), so that every weight sits below 2^8 in magnitude and the
     // largest ones near the top of the f16 range whatever the V scales are.
     // cw = 2^(ml - mo) turns a row-sum term into an O weight: w = p * s_v * cw.
-    // The three are the same for every thread and live in shared memory,
-    // two copies that alternate at each move; l is this thread's partial sum.
-    // (copy 0 starts at -inf, -inf, 0: set before the CTA's first barrier)
-    float* refs = reinterpret_cast<float*>(sm + Sh::OFF_REF);   // [2][3][QROWS]
-    int rp = 0;                                                  // current copy
+    // The three are the same for every thread of the group and live in shared
+    // memory, two copies that alternate at each move (copy 0 starts at -inf,
+    // -inf, 0); l is this thread's partial sum.
+    float* refs = gw + Sh::G_REF;   // [2][3][QROWS]
+    const float* qs = reinterpret_cast<const float*>(sm + Sh::OFF_QS);
+    uint64_t* agr = agree + grp;
+    const uint32_t colO = Sh::COL_O + grp * NQ;
+    const bool causal = p.mask_kind == FA_MASK_CAUSAL;
+    bool ok = true;
+    int rp = 0;        // current reference copy
+    uint32_t ph = 0;   // completed phases of the group's agreement barrier
+    auto agree_wait = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(agr);
+      const bool r = __all_sync(0xffffffffu, mbar_wait(agr, ph & 1, abort_flag, wait_ns));
+      ++ph;
+      return r;
+    };
     float l[QVP];
 #pragma unroll
     for (int q = 0; q < QVP; ++q) l[q] = 0.f;
     // the logit scales qs[] are read from shared memory once q_full has completed
-    if (T > 0 && !__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, wait_ns))) ok = false;
-    // this key's list entries three tiles ahead and its raw fp16 scales two
-    // tiles ahead; a scale is read at row 0 for a dead entry and zeroed at use
+    if (T > grp && !__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, wait_ns))) ok = false;
+    // this group's tiles are grp, grp + 2, ...; this key's list entries three
+    // of them ahead and its raw fp16 scales two ahead; a scale is read at row
+    // 0 for a dead entry and zeroed at use
+    auto tile_of = [&](int i) { return grp + 2 * i; };
     auto scale_raw = [&](const uint16_t* sc, int r) {
       const int rr = valid(r) ? r : 0;
       return __ldg(sc + ((size_t)(rr >> 6) * p.Hkv + g) * kPage + (rr & 63));
     };
     const bool has_rows = p.R > 0;
-    int e1 = entry_raw(k), e2 = entry_raw(BN + k), e3 = entry_raw(2 * BN + k);
-    int r1 = live(k, e1), r2 = live(BN + k, e2);
+    int e1 = entry_raw(tile_of(0) * BN + k), e2 = entry_raw(tile_of(1) * BN + k), e3 = entry_raw(tile_of(2) * BN + k);
+    int r1 = live(tile_of(0) * BN + k, e1), r2 = live(tile_of(1) * BN + k, e2);
     uint16_t hk1 = 0, hv1 = 0, hk2 = 0, hv2 = 0;
     if (has_rows) {
       hk1 = scale_raw(p.k_scale, r1);
@@ -566,21 +549,58 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       hk2 = scale_raw(p.k_scale, r2);
       hv2 = scale_raw(p.v_scale, r2);
     }
-    for (int j = 0; ok && j < T; ++j) {
+    for (int i = 0; ok && tile_of(i) < T; ++i) {
+      const int j = tile_of(i);
       const int r = valid(r1) ? r1 : -1;
       const float sk = r >= 0 ? __half2float(__ushort_as_half(hk1)) : 0.f;
       const float sv = r >= 0 ? __half2float(__ushort_as_half(hv1)) : 0.f;
       r1 = r2;
       hk1 = hk2;
       hv1 = hv2;
-      r2 = live((j + 2) * BN + k, e3);   // loaded an iteration ago
-      e3 = entry_raw((j + 3) * BN + k);
+      r2 = live(tile_of(i + 2) * BN + k, e3);   // loaded an iteration ago
+      e3 = entry_raw(tile_of(i + 3) * BN + k);
       if (has_rows) {
         hk2 = scale_raw(p.k_scale, r2);
         hv2 = scale_raw(p.v_scale, r2);
       }
       const float lsv = __log2f(fabsf(sv));   // -inf for a zero scale
-      const int pos = j0 + j * BN + k;   // list position of this key
+      const int pos = j0 + j * BN + k;        // list position of this key
+      {
+        // V of this tile, widened in place: this key's codes into registers;
+        // once the widen warps hold the stage's K codes (and, for INT4, the
+        // group's four warps hold their V codes: the f16 rows then cover
+        // other keys' code rows), row k of the f16 tile: dimensions
+        // 8t..8t+7 (words 4t..4t+3) in 16-byte chunk t % 8 of atom t / 8,
+        // swizzled by the row; atom a holds dimensions 64a..64a+63, widened
+        // from half a of the codes
+        constexpr int HC = CPR / 2;
+        const int c = j % NC;
+        unsigned char* stg = sm + Sh::OFF_C + c * Sh::STAGE;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(code_full + c, (j / NC) & 1, abort_flag, wait_ns)))) break;
+        uint4 ca[HC], cb[HC];
+#pragma unroll
+        for (int ch = 0; ch < HC; ++ch) {
+          ca[ch] = *reinterpret_cast<const uint4*>(stg + Sh::VATOM + code_off<CB>(k, ch));
+          cb[ch] = *reinterpret_cast<const uint4*>(stg + Sh::VATOM + code_off<CB>(k, HC + ch));
+        }
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(kc_read + c, (j / NC) & 1, abort_flag, wait_ns)))) break;
+        if constexpr (CB != 128) {
+          if (!(ok = agree_wait())) break;
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          uint32_t w[32];
+#pragma unroll
+          for (int ch = 0; ch < HC; ++ch) widen_chunk<KQ>(a ? cb[ch] : ca[ch], w + ch * Sh::WPC);
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            *reinterpret_cast<uint4*>(stg + a * Sh::VATOM + k * 128 + ((t ^ (k & 7)) << 4)) =
+                make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(vb_full + c);
+      }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + j % NS, (j / NS) & 1, abort_flag, wait_ns)))) break;
       tc_fence_after();
       uint32_t sr[32];
@@ -601,11 +621,11 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
         x[q] = vis ? __uint_as_float(sr[q]) * (qs[q] * sk) : NEG_INF;
         exceed = exceed || (x[q] > ml[q] + 8.f) || (x[q] + lsv > mo[q] + 8.f);
       }
-      // do the four warps agree that no reference has to move?
+      // do the group's four warps agree that no reference has to move?
       const bool wex = __any_sync(0xffffffffu, exceed);
-      if (lane == 0) flags[(j & 1) * 4 + warp] = wex ? 1 : 0;
+      if (lane == 0) flags[(i & 1) * 4 + wq] = wex ? 1 : 0;
       if (!(ok = agree_wait())) break;
-      const int* fl = flags + (j & 1) * 4;
+      const int* fl = flags + (i & 1) * 4;
       if (fl[0] | fl[1] | fl[2] | fl[3]) {
         // rare: each query vector's maxima over the tile's keys
 #pragma unroll
@@ -617,14 +637,14 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
             vo = fmaxf(vo, __shfl_xor_sync(0xffffffffu, vo, o));
           }
           if (lane == 0) {
-            red[warp * QROWS + q] = v;
-            red[(4 + warp) * QROWS + q] = vo;
+            red[wq * QROWS + q] = v;
+            red[(4 + wq) * QROWS + q] = vo;
           }
         }
         if (!(ok = agree_wait())) break;
-        // new references into the other copy (warp 0, a lane per query
-        // vector); each thread scales its own partial sums and keeps the O^T
-        // factors
+        // new references into the other copy (the group's first warp, a lane
+        // per query vector); each thread scales its own partial sums and
+        // keeps the O^T factors
         float* nref = refs + (rp ^ 1) * 3 * QROWS;
         float alpha[QVP];
         bool any_scale = false;
@@ -645,7 +665,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
             no = mto;
             any_scale = true;
           }
-          if (warp == 0 && lane == q) {
+          if (wq == 0 && lane == q) {
             nref[q] = nl;
             nref[QROWS + q] = no;
             nref[2 * QROWS + q] = no == NEG_INF || nl == NEG_INF ? 0.f : fast_ex2(nl - no);
@@ -655,23 +675,24 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
         // and the old copy, before any thread goes on
         if (!(ok = agree_wait())) break;
         rp ^= 1;
-        if (any_scale && j > 0) {
-          // O^T (this thread's lane = head dimension k) times alpha per query
-          // vector, once the PV of the previous tile has completed
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready, (j - 1) & 1, abort_flag, wait_ns)))) break;
+        if (any_scale && i > 0) {
+          // the group's O^T (this thread's lane = head dimension k) times
+          // alpha per query vector, once the PV of its previous tile has
+          // completed
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready + grp, (i - 1) & 1, abort_flag, wait_ns)))) break;
           tc_fence_after();
           uint32_t o[32];
           if constexpr (NQ == 16) {
-            tmem_ld16(tbase + lane_sel + Sh::COL_O, *reinterpret_cast<uint32_t(*)[16]>(o));
+            tmem_ld16(tbase + lane_sel + colO, *reinterpret_cast<uint32_t(*)[16]>(o));
           } else {
-            tmem_ld32(tbase + lane_sel + Sh::COL_O, o);
+            tmem_ld32(tbase + lane_sel + colO, o);
           }
 #pragma unroll
           for (int q = 0; q < QVP; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha[q]);
           if constexpr (NQ == 16) {
-            tmem_st16(tbase + lane_sel + Sh::COL_O, *reinterpret_cast<uint32_t(*)[16]>(o));
+            tmem_st16(tbase + lane_sel + colO, *reinterpret_cast<uint32_t(*)[16]>(o));
           } else {
-            tmem_st32(tbase + lane_sel + Sh::COL_O, o);
+            tmem_st32(tbase + lane_sel + colO, o);
           }
         }
       }
@@ -694,45 +715,66 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + pb);
     }
-    // ---- the row sums over all keys, then O^T normalised: this thread's
-    // lane is now head dimension k
+    // ---- each group's row sums, then the first group (this thread's lane
+    // now head dimension k) combines the two groups' states and normalises
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag, wait_ns));
 #pragma unroll
     for (int q = 0; q < QVP; ++q) {
       float v = l[q];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) rsum[warp * QROWS + q] = v;
+      if (lane == 0) rsum[wq * QROWS + q] = v;
     }
-    if (ok) ok = agree_wait();
+    if (wq == 0 && lane == 0) final_copy[grp] = rp;
+    named_barrier(1, 8 * 32);   // the eight softmax warps; every wait before it is bounded
     tc_fence_after();
-    const float* ml = refs + rp * 3 * QROWS;
-    const float* mo = ml + QROWS;
-    if (ok && !*abort_flag) {
-      uint32_t o[32];
+    if (grp == 0 && ok && !*abort_flag) {
+      const float* fA = grp_words(0) + Sh::G_REF + final_copy[0] * 3 * QROWS;
+      const float* fB = grp_words(1) + Sh::G_REF + final_copy[1] * 3 * QROWS;
+      const float* sA = grp_words(0) + Sh::G_SUM;
+      const float* sB = grp_words(1) + Sh::G_SUM;
+      uint32_t oA[32], oB[32];
       if (T > 0) {
         if constexpr (NQ == 16) {
-          tmem_ld16(tbase + lane_sel + Sh::COL_O, *reinterpret_cast<uint32_t(*)[16]>(o));
+          tmem_ld16(tbase + lane_sel + Sh::COL_O, *reinterpret_cast<uint32_t(*)[16]>(oA));
         } else {
-          tmem_ld32(tbase + lane_sel + Sh::COL_O, o);
+          tmem_ld32(tbase + lane_sel + Sh::COL_O, oA);
+        }
+      }
+      if (T > 1) {
+        if constexpr (NQ == 16) {
+          tmem_ld16(tbase + lane_sel + Sh::COL_O + NQ, *reinterpret_cast<uint32_t(*)[16]>(oB));
+        } else {
+          tmem_ld32(tbase + lane_sel + Sh::COL_O + NQ, oB);
         }
       }
 #pragma unroll
       for (int q = 0; q < QVP; ++q) {
         if (q >= QV) continue;
-        const float L = rsum[q] + rsum[QROWS + q] + rsum[2 * QROWS + q] + rsum[3 * QROWS + q];
-        // O^T holds the sum of 2^(x - mo) s_v v; relative to ml that is times 2^(mo - ml)
-        const float ov = T > 0 && mo[q] != NEG_INF && ml[q] != NEG_INF ? __uint_as_float(o[q]) * exp2f(mo[q] - ml[q]) : 0.f;
-        const int i = q / G, h = g * G + q % G;
-        const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
+        // a group with no tile has ml = mo = -inf and contributes nothing
+        const float mlA = fA[q], moA = fA[QROWS + q], mlB = fB[q], moB = fB[QROWS + q];
+        const float LA = sA[q] + sA[QROWS + q] + sA[2 * QROWS + q] + sA[3 * QROWS + q];
+        const float LB = sB[q] + sB[QROWS + q] + sB[2 * QROWS + q] + sB[3 * QROWS + q];
+        const float m = fmaxf(mlA, mlB);
+        float L = 0.f, ov = 0.f;
+        if (m != NEG_INF) {
+          if (mlA != NEG_INF) L += LA * exp2f(mlA - m);
+          if (mlB != NEG_INF) L += LB * exp2f(mlB - m);
+          // O^T of a group holds the sum of 2^(x - mo) s_v v: relative to m
+          // that is times 2^(mo - m)
+          if (T > 0 && moA != NEG_INF) ov += __uint_as_float(oA[q]) * exp2f(moA - m);
+          if (T > 1 && moB != NEG_INF) ov += __uint_as_float(oB[q]) * exp2f(moB - m);
+        }
+        const int qi = q / G, h = g * G + q % G;
+        const size_t oi = ((size_t)s * p.Nq + qi) * p.Hq + h;
         const size_t pi = (unit * p.nsplit + split) * QV + q;
-        if (p.nsplit == 1) {
+        if (single) {
           store_out(p.out, oi * D + k, L > 0.f ? ov / L : 0.f, p.out_dtype);
-          if (k == 0 && p.lse) p.lse[oi] = L > 0.f ? (ml[q] + __log2f(L)) * kLn2 : NEG_INF;
+          if (k == 0 && p.lse) p.lse[oi] = L > 0.f ? (m + __log2f(L)) * kLn2 : NEG_INF;
         } else {
-          if (ml[q] != NEG_INF) p.part_o[pi * D + k] = ov;
+          if (m != NEG_INF) p.part_o[pi * D + k] = ov;
           if (k == 0) {
-            p.part_ml[pi * 2] = ml[q];
+            p.part_ml[pi * 2] = m;
             p.part_ml[pi * 2 + 1] = L;
           }
         }
@@ -751,16 +793,16 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   // on its split counter (marked as aborted) so the counter ends at zero.
   const bool aborted = *abort_flag != 0;
   if (aborted && threadIdx.x == 0 && kp.err) atomicOr(kp.err, FA_WS_WAIT_EXPIRED);
-  if (p.nsplit == 1) return;
+  if (single) return;
 
   // ---- cross-split merge by the last CTA of this (slice, KV head)
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *am_last = split_arrive_last(p.counters + unit, p.nsplit, aborted);
+  if (threadIdx.x == 0) *am_last = split_arrive_last(p.counters + unit, ns_unit, aborted);
   __syncthreads();
   if (!*am_last) return;
   __threadfence();
-  merge_splits<D>(p, unit, QV, QV, s, g, reinterpret_cast<float*>(sm + Sh::OFF_C));
+  merge_splits<D>(p, unit, QV, QV, s, g, reinterpret_cast<float*>(sm + Sh::OFF_C), ns_unit);
   if (threadIdx.x == 0) p.counters[unit] = 0u;
 }
 

@@ -32,19 +32,20 @@ __device__ __forceinline__ bool split_arrive_last(unsigned int* counter, int nsp
   return true;
 }
 
-// part_ml / part_o rows are indexed (unit * nsplit + k) * rows + r.
+// part_ml / part_o rows are indexed (unit * nsplit + k) * rows + r; the
+// first ns_used splits of the unit are merged (0: all nsplit).
 // scratch: at least 2 * nsplit * QV + 2 * QV floats of shared memory.
 template <int D>
 __device__ __forceinline__ void merge_splits(const DecodeParams& p, size_t unit, int rows, int QV, int s, int g,
-                                             float* scratch) {
+                                             float* scratch, int ns_used = 0) {
   const float NEG_INF = __int_as_float(0xff800000);
   const int nthreads = blockDim.x, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
-  const int ns = p.nsplit;
+  const int ns = ns_used > 0 ? ns_used : p.nsplit;
   float* sw = scratch;                 // [ns][QV] weights (after step 2; m before)
   float* sl = scratch + ns * QV;       // [ns][QV] sums
   float* fin = sl + ns * QV;           // [QV] merged max, [QV] merged sum
-  const size_t base = unit * ns;
+  const size_t base = unit * p.nsplit;
   for (int t = tid; t < ns * QV; t += nthreads) {
     const int k = t / QV, r = t % QV;
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + (base + k) * rows + r);
