@@ -28,9 +28,10 @@
 //                    P^T in shared memory) into the O^T accumulator of the
 //                    tile's softmax group; O^T holds a lane per head
 //                    dimension and a column per query vector.
-//   softmax (2 x 4)  two groups of four warps take alternate tiles, each with
-//                    its own references, row sums and O^T, so that one
-//                    group's barriers and waits overlap the other's work; one
+//   softmax (n x 4)  three groups of four warps (two for more than 8 query
+//                    vectors) take the tiles in turn, each with its own
+//                    references, row sums and O^T, so that one group's
+//                    barriers and waits overlap the others' work; one
 //                    thread per key.  Each tile starts with its V codes,
 //                    widened exactly to f16 in place: the f16 V tile (rows =
 //                    keys) takes the whole code stage once the widen warps
@@ -46,8 +47,8 @@
 //                    O weight P * s_v as f16 into P^T, kept below 2^8 by a
 //                    second lazy reference of the same kind over
 //                    logit + log2|s_v|.  At the end the first group (now one
-//                    thread per head dimension) combines the two groups'
-//                    states and normalises.
+//                    thread per head dimension) combines the groups' states
+//                    and normalises.
 // The last CTA to finish a (slice, KV head) merges the splits.  Every wait is
 // bounded in time and reported through the workspace status word.
 #include <cuda.h>
@@ -71,12 +72,7 @@ constexpr int HB = 64;        // rows per half tile (a 64-token page)
 constexpr int QROWS = 32;     // query vectors per KV head, at most
 constexpr int NKT = 4;        // K tiles in tensor memory
 constexpr int NS = 4;         // S^T buffers in tensor memory
-constexpr int NPB = 4;        // P^T buffers (two per softmax group)
-constexpr int NWARP = 14;
-// warps 0-7: softmax, group w / 4 takes the tiles j with j % 2 == w / 4
-// (tensor-memory lane quarter w % 4); 8-11: widen (lane quarter w - 8);
-// 12: gather; 13: MMA
-constexpr int W_WID0 = 8, W_GATHER = 12, W_MMA = 13;
+constexpr int NPB = 4;        // P^T buffers (the tile j - 4 of a buffer is a softmax group's earlier tile)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_K = 0;                  // NKT K tiles of 64 columns (128 f16 per key)
 constexpr uint32_t COL_S = NKT * 64;           // NS S^T buffers of NQ columns, then two O^T
@@ -85,6 +81,15 @@ constexpr uint32_t COL_S = NKT * 64;           // NS S^T buffers of NQ columns, 
 // KQ: 1 = INT8 codes, 2 = INT4 codes (two per byte), 3 = FP8 E4M3 codes.
 template <int QVP, int KQ>
 struct DqShape {
+  // NGRP softmax groups of four warps; group g takes the tiles j with
+  // j % NGRP == g (tensor-memory lane quarter = warp % 4).  Then four widen
+  // warps (lane quarter = warp % 4), the gather warp and the MMA warp.
+  static constexpr int NGRP = QVP <= 8 ? 3 : 2;
+  static constexpr int NWARP = 4 * NGRP + 6;
+  static constexpr int W_WID0 = 4 * NGRP, W_GATHER = 4 * NGRP + 4, W_MMA = 4 * NGRP + 5;
+  // registers per thread: a scheduler holds ceil(NWARP / 4) of the CTA's
+  // warps in its 16,384-register file (18 warps: 96, 14 warps: 128)
+  static constexpr int MAXREG = (16384 / (32 * ((NWARP + 3) / 4))) & ~7;
   static constexpr int NQ = QVP < 16 ? 16 : QVP;            // MMA N: query vectors, padded
   static constexpr int CB = KQ == 2 ? dq::D / 2 : dq::D;   // code bytes of one (row, head)
   static constexpr int CPR = CB / 16;                      // their 16-byte chunks
@@ -104,21 +109,29 @@ struct DqShape {
   // per group: agreement flags [2][4], tile maxima [2][4][QROWS], row sums
   // [4][QROWS], references [2][3][QROWS]; logit scales [QROWS]
   static constexpr int GRP_FLOATS = 8 + 8 * dq::QROWS + 4 * dq::QROWS + 6 * dq::QROWS;
-  static constexpr int TAIL = 512 + 64 + 2 * GRP_FLOATS * 4 + dq::QROWS * 4;
+  static constexpr int TAIL = 512 + 64 + NGRP * GRP_FLOATS * 4 + dq::QROWS * 4;
   static constexpr int BUDGET = 227 * 1024 - 1024 - OFF_C - TAIL;
   static constexpr int NC = BUDGET / STAGE < 8 ? BUDGET / STAGE : 8;   // code stages
   static constexpr int OFF_BAR = OFF_C + NC * STAGE;
-  // q_full, code_full[NC], code_empty[NC], vb_full[NC], kc_read[NC], kt_full[NKT],
-  // kt_empty[NKT], s_full[NS], p_full[NPB], p_empty[NPB], o_ready[2], agree[2], drain
-  static constexpr int NBAR = 1 + 4 * NC + 2 * dq::NKT + dq::NS + 2 * dq::NPB + 5;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base, abort flag, last-CTA flag, final copies [2]
-  static constexpr int OFF_GRP = OFF_MISC + 32;         // [2] groups of GRP_FLOATS words
+  // q_full, code_full[NC], pv_done[NC], kc_read[NC], kt_full[NKT], s_full[NS],
+  // p_full[NPB], agree[NGRP], drain
+  static constexpr int NBAR = 1 + 3 * NC + dq::NKT + dq::NS + dq::NPB + NGRP + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base, abort flag, last-CTA flag, final copies [NGRP]
+  static constexpr int OFF_GRP = OFF_MISC + 32;         // [NGRP] groups of GRP_FLOATS words
   static constexpr int G_FLAG = 0, G_RED = 8, G_SUM = 8 + 8 * dq::QROWS, G_REF = 8 + 12 * dq::QROWS;
-  static constexpr int OFF_QS = OFF_GRP + 2 * GRP_FLOATS * 4;   // [QROWS] float
+  static constexpr int OFF_QS = OFF_GRP + NGRP * GRP_FLOATS * 4;   // [QROWS] float
   static constexpr int SMEM_USED = OFF_QS + dq::QROWS * 4;
   static constexpr int SMEM = SMEM_USED + 1024;
   static constexpr uint32_t COL_O = dq::COL_S + dq::NS * NQ;   // O^T of group g: NQ columns at COL_O + g * NQ
-  static_assert(COL_O + 2 * NQ <= dq::TMEM_COLS, "tensor memory");
+  static_assert(COL_O + NGRP * NQ <= dq::TMEM_COLS, "tensor memory");
+  // the QK of tile j is issued NGRP tiles before the PV of tile j: its S^T
+  // buffer, last read by tile j - NS, must have had its PV waited for
+  static_assert(dq::NS >= NGRP + 1 && NGRP <= 3, "S^T ring");
+  static_assert(dq::NKT == dq::NS, "a K tile is released by the QK that fills the S^T buffer of the same index");
+  // a PV is waited for through its stage's barrier: by the next user of its
+  // P^T buffer (NPB tiles on) and of its group's O^T (NGRP tiles on) before
+  // the stage's next PV (NC tiles on) can complete
+  static_assert(NC > dq::NPB && NC > NGRP, "pv_done ring");
   static_assert(NC >= 3, "code ring too shallow");
   static_assert(NBAR * 8 <= 512, "barrier area");
   static_assert(SMEM_USED - OFF_BAR <= TAIL, "tail area");
@@ -177,15 +190,16 @@ __device__ __forceinline__ uint32_t code_off(int k, int ch) {
 
 }  // namespace
 
-// 448 threads: 14 warps put four on some of the SM's four schedulers, whose
-// register files hold 16,384 each, so at most 128 registers per thread
+// One CTA per SM (all 512 tensor-memory columns); the register cap keeps the
+// warps that share a scheduler within its register file.
 template <int QVP, int KQ>
-__global__ void __launch_bounds__(dq::NWARP * 32, 1)
+__global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
     fa_rows_decode_tcq_kernel(const DqParams kp, const __grid_constant__ CUtensorMap tk,
                               const __grid_constant__ CUtensorMap tv) {
   using Sh = DqShape<QVP, KQ>;
   using namespace dq;
   constexpr int NC = Sh::NC, NQ = Sh::NQ, CB = Sh::CB, CPR = Sh::CPR;
+  constexpr int NGRP = Sh::NGRP, W_WID0 = Sh::W_WID0, W_GATHER = Sh::W_GATHER, W_MMA = Sh::W_MMA;
   const DecodeParams& p = kp.a;
   const unsigned long long wait_ns = p.wait_ns;
   const float NEG_INF = __int_as_float(0xff800000);
@@ -194,21 +208,21 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* code_full = q_full + 1;
-  uint64_t* code_empty = code_full + NC;   // the stage's PV has completed
-  uint64_t* vb_full = code_empty + NC;     // the stage holds the f16 V tile
-  uint64_t* kc_read = vb_full + NC;        // the widen warps hold the stage's K codes
+  // One commit per MMA group: pv_done[t % NC] completes with the PV of tile
+  // t (its code stage, its P^T buffer and its group's O^T are free again),
+  // s_full[j % NS] with the QK of tile j (its S^T is ready and its K tile,
+  // j % NKT with NKT = NS, may be overwritten).
+  uint64_t* pv_done = code_full + NC;
+  uint64_t* kc_read = pv_done + NC;        // the widen warps hold the stage's K codes
   uint64_t* kt_full = kc_read + NC;
-  uint64_t* kt_empty = kt_full + NKT;
-  uint64_t* s_full = kt_empty + NKT;
+  uint64_t* s_full = kt_full + NKT;
   uint64_t* p_full = s_full + NS;
-  uint64_t* p_empty = p_full + NPB;
-  uint64_t* o_ready = p_empty + NPB;   // [2]: the PV of a group's tile has completed
-  uint64_t* agree = o_ready + 2;       // [2]: a group's four warps
-  uint64_t* drain = agree + 2;
+  uint64_t* agree = p_full + NPB;      // [NGRP]: a group's four warps
+  uint64_t* drain = agree + NGRP;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Sh::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::OFF_MISC + 4);
   int* am_last = reinterpret_cast<int*>(sm + Sh::OFF_MISC + 8);
-  int* final_copy = reinterpret_cast<int*>(sm + Sh::OFF_MISC + 16);   // [2]
+  int* final_copy = reinterpret_cast<int*>(sm + Sh::OFF_MISC + 16);   // [NGRP]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int G = p.G, QV = p.QV;
@@ -239,21 +253,17 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < NC; ++i) {
       mbar_init(code_full + i, 32);   // one arrival per gather lane
-      mbar_init(code_empty + i, 1);
-      mbar_init(vb_full + i, 4);   // the four warps of the tile's softmax group
+      mbar_init(pv_done + i, 1);
       mbar_init(kc_read + i, 4);
     }
     for (int i = 0; i < NKT; ++i) {
       mbar_init(kt_full + i, 4);
-      mbar_init(kt_empty + i, 1);
     }
     for (int i = 0; i < NS; ++i) mbar_init(s_full + i, 1);
     for (int i = 0; i < NPB; ++i) {
       mbar_init(p_full + i, 4);
-      mbar_init(p_empty + i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(o_ready + i, 1);
+    for (int i = 0; i < NGRP; ++i) {
       mbar_init(agree + i, 4);
     }
     mbar_init(drain, 1);
@@ -264,7 +274,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 0 || warp == 4) {   // each group's first reference copy: ml = mo = -inf, cw = 0
+  if (warp < W_WID0 && (warp & 3) == 0) {   // each group's first reference copy: ml = mo = -inf, cw = 0
     float* refs = grp_words(warp >> 2) + Sh::G_REF;
     refs[lane] = NEG_INF;
     refs[QROWS + lane] = NEG_INF;
@@ -347,7 +357,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
         nx[t] = nx2[t];
         nx2[t] = entry_raw((j + 2) * BN + lane + 32 * t);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(code_empty + c, (u & 1) ^ 1, abort_flag, wait_ns))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(pv_done + c, (u & 1) ^ 1, abort_flag, wait_ns))) break;
       unsigned char* Kc = sm + Sh::OFF_C + c * Sh::STAGE;
       unsigned char* Vc = Kc + Sh::VATOM;
       // half h holds entries 64h .. 64h + 63 (lane values r[2h], r[2h + 1]);
@@ -416,12 +426,13 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_C), Sh::VATOM, 1024);
       bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
-      // step j: QK of tile j, then PV of tile j - 2 into the O^T of its
-      // group, so that a tile's S^T is computed while the softmax still
-      // works on earlier tiles.  The waits block (the warp sleeps in them)
-      // rather than poll.  S^T buffer j % NS was last read by the softmax of
-      // tile j - NS, whose P^T the PV of step j - NS + 2 <= j - 2 waited for.
-      for (int j = 0; ok && j <= T + 1; ++j) {
+      // step j: QK of tile j, then PV of tile j - NGRP into the O^T of its
+      // group, so that a tile's S^T is computed while the softmax groups
+      // still work on earlier tiles.  The waits block (the warp sleeps in
+      // them) rather than poll.  S^T buffer j % NS was last read by the
+      // softmax of tile j - NS, whose P^T the PV of step j - NS + NGRP <= j - 1
+      // waited for.
+      for (int j = 0; ok && j < T + NGRP; ++j) {
         if (j < T) {
           ok = mbar_wait(kt_full + j % NKT, (j / NKT) & 1, abort_flag, wait_ns);
           if (!ok) break;
@@ -432,24 +443,21 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ts(dS, ak + kk * 8, sdesc_at(dQ, (kk >> 2) * Sh::QATOM + (kk & 3) * 32), id_qk, kk > 0);
           tc_commit(s_full + j % NS);
-          tc_commit(kt_empty + j % NKT);
         }
-        if (j >= 2) {
-          const int t = j - 2, c = t % NC;
-          ok = mbar_wait(p_full + t % NPB, (t / NPB) & 1, abort_flag, wait_ns) &&
-               mbar_wait(vb_full + c, (t / NC) & 1, abort_flag, wait_ns);
+        if (j >= NGRP) {
+          const int t = j - NGRP, c = t % NC;
+          // the group arrives after its V tile and then its P^T are written
+          ok = mbar_wait(p_full + t % NPB, (t / NPB) & 1, abort_flag, wait_ns);
           if (!ok) break;
           tc_fence_after();
           const uint64_t av = sdesc_at(dV, c * Sh::STAGE);
           const uint64_t bp = sdesc_at(dP, (t % NPB) * Sh::PBUF);
-          const uint32_t tO = tbase + Sh::COL_O + (t & 1) * NQ;
+          const uint32_t tO = tbase + Sh::COL_O + (t % NGRP) * NQ;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ss(tO, sdesc_at(av, kk * 2048), sdesc_at(bp, (kk >> 2) * Sh::PATOM + (kk & 3) * 32), id_pv,
-                   t > 1 || kk > 0);
-          tc_commit(code_empty + c);
-          tc_commit(p_empty + t % NPB);
-          tc_commit(o_ready + (t & 1));
+                   t >= NGRP || kk > 0);
+          tc_commit(pv_done + c);
         }
       }
       tc_commit(drain);
@@ -475,7 +483,8 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(kc_read + c);   // the f16 V tile may now cover the K codes
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(kt_empty + kt, ((j / NKT) & 1) ^ 1, abort_flag, wait_ns)))) break;
+      // K tile kt last held tile j - NKT, whose QK completed with s_full[kt]
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + kt, ((j / NKT) & 1) ^ 1, abort_flag, wait_ns)))) break;
       tc_fence_after();
       {
         uint32_t w[32];
@@ -531,10 +540,10 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
     for (int q = 0; q < QVP; ++q) l[q] = 0.f;
     // the logit scales qs[] are read from shared memory once q_full has completed
     if (T > grp && !__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, wait_ns))) ok = false;
-    // this group's tiles are grp, grp + 2, ...; this key's list entries three
+    // this group's tiles are grp, grp + NGRP, ...; this key's list entries three
     // of them ahead and its raw fp16 scales two ahead; a scale is read at row
     // 0 for a dead entry and zeroed at use
-    auto tile_of = [&](int i) { return grp + 2 * i; };
+    auto tile_of = [&](int i) { return grp + NGRP * i; };
     auto scale_raw = [&](const uint16_t* sc, int r) {
       const int rr = valid(r) ? r : 0;
       return __ldg(sc + ((size_t)(rr >> 6) * p.Hkv + g) * kPage + (rr & 63));
@@ -598,8 +607,6 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
                 make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
         }
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(vb_full + c);
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + j % NS, (j / NS) & 1, abort_flag, wait_ns)))) break;
       tc_fence_after();
@@ -679,7 +686,8 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
           // the group's O^T (this thread's lane = head dimension k) times
           // alpha per query vector, once the PV of its previous tile has
           // completed
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_ready + grp, (i - 1) & 1, abort_flag, wait_ns)))) break;
+          const int jp = j - NGRP;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(pv_done + jp % NC, (jp / NC) & 1, abort_flag, wait_ns)))) break;
           tc_fence_after();
           uint32_t o[32];
           if constexpr (NQ == 16) {
@@ -699,7 +707,10 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       // P^T row q, key k: the O weight as f16, once the PV that last read this
       // buffer has completed
       const int pb = j % NPB;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_empty + pb, ((j / NPB) & 1) ^ 1, abort_flag, wait_ns)))) break;
+      if (j >= NPB) {
+        const int jp = j - NPB;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(pv_done + jp % NC, (jp / NC) & 1, abort_flag, wait_ns)))) break;
+      }
       unsigned char* Pb = sm + Sh::OFF_P + pb * Sh::PBUF + (k >> 6) * Sh::PATOM + (k & 7) * 2;
       const float* mlc = refs + rp * 3 * QROWS;
       const float* cw = mlc + 2 * QROWS;
@@ -716,7 +727,7 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       if (lane == 0) mbar_arrive(p_full + pb);
     }
     // ---- each group's row sums, then the first group (this thread's lane
-    // now head dimension k) combines the two groups' states and normalises
+    // now head dimension k) combines the groups' states and normalises
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag, wait_ns));
 #pragma unroll
     for (int q = 0; q < QVP; ++q) {
@@ -726,53 +737,55 @@ __global__ void __launch_bounds__(dq::NWARP * 32, 1)
       if (lane == 0) rsum[wq * QROWS + q] = v;
     }
     if (wq == 0 && lane == 0) final_copy[grp] = rp;
-    named_barrier(1, 8 * 32);   // the eight softmax warps; every wait before it is bounded
+    named_barrier(1, NGRP * 4 * 32);   // the softmax warps; every wait before it is bounded
     tc_fence_after();
     if (grp == 0 && ok && !*abort_flag) {
-      const float* fA = grp_words(0) + Sh::G_REF + final_copy[0] * 3 * QROWS;
-      const float* fB = grp_words(1) + Sh::G_REF + final_copy[1] * 3 * QROWS;
-      const float* sA = grp_words(0) + Sh::G_SUM;
-      const float* sB = grp_words(1) + Sh::G_SUM;
-      uint32_t oA[32], oB[32];
-      if (T > 0) {
-        if constexpr (NQ == 16) {
-          tmem_ld16(tbase + lane_sel + Sh::COL_O, *reinterpret_cast<uint32_t(*)[16]>(oA));
-        } else {
-          tmem_ld32(tbase + lane_sel + Sh::COL_O, oA);
-        }
+      // per query vector: m = the largest group reference, L = the groups'
+      // sums relative to m, and O^T relative to m (a group's O^T holds the
+      // sum of 2^(x - mo) s_v v, so it enters times 2^(mo - m)); a group with
+      // no tile has ml = mo = -inf and contributes nothing
+      float mq[QVP], ov[QVP];
+#pragma unroll
+      for (int q = 0; q < QVP; ++q) {
+        float m = NEG_INF;
+        for (int gi = 0; gi < NGRP; ++gi) m = fmaxf(m, grp_words(gi)[Sh::G_REF + final_copy[gi] * 3 * QROWS + q]);
+        mq[q] = m;
+        ov[q] = 0.f;
       }
-      if (T > 1) {
+      for (int gi = 0; gi < NGRP && gi < T; ++gi) {
+        const float* fr = grp_words(gi) + Sh::G_REF + final_copy[gi] * 3 * QROWS;
+        uint32_t o[32];
         if constexpr (NQ == 16) {
-          tmem_ld16(tbase + lane_sel + Sh::COL_O + NQ, *reinterpret_cast<uint32_t(*)[16]>(oB));
+          tmem_ld16(tbase + lane_sel + Sh::COL_O + gi * NQ, *reinterpret_cast<uint32_t(*)[16]>(o));
         } else {
-          tmem_ld32(tbase + lane_sel + Sh::COL_O + NQ, oB);
+          tmem_ld32(tbase + lane_sel + Sh::COL_O + gi * NQ, o);
+        }
+#pragma unroll
+        for (int q = 0; q < QVP; ++q) {
+          const float mo = fr[QROWS + q];
+          if (mq[q] != NEG_INF && mo != NEG_INF) ov[q] += __uint_as_float(o[q]) * exp2f(mo - mq[q]);
         }
       }
 #pragma unroll
       for (int q = 0; q < QVP; ++q) {
         if (q >= QV) continue;
-        // a group with no tile has ml = mo = -inf and contributes nothing
-        const float mlA = fA[q], moA = fA[QROWS + q], mlB = fB[q], moB = fB[QROWS + q];
-        const float LA = sA[q] + sA[QROWS + q] + sA[2 * QROWS + q] + sA[3 * QROWS + q];
-        const float LB = sB[q] + sB[QROWS + q] + sB[2 * QROWS + q] + sB[3 * QROWS + q];
-        const float m = fmaxf(mlA, mlB);
-        float L = 0.f, ov = 0.f;
+        const float m = mq[q];
+        float L = 0.f;
         if (m != NEG_INF) {
-          if (mlA != NEG_INF) L += LA * exp2f(mlA - m);
-          if (mlB != NEG_INF) L += LB * exp2f(mlB - m);
-          // O^T of a group holds the sum of 2^(x - mo) s_v v: relative to m
-          // that is times 2^(mo - m)
-          if (T > 0 && moA != NEG_INF) ov += __uint_as_float(oA[q]) * exp2f(moA - m);
-          if (T > 1 && moB != NEG_INF) ov += __uint_as_float(oB[q]) * exp2f(moB - m);
+          for (int gi = 0; gi < NGRP; ++gi) {
+            const float ml = grp_words(gi)[Sh::G_REF + final_copy[gi] * 3 * QROWS + q];
+            const float* sg = grp_words(gi) + Sh::G_SUM;
+            if (ml != NEG_INF) L += (sg[q] + sg[QROWS + q] + sg[2 * QROWS + q] + sg[3 * QROWS + q]) * exp2f(ml - m);
+          }
         }
         const int qi = q / G, h = g * G + q % G;
         const size_t oi = ((size_t)s * p.Nq + qi) * p.Hq + h;
         const size_t pi = (unit * p.nsplit + split) * QV + q;
         if (single) {
-          store_out(p.out, oi * D + k, L > 0.f ? ov / L : 0.f, p.out_dtype);
+          store_out(p.out, oi * D + k, L > 0.f ? ov[q] / L : 0.f, p.out_dtype);
           if (k == 0 && p.lse) p.lse[oi] = L > 0.f ? (m + __log2f(L)) * kLn2 : NEG_INF;
         } else {
-          if (m != NEG_INF) p.part_o[pi * D + k] = ov;
+          if (m != NEG_INF) p.part_o[pi * D + k] = ov[q];
           if (k == 0) {
             p.part_ml[pi * 2] = m;
             p.part_ml[pi * 2 + 1] = L;
@@ -833,7 +846,7 @@ int dq_occupancy() {
   auto kern = fa_rows_decode_tcq_kernel<QVP, KQ>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, dq::NWARP * 32, Sh::SMEM) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Sh::NWARP * 32, Sh::SMEM) != cudaSuccess) return 0;
   n = n < 1 ? n : 1;   // 512 tensor-memory columns: one CTA per SM
   if (n > 0) cached[dev].store(n, std::memory_order_relaxed);
   return n;
@@ -851,7 +864,7 @@ cudaError_t dq_launch(const DecodeParams& a, unsigned int* err, cudaStream_t st)
   memset(&tv, 0, sizeof(tv));
   kp.tma = a.R >= dq::HB && dq_map(&tk, a.k, Sh::CB, a.Hkv, a.R) && dq_map(&tv, a.v, Sh::CB, a.Hkv, a.R);
   dim3 grid(a.nsplit, a.Hkv, a.S);
-  fa_rows_decode_tcq_kernel<QVP, KQ><<<grid, dq::NWARP * 32, Sh::SMEM, st>>>(kp, tk, tv);
+  fa_rows_decode_tcq_kernel<QVP, KQ><<<grid, Sh::NWARP * 32, Sh::SMEM, st>>>(kp, tk, tv);
   return cudaGetLastError();
 }
 
