@@ -23,11 +23,11 @@
 //                    largest), taken back out of its logit scale.
 //   widen warps (4)  one thread per key: its K codes widened exactly to f16
 //                    into a K tile in tensor memory (lane = key).
-//   MMA warp         S^T = K Q^T (A = the K tile in tensor memory, B = Q^T),
-//                    then O^T += V^T P^T (A = the V tile read MN-major, B =
-//                    P^T in shared memory) into the O^T accumulator of the
-//                    tile's softmax group; O^T holds a lane per head
-//                    dimension and a column per query vector.
+//   MMA warps (2)    one issues S^T = K Q^T (A = the K tile in tensor
+//                    memory, B = Q^T), the other O^T += V^T P^T (A = the V
+//                    tile read MN-major, B = P^T in shared memory) into the
+//                    O^T accumulator of the tile's softmax group; O^T holds a
+//                    lane per head dimension and a column per query vector.
 //   softmax (n x 4)  three groups of four warps (two for more than 8 query
 //                    vectors) take the tiles in turn, each with its own
 //                    references, row sums and O^T, so that one group's
@@ -83,12 +83,14 @@ template <int QVP, int KQ>
 struct DqShape {
   // NGRP softmax groups of four warps; group g takes the tiles j with
   // j % NGRP == g (tensor-memory lane quarter = warp % 4).  Then four widen
-  // warps (lane quarter = warp % 4), the gather warp and the MMA warp.
+  // warps (lane quarter = warp % 4), the gather warp, the QK warp and the PV
+  // warp (two issuers, so that neither kind of MMA waits behind the other's
+  // operands).
   static constexpr int NGRP = QVP <= 8 ? 3 : 2;
-  static constexpr int NWARP = 4 * NGRP + 6;
-  static constexpr int W_WID0 = 4 * NGRP, W_GATHER = 4 * NGRP + 4, W_MMA = 4 * NGRP + 5;
+  static constexpr int NWARP = 4 * NGRP + 7;
+  static constexpr int W_WID0 = 4 * NGRP, W_GATHER = 4 * NGRP + 4, W_MMA = 4 * NGRP + 5, W_PV = 4 * NGRP + 6;
   // registers per thread: a scheduler holds ceil(NWARP / 4) of the CTA's
-  // warps in its 16,384-register file (18 warps: 96, 14 warps: 128)
+  // warps in its 16,384-register file (19 warps: 96, 15 warps: 128)
   static constexpr int MAXREG = (16384 / (32 * ((NWARP + 3) / 4))) & ~7;
   static constexpr int NQ = QVP < 16 ? 16 : QVP;            // MMA N: query vectors, padded
   static constexpr int CB = KQ == 2 ? dq::D / 2 : dq::D;   // code bytes of one (row, head)
@@ -127,6 +129,9 @@ struct DqShape {
   // the QK of tile j is issued NGRP tiles before the PV of tile j: its S^T
   // buffer, last read by tile j - NS, must have had its PV waited for
   static_assert(dq::NS >= NGRP + 1 && NGRP <= 3, "S^T ring");
+  // the QK of tile j waits for the P^T of tile j - NS (its S^T buffer's last
+  // reader): that barrier's next phase, tile j - NS + NPB, needs the QK of j
+  static_assert(dq::NPB >= dq::NS, "P^T ring");
   static_assert(dq::NKT == dq::NS, "a K tile is released by the QK that fills the S^T buffer of the same index");
   // a PV is waited for through its stage's barrier: by the next user of its
   // P^T buffer (NPB tiles on) and of its group's O^T (NGRP tiles on) before
@@ -199,7 +204,7 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
   using Sh = DqShape<QVP, KQ>;
   using namespace dq;
   constexpr int NC = Sh::NC, NQ = Sh::NQ, CB = Sh::CB, CPR = Sh::CPR;
-  constexpr int NGRP = Sh::NGRP, W_WID0 = Sh::W_WID0, W_GATHER = Sh::W_GATHER, W_MMA = Sh::W_MMA;
+  constexpr int NGRP = Sh::NGRP, W_WID0 = Sh::W_WID0, W_GATHER = Sh::W_GATHER, W_MMA = Sh::W_MMA, W_PV = Sh::W_PV;
   const DecodeParams& p = kp.a;
   const unsigned long long wait_ns = p.wait_ns;
   const float NEG_INF = __int_as_float(0xff800000);
@@ -266,7 +271,7 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
     for (int i = 0; i < NGRP; ++i) {
       mbar_init(agree + i, 4);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);   // one commit from each MMA issuer
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -414,51 +419,58 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
         if ((tma_pend >> c) & 1u) dq_wait_drain(code_full + c, (tma_par >> c) & 1u);
     }
   } else if (warp == W_MMA) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK issuer
     if (lane == 0 && T > 0) {
-      // S^T = K Q^T: M = 128 keys (A in tensor memory), N = NQ, K = 128 dims
+      // S^T = K Q^T: M = 128 keys (A in tensor memory), N = NQ, K = 128 dims;
+      // the Q^T descriptor is built once and each MMA adds a constant offset
       const uint32_t id_qk = make_idesc_f16_ab(128, NQ, false, false, false);
-      // O^T += V^T P^T: M = 128 dims (A = the V buffer read MN-major), N = NQ, K = 16 keys each
-      const uint32_t id_pv = make_idesc_f16_ab(128, NQ, false, true, false);
-      // operand descriptors built once; each MMA only adds a constant offset
       const uint64_t dQ = sdesc_sw128(smem_u32(sm + Sh::OFF_Q), 16, 1024);
-      const uint64_t dP = sdesc_sw128(smem_u32(sm + Sh::OFF_P), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_C), Sh::VATOM, 1024);
       bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
-      // step j: QK of tile j, then PV of tile j - NGRP into the O^T of its
-      // group, so that a tile's S^T is computed while the softmax groups
-      // still work on earlier tiles.  The waits block (the warp sleeps in
-      // them) rather than poll.  S^T buffer j % NS was last read by the
-      // softmax of tile j - NS, whose P^T the PV of step j - NS + NGRP <= j - 1
-      // waited for.
-      for (int j = 0; ok && j < T + NGRP; ++j) {
-        if (j < T) {
-          ok = mbar_wait(kt_full + j % NKT, (j / NKT) & 1, abort_flag, wait_ns);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t ak = tbase + COL_K + (j % NKT) * 64;
-          const uint32_t dS = tbase + COL_S + (j % NS) * NQ;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(dS, ak + kk * 8, sdesc_at(dQ, (kk >> 2) * Sh::QATOM + (kk & 3) * 32), id_qk, kk > 0);
-          tc_commit(s_full + j % NS);
-        }
-        if (j >= NGRP) {
-          const int t = j - NGRP, c = t % NC;
-          // the group arrives after its V tile and then its P^T are written
+      for (int j = 0; ok && j < T; ++j) {
+        // S^T buffer j % NS last held tile j - NS, whose softmax has read it
+        // once that tile's P^T is written
+        if (j >= NS) {
+          const int t = j - NS;
           ok = mbar_wait(p_full + t % NPB, (t / NPB) & 1, abort_flag, wait_ns);
           if (!ok) break;
-          tc_fence_after();
-          const uint64_t av = sdesc_at(dV, c * Sh::STAGE);
-          const uint64_t bp = sdesc_at(dP, (t % NPB) * Sh::PBUF);
-          const uint32_t tO = tbase + Sh::COL_O + (t % NGRP) * NQ;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tO, sdesc_at(av, kk * 2048), sdesc_at(bp, (kk >> 2) * Sh::PATOM + (kk & 3) * 32), id_pv,
-                   t >= NGRP || kk > 0);
-          tc_commit(pv_done + c);
         }
+        ok = mbar_wait(kt_full + j % NKT, (j / NKT) & 1, abort_flag, wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ak = tbase + COL_K + (j % NKT) * 64;
+        const uint32_t dS = tbase + COL_S + (j % NS) * NQ;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(dS, ak + kk * 8, sdesc_at(dQ, (kk >> 2) * Sh::QATOM + (kk & 3) * 32), id_qk, kk > 0);
+        tc_commit(s_full + j % NS);
+      }
+      tc_commit(drain);
+      dq_wait_drain(drain, 0);
+    }
+  } else if (warp == W_PV) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0 && T > 0) {
+      // O^T += V^T P^T: M = 128 dims (A = the V tile read MN-major), N = NQ,
+      // K = 16 keys each, into the O^T of the tile's group
+      const uint32_t id_pv = make_idesc_f16_ab(128, NQ, false, true, false);
+      const uint64_t dP = sdesc_sw128(smem_u32(sm + Sh::OFF_P), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_C), Sh::VATOM, 1024);
+      bool ok = true;
+      for (int t = 0; ok && t < T; ++t) {
+        // the group arrives after its V tile and then its P^T are written
+        ok = mbar_wait(p_full + t % NPB, (t / NPB) & 1, abort_flag, wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const int c = t % NC;
+        const uint64_t av = sdesc_at(dV, c * Sh::STAGE);
+        const uint64_t bp = sdesc_at(dP, (t % NPB) * Sh::PBUF);
+        const uint32_t tO = tbase + Sh::COL_O + (t % NGRP) * NQ;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss(tO, sdesc_at(av, kk * 2048), sdesc_at(bp, (kk >> 2) * Sh::PATOM + (kk & 3) * 32), id_pv,
+                 t >= NGRP || kk > 0);
+        tc_commit(pv_done + c);
       }
       tc_commit(drain);
       dq_wait_drain(drain, 0);
