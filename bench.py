@@ -507,7 +507,9 @@ def measure(args, rank, world, p, workload, cpu_baseline):
                                               rows.data_ptr(), p.L, sh))
         call(entry(ctypes.byref(a_list[i % len(a_list)] if a is None else a), ws.data_ptr(), ws.numel(), sh))
 
-    launches_per_step = 1 + (1 if paged else 0) + (8 if select else 0)
+    # a bf16 prefill is three kernels: the V-range scan, then the two prefill
+    # modes (V to f16, V kept in bf16), one of which exits at once
+    launches_per_step = 1 + (1 if paged else 0) + (8 if select else 0) + (2 if is_prefill and p.dtype == "bf16" else 0)
 
     for i in range(args.warmup):
         step(i)

@@ -15,6 +15,13 @@
 //                  listed rows are one contiguous pool run, else a cp.async
 //                  gather into the same 128-byte-swizzled layout (padding
 //                  rows zero-filled); two K/V stages.
+//   converters     (bf16 pools) two warps turn each landed V stage into f16
+//                  in place, so that P can be one f16 value: exact for every
+//                  bf16 value below 65536 in magnitude (one below 2^-14 becomes
+//                  an f16 subnormal, within 2^-25 of it).  A scan of the
+//                  listed V rows before the launch finds any finite value of
+//                  65536 or more; the launch then keeps V in bf16 and P as the
+//                  pair below.
 //   MMA warp       S_t = Q_t K_j^T into tensor memory (tcgen05.mma, both
 //                  operands in shared memory), then O_t += P_t V_j with P_t read
 //                  from tensor memory and V_j in shared memory (MN-major).
@@ -22,10 +29,10 @@
 //                  loads S_t, masks, keeps a running max that is only moved
 //                  when it grows by more than 2^8 (then O_t is rescaled in
 //                  place), writes P_t = exp2(S*c - m) over S_t as 16-bit
-//                  values (bf16: the pair P_hi = rn(P), P_lo = rn(P - P_hi),
-//                  which keeps about 16 significant bits of P where one bf16
-//                  rounding keeps 8; f16: rn(P) alone, 11 bits), and finally
-//                  normalises O_t.
+//                  values (f16 rn(P), 11 bits, whenever V is f16; else the bf16
+//                  pair P_hi = rn(P), P_lo = rn(P - P_hi), which keeps about 16
+//                  significant bits of P where one bf16 rounding keeps 8), and
+//                  finally normalises O_t.
 //
 // Tensor memory: S0 | S1 | O0 | O1, 128 columns each (all 512).  The two
 // warpgroups ping-pong: while one computes softmax, the tensor core runs the
@@ -40,6 +47,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -67,8 +75,9 @@ constexpr int OFF_K = 2 * TILE;
 constexpr int OFF_V = OFF_K + NST * TILE;
 constexpr int OFF_BAR = OFF_V + NST * TILE;
 // q_full, k_full[NST], v_full[NST], k_empty[NST], v_empty[NST], s_full[2],
-// p_full[2], o_final[2], drain, pair[8] (the two warps that share a Q tile's rows)
-constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 1 + 8;
+// p_full[2], o_final[2], drain, pair[8] (the two warps that share a Q tile's rows),
+// v_conv[NST] (bf16: the V stage is ready for the PV)
+constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 1 + 8 + NST;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int OFF_IDX = OFF_MISC + 16;     // [NPROD][BN] list entries of the tile each gather warp is on
 // [2 tile parities][2 Q tiles][2 column halves][128 rows] partial row maxima, then
@@ -112,12 +121,24 @@ __device__ __forceinline__ bool col_visible(int k, unsigned vb0, unsigned vb1, u
   return ((vb >> (k & 31)) & 1u) && (jbase + k <= lim);
 }
 
-template <bool BF16>
+// MODE 0: f16 pool.  MODE 1: bf16 pool, V converted to f16 (f16 P).
+// MODE 2: bf16 pool, V kept in bf16 (the P pair).  A bf16 launch runs modes
+// 1 and 2; each CTA of the one the scan before the launch does not select
+// exits at once.  Mode 2 is selected when a listed V value is beyond f16's
+// range, or when more than a quarter of the KV tiles are gathered (not one
+// contiguous pool run): there mode 1 has a single warp gathering K (two
+// gather and convert V), mode 2 three warps on both.
+template <int MODE>
 __global__ void __launch_bounds__(pf::NWARP * 32, 1)
     fa_rows_prefill_kernel(const PrefillKernelParams kp, const __grid_constant__ CUtensorMap tq,
                            const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
   using namespace pf;
+  constexpr bool BF16 = MODE != 0, VF16 = MODE == 1, PAIR = MODE == 2;
   const PrefillParams& p = kp.a;
+  if constexpr (BF16) {
+    const bool pair_mode = __ldcg(p.err + 1) != 0u || 4u * __ldcg(p.err + 2) > __ldcg(p.err + 3);
+    if (pair_mode != PAIR) return;
+  }
   const unsigned long long wait_ns = p.wait_ns;
   const float NEG_INF = __int_as_float(0xff800000);
   extern __shared__ unsigned char smem_raw[];
@@ -133,6 +154,9 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
   uint64_t* o_final = p_full + 2;
   uint64_t* drain = o_final + 2;
   uint64_t* pair = drain + 1;
+  uint64_t* v_conv = pair + 8;
+  // V converted to f16: one warp gathers and two convert
+  constexpr int NPRODK = VF16 ? 1 : NPROD;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
 
@@ -154,8 +178,9 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
     for (int i = 0; i < NST; ++i) {
       // one arrival per lane of the three producer warps: asynchronous when
       // its gathered copies land, or plain next to the TMA byte count
-      mbar_init(k_full + i, NPROD * 32);
-      mbar_init(v_full + i, NPROD * 32);
+      mbar_init(k_full + i, NPRODK * 32);
+      mbar_init(v_full + i, NPRODK * 32);
+      mbar_init(v_conv + i, 2);
       mbar_init(k_empty + i, 1);
       mbar_init(v_empty + i, 1);
     }
@@ -179,7 +204,100 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
   const uint32_t tbase = *tmem_holder;
 
   if (warp >= NSMX) {
-    if (warp == W_PROD || warp > W_MMA) {
+    if (VF16 && warp > W_MMA) {
+      // ------------------------------------------------------------ V converters (bf16)
+      // A V tile that is one contiguous pool run arrives by TMA (the
+      // producer's); the converters gather the others themselves with
+      // cp.async, one tile ahead, each thread later converting exactly the
+      // 16-byte groups it copied.  Thread tid owns groups it * 64 + tid of the
+      // tile: row e = group / 16, 16-byte column c = group % 16.
+      const int ci = warp - W_MMA - 1;                    // 0, 1
+      const int tid = ci * 32 + lane;                     // 0..63
+      constexpr int NU = TILE / 16 / 64;                  // 16-byte groups per thread
+      const char* vbase = static_cast<const char*>(p.v);
+      int32_t* cidx = reinterpret_cast<int32_t*>(sm + OFF_IDX) + (1 + ci) * BN;   // this warp's copy of a tile's rows
+      // the tile's 128 entries (lane + 32t), its contiguity as the producer decides it
+      int nxt[4];
+      #pragma unroll
+      for (int t = 0; t < 4; ++t) nxt[t] = lane + 32 * t < n_s ? __ldg(rows_g + lane + 32 * t) : -1;
+      auto next_tile = [&](int j, bool& contig) {
+        int rows[4];
+        #pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int r = nxt[t];
+          rows[t] = (r < 0 || (long long)r >= p.R) ? -1 : r;
+          const int pos = (j + 1) * BN + lane + 32 * t;
+          nxt[t] = pos < n_s ? __ldg(rows_g + pos) : -1;
+        }
+        const int r0 = __shfl_sync(0xffffffffu, rows[0], 0);
+        bool c = true;
+        #pragma unroll
+        for (int t = 0; t < 4; ++t) c = c && rows[t] >= 0 && rows[t] == r0 + lane + 32 * t;
+        contig = __all_sync(0xffffffffu, c) && kp.tma_kv;
+        if (!contig) {
+          __syncwarp();
+          #pragma unroll
+          for (int t = 0; t < 4; ++t) cidx[lane + 32 * t] = rows[t];
+          __syncwarp();
+        }
+      };
+      // a gathered tile's copies into its stage, once both PVs of the tile two
+      // back have read it; one commit group per tile (empty for a TMA tile)
+      auto issue = [&](int j, bool contig) -> bool {
+        if (!contig) {
+          const int st = j % NST;
+          if (!__all_sync(0xffffffffu, mbar_wait(v_empty + st, ((j / NST) & 1) ^ 1, abort_flag, wait_ns))) return false;
+          unsigned char* dst = sm + OFF_V + st * TILE;
+          #pragma unroll 4
+          for (int it = 0; it < NU; ++it) {
+            const int grp = it * 64 + tid, e = grp >> 4, c = grp & 15;
+            const int r = cidx[e];
+            const bool ok = r >= 0;
+            const size_t go = ((size_t)(ok ? r : 0) * p.Hkv + g) * (HD * 2) + c * 16;
+            cp_async16(dst + (c >> 3) * HALF + e * 128 + (((c & 7) ^ (e & 7)) << 4), vbase + go, ok);
+          }
+        }
+        cp_async_commit();
+        return true;
+      };
+      bool contig_cur = true, contig_nxt = true, ok = true;
+      if (T > 0) {
+        next_tile(0, contig_cur);
+        ok = issue(0, contig_cur);
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        const int st = j % NST;
+        const bool contig = contig_cur;
+        if (j + 1 < T) {
+          next_tile(j + 1, contig_nxt);
+          if (!(ok = issue(j + 1, contig_nxt))) break;
+          contig_cur = contig_nxt;
+          cp_async_wait<1>();   // this thread's copies of tile j (not j + 1)
+        } else {
+          cp_async_wait<0>();
+        }
+        if (contig && !(ok = __all_sync(0xffffffffu, mbar_wait(v_full + st, (j / NST) & 1, abort_flag, wait_ns)))) break;
+        uint4* vt = reinterpret_cast<uint4*>(sm + OFF_V + st * TILE);
+        #pragma unroll 8
+        for (int it = 0; it < NU; ++it) {
+          const int grp = it * 64 + tid, e = grp >> 4, c = grp & 15;
+          uint4* at = vt + ((c >> 3) * HALF + e * 128 + (((c & 7) ^ (e & 7)) << 4)) / 16;
+          const uint4 w = *at;
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+          uint32_t o[4];
+          #pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const __half2 hv = __floats2half2_rn(__uint_as_float(wv[t] << 16), __uint_as_float(wv[t] & 0xffff0000u));
+            o[t] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          *at = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(v_conv + st);
+      }
+      cp_async_wait_all();
+    } else if (warp == W_PROD || warp > W_MMA) {
       // ------------------------------------------------------------ producers
       // Per KV tile: one TMA tile load per 64-column half and matrix when the
       // 128 listed rows are one contiguous pool run (warp 8, lane 0), else a
@@ -207,7 +325,8 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       const char* vb = static_cast<const char*>(p.v);
       int32_t* idx = reinterpret_cast<int32_t*>(sm + OFF_IDX) + pi * BN;
       // this warp's row pairs of a gathered tile: [it_lo, it_hi) of the 64
-      const int it_lo = pi * 22, it_hi = min(BN / 2, it_lo + 22);
+      constexpr int PER = (BN / 2 + NPRODK - 1) / NPRODK;
+      const int it_lo = pi * PER, it_hi = min(BN / 2, it_lo + PER);
       const int c = lane & 15;
       int nxt[4];
       #pragma unroll
@@ -266,7 +385,11 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
         load(contig, r0, sm + OFF_K + st * TILE, &tk, kb, k_full + st, st, u);
         if (!__all_sync(0xffffffffu, mbar_wait(v_empty + st, (u & 1) ^ 1, abort_flag, wait_ns))) break;
         if (lead) tma_pend &= ~(1u << (NST + st));
-        load(contig, r0, sm + OFF_V + st * TILE, &tv, vb, v_full + st, NST + st, u);
+        if (VF16 && !contig) {
+          mbar_arrive(v_full + st);   // the converters gather this V tile
+        } else {
+          load(contig, r0, sm + OFF_V + st * TILE, &tv, vb, v_full + st, NST + st, u);
+        }
       }
       cp_async_wait_all();
       // bulk copies still in flight must land before the CTA can exit
@@ -281,7 +404,8 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0 && T > 0) {
         const uint32_t id_qk = make_idesc_f16(128, 128, BF16, false);
-        const uint32_t id_pv = make_idesc_f16(128, 128, BF16, true);
+        // PV: f16 P times an f16 V tile, or the bf16 pair times a bf16 tile
+        const uint32_t id_pv = make_idesc_f16(128, 128, PAIR, true);
         // operand descriptors built once; each MMA only adds a constant offset
         static_assert(NST == 2, "two K and V stages");
         const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + OFF_Q), 16, 1024), dQ1 = sdesc_at(dQ0, TILE);
@@ -305,7 +429,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
           #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t vd = sdesc_at(vb, kk * 2048);
-            if constexpr (BF16) {
+            if constexpr (PAIR) {
               mma_ts(d, a + kk * 16, vd, id_pv, acc || kk > 0);
               mma_ts(d, a + kk * 16 + 8, vd, id_pv, 1);
             } else {
@@ -332,7 +456,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
           for (int qt = 0; qt < 2; ++qt) {
             if (np[qt] < nq[qt]) {
               const int j = np[qt], st = j % NST;
-              if (mbar_test_wait(p_full + qt, j & 1) && mbar_test_wait(v_full + st, (j / NST) & 1)) {
+              if (mbar_test_wait(p_full + qt, j & 1) && mbar_test_wait((VF16 ? v_conv : v_full) + st, (j / NST) & 1)) {
                 tc_fence_after();
                 fence_proxy_async_smem();
                 pv(qt, st, j > 0);
@@ -494,7 +618,8 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       const float nmu = (m_used == NEG_INF) ? 0.f : -m_used;
       const float2 c2v = make_float2(c, c), nmu2 = make_float2(nmu, nmu);
       float2 acc = make_float2(0.f, 0.f);
-      auto emit = [&](const uint32_t (&sv)[32], int q) {
+      auto emit = [&](const uint32_t (&sv)[32], int q, auto pair_t) {
+        constexpr bool PAIR = decltype(pair_t)::value;
         #pragma unroll
         for (int o = 0; o < 4; ++o) {
           // keys 8o..8o+7 of this 32-column chunk: 4 P (or P_hi) words, and
@@ -507,9 +632,9 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
                 __ffma2_rn(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), c2v, nmu2);
             const float2 pr = make_float2(fast_ex2(t.x), fast_ex2(t.y));
             acc = __fadd2_rn(acc, pr);
-            const uint32_t hi = pack2(pr.x, pr.y, BF16);
+            const uint32_t hi = pack2(pr.x, pr.y, PAIR);
             w[k] = hi;
-            if constexpr (BF16) {
+            if constexpr (PAIR) {
               const float2 rem =
                   __fadd2_rn(pr, make_float2(-__uint_as_float(hi << 16), -__uint_as_float(hi & 0xffff0000u)));
               w[4 + k] = pack2(rem.x, rem.y, true);
@@ -518,7 +643,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
           // this half's keys 32q + 8o ..: column 16 * (2q + o/2) + 4 * (o%2) of its 64
           const uint32_t col = tS + (2 * q + (o >> 1)) * 16 + (o & 1) * 4;
           tmem_st4_nowait(col, w[0], w[1], w[2], w[3]);
-          if constexpr (BF16) tmem_st4_nowait(col + 8, w[4], w[5], w[6], w[7]);
+          if constexpr (PAIR) tmem_st4_nowait(col + 8, w[4], w[5], w[6], w[7]);
         }
       };
       // pass 2: the same 32-column chunks read again, turned into P
@@ -526,7 +651,7 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
       for (int q = 0; q < 2; ++q) {
         uint32_t sv[32];
         load_chunk(sv, q);
-        emit(sv, q);
+        emit(sv, q, std::integral_constant<bool, PAIR>{});
       }
       tmem_wait_st();
       l += acc.x + acc.y;
@@ -592,6 +717,64 @@ __global__ void __launch_bounds__(pf::NWARP * 32, 1)
   if (threadIdx.x == 0 && *abort_flag && p.err) atomicOr(p.err, FA_WS_WAIT_EXPIRED);
 }
 
+// Before a bf16 launch, per 128-entry KV tile of every slice (one warp each):
+// is any listed V value finite and of magnitude 65536 or more (not an f16
+// value: word 1 of the status block gets 1), and is the tile not one
+// contiguous pool run (word 2 counts those, word 3 all tiles)?  The words
+// were zeroed before.
+__global__ void __launch_bounds__(256) prefill_v_scan_kernel(const uint4* v, const int32_t* kv_rows,
+                                                             const int32_t* kv_len, int S, int L, long long R,
+                                                             int row_chunks, int tma_kv, unsigned int* words) {
+  const int lane = threadIdx.x & 31;
+  const int tiles_per = (L + pf::BN - 1) / pf::BN;
+  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+  uint32_t bad = 0;
+  unsigned gathered = 0, tiles = 0;
+  for (long long e = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); e < (long long)S * tiles_per;
+       e += nw) {
+    const int s = (int)(e / tiles_per), j0 = (int)(e % tiles_per) * pf::BN;
+    const int n_s = kv_len ? min(max(__ldg(kv_len + s), 0), L) : L;
+    if (j0 >= n_s) continue;
+    const int32_t* rows = kv_rows + (size_t)s * L + j0;
+    int r[4];
+    #pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int pos = lane + 32 * t;
+      const int x = j0 + pos < n_s ? __ldg(rows + pos) : -1;
+      r[t] = (x < 0 || (long long)x >= R) ? -1 : x;
+    }
+    const int r0 = __shfl_sync(0xffffffffu, r[0], 0);
+    bool contig = tma_kv != 0;
+    #pragma unroll
+    for (int t = 0; t < 4; ++t) contig = contig && r[t] >= 0 && r[t] == r0 + lane + 32 * t;
+    contig = __all_sync(0xffffffffu, contig);
+    ++tiles;
+    if (!contig) ++gathered;
+    #pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      for (int rr = 0; rr < 32; ++rr) {
+        const int row = __shfl_sync(0xffffffffu, r[t], rr);
+        if (row < 0) continue;
+        const uint4* rowp = v + (size_t)row * row_chunks;
+        for (int i = lane; i < row_chunks; i += 32) {
+          const uint4 w = __ldg(rowp + i);
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+          #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t a = wv[u] & 0x7fff7fffu;
+            bad |= __vcmpgeu2(a, 0x47804780u) & __vcmpltu2(a, 0x7f807f80u);
+          }
+        }
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(words, 1u);
+  if (lane == 0 && tiles) {
+    atomicAdd(words + 1, gathered);
+    atomicAdd(words + 2, tiles);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 
@@ -630,21 +813,42 @@ cudaError_t prefill_launch(const PrefillParams& a, cudaStream_t st) {
     if (!make_map_3d(&tk, a.k, bf16, pf::HD, a.Hkv, a.R, 64, 1, pf::BN)) return cudaErrorInvalidValue;
     if (!make_map_3d(&tv, a.v, bf16, pf::HD, a.Hkv, a.R, 64, 1, pf::BN)) return cudaErrorInvalidValue;
   }
-  auto kern = bf16 ? fa_rows_prefill_kernel<true> : fa_rows_prefill_kernel<false>;
+  if (bf16) {
+    // words 1-3 of the status block: the scan's V-range flag, gathered and all KV tiles
+    cudaError_t e = cudaMemsetAsync(a.err + 1, 0, 3 * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return e;
+    const long long tiles = (long long)a.S * ((a.L + pf::BN - 1) / pf::BN);   // one warp each, 8 per block
+    const long long blocks = (tiles + 7) / 8;
+    if (blocks > 0) {
+      prefill_v_scan_kernel<<<(unsigned)(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, st>>>(
+          static_cast<const uint4*>(a.v), a.kv_rows, a.kv_len, a.S, a.L, a.R, a.Hkv * pf::HD / 8, kp.tma_kv,
+          a.err + 1);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
   static std::atomic<int> attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  const int bit = bf16 ? 1 : 2;
-  if (!(attr_done[dev].load(std::memory_order_relaxed) & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done[dev].fetch_or(bit, std::memory_order_relaxed);
-  }
   const int qb = (a.Nq + 2 * kp.PT - 1) / (2 * kp.PT);
   dim3 grid(qb, a.Hkv, a.S);
-  kern<<<grid, pf::NWARP * 32, pf::SMEM, st>>>(kp, tq, tk, tv);
-  return cudaGetLastError();
+  // f16: mode 0; bf16: modes 1 (V to f16) and 2 (V kept), one of which exits
+  const int modes[2] = {bf16 ? 1 : 0, bf16 ? 2 : -1};
+  for (int mode : modes) {
+    if (mode < 0) continue;
+    auto kern = mode == 0 ? fa_rows_prefill_kernel<0> : mode == 1 ? fa_rows_prefill_kernel<1> : fa_rows_prefill_kernel<2>;
+    const int bit = 1 << mode;
+    if (!(attr_done[dev].load(std::memory_order_relaxed) & bit)) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::SMEM);
+      if (e != cudaSuccess) return e;
+      attr_done[dev].fetch_or(bit, std::memory_order_relaxed);
+    }
+    kern<<<grid, pf::NWARP * 32, pf::SMEM, st>>>(kp, tq, tk, tv);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace far

@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import row_indexed_flash_gb300 as far
 import synth
 from helpers import assert_lse, assert_parity, dev_bits, oracle_for
@@ -99,6 +100,43 @@ def test_prefill_peaked_attention(peak, layout, dtype):
     ref, ref_lse = oracle_for(p)
     assert_parity(out, ref, f"{peak} {layout} {dtype}")
     assert_lse(lse, ref_lse, f"{peak} {layout} {dtype}")
+
+
+def _bf16_times_pow2(bits, e):
+    """16-bit patterns of x * 2^e for bf16 x (exact for N(0,1) data)."""
+    f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** e)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("layout", sorted(PEAKED_LAYOUTS))
+@pytest.mark.parametrize("where", ["all_rows", "one_tile"])
+def test_prefill_bf16_values_beyond_f16_range(where, layout):
+    """bf16 V tiles go to f16 before PV unless a listed V value is finite and
+    2^16 or more, which f16 cannot represent: the launch then keeps V in bf16
+    and P as the bf16 pair.  With every V row times 2^17, out / 2^17 must
+    match the oracle on the unscaled rows; with only the rows of one 128-entry
+    tile of the first slice scaled, the rest of the launch has ordinary values
+    (checked at |err| <= 2e-3 + 1e-4 * the softmax-weighted |V|: terms near
+    2^17 meet in f32 sums)."""
+    p = PEAKED_LAYOUTS[layout]("bf16")
+    if where == "all_rows":
+        ref, ref_lse = oracle_for(p)
+        p.v = _bf16_times_pow2(p.v, 17)
+        out, lse = run_prefill(p)
+        assert_parity(out / 2.0 ** 17, ref, f"{where} {layout}")
+        return
+    rows = p.kv_rows[0, 256:384]
+    rows = rows[rows >= 0]
+    p.v[rows] = _bf16_times_pow2(p.v[rows], 17)
+    ref, _ = oracle_for(p)
+    # the softmax-weighted |V|: the size of the terms whose rounding is summed
+    mag, _ = oracle_for(p, k=oracle.widen_bf16(p.k), v=np.abs(oracle.widen_bf16(p.v)))
+    out, _ = run_prefill(p)
+    g = out.double().cpu().numpy()
+    assert np.all(np.isfinite(g))
+    err = np.abs(g - ref)
+    assert (err <= 2e-3 + 1e-4 * mag).all(), f"{where} {layout}: max err {err.max():.3e}"
+    assert np.abs(ref[0]).max() > 2.0 ** 10, "the scaled rows must reach the first slice's output"
 
 
 @pytest.mark.parametrize("odt", [torch.bfloat16, torch.float16])
