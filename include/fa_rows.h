@@ -123,7 +123,8 @@ typedef struct fa_rows_args {
  * Bytes of scratch (a device buffer, 256-byte aligned) that fa_rows_decode /
  * fa_rows_prefill need for these arguments; at least 256.  Layout: bytes
  * [0, 256) are the status block, whose first uint32 is the status word
- * (FA_WS_WAIT_EXPIRED); decode then holds one arrival counter per (slice, KV
+ * (FA_WS_WAIT_EXPIRED; the next words are the calls' own scratch); decode
+ * then holds one arrival counter per (slice, KV
  * head) and, when the list is split over several CTAs, the per-split partial
  * results.  The buffer must be ZERO-FILLED once after allocation
  * (fa_rows_workspace_init); every call leaves the counters at zero again, an
@@ -186,6 +187,14 @@ fa_status fa_rows_decode_static(const fa_rows_args* a, fa_stream_t stream);
  * D = 128, FA_BF16 or FA_F16 for q and the pool; Nq >= 1.  The workspace
  * (fa_rows_workspace_size(a, 1) = 256 bytes, zero-filled once) is required:
  * it holds the status word; a NULL ws is rejected with FA_ERR_WORKSPACE.
+ * bf16 pools: the call first scans the listed V rows (one extra kernel, one
+ * read of them) and writes words 1-3 of the status block as its own scratch:
+ * when no listed V value is beyond f16's range (finite, 65536 or more) and
+ * at most a quarter of the 128-entry KV tiles are gathered rather than one
+ * contiguous pool run, V tiles are converted to f16 in shared memory and P
+ * enters the PV product as one f16 value (11 significant bits; a bf16 V value
+ * below 2^-14 in magnitude becomes an f16 subnormal, within 2^-25 of it);
+ * otherwise V stays bf16 and P is the pair rn(P) + rn(P - rn(P)).
  */
 fa_status fa_rows_prefill(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_stream_t stream);
 

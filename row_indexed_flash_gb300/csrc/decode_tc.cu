@@ -636,7 +636,10 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
       // M=64 takes as long.
       const uint32_t id_qk = make_idesc_f16(QVP <= 16 ? 64 : 128, BN, bf16, false);
       const uint32_t id_pv = make_idesc_f16(128, D, bf16, true);
-      const uint32_t sQ = smem_u32(sm + Sh::OFF_Q), sK = smem_u32(sm + Sh::OFF_K), sV = smem_u32(sm + Sh::OFF_V);
+      // operand descriptors built once; each MMA adds a constant offset
+      const uint64_t dQ = sdesc_sw128(smem_u32(sm + Sh::OFF_Q), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(sm + Sh::OFF_K), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sm + Sh::OFF_V), Sh::KV_ATOM, 1024);
       const uint32_t tO = tbase + Sh::COL_O;
       bool ok = mbar_wait(q_full, 0, abort_flag, wait_ns);
       tc_fence_after();
@@ -654,12 +657,12 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
           // 16-bit stages are written by cp.async copies that arrived on
           // k_full by themselves: order them before the tensor core's reads
           if constexpr (KQ == 0) fence_proxy_async_smem();
+          const uint64_t dKs = sdesc_at(dK, st * Sh::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t a_off = (kk >> 2) * Sh::QATOM + (kk & 3) * 32;
             const uint32_t b_off = (kk >> 2) * Sh::KV_ATOM + (kk & 3) * 32;
-            mma_ss(tbase + Sh::COL_S + b * BN, sdesc_sw128(sQ + a_off, 16, 1024),
-                   sdesc_sw128(sK + st * Sh::TILE + b_off, 16, 1024), id_qk, kk > 0);
+            mma_ss(tbase + Sh::COL_S + b * BN, sdesc_at(dQ, a_off), sdesc_at(dKs, b_off), id_qk, kk > 0);
           }
           tc_commit(s_full + b);
           tc_commit(k_empty + st);
@@ -672,10 +675,10 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
           tc_fence_after();
           if constexpr (KQ == 0) fence_proxy_async_smem();
           // O += P_hi V + P_lo V (P_hi in S columns 0..BN/2-1, P_lo after it)
+          const uint64_t dVs = sdesc_at(dV, pst * Sh::TILE);
 #pragma unroll
           for (int kk = 0; kk < 2 * (BN / 16); ++kk)
-            mma_ts(tO, tbase + Sh::COL_S + pb * BN + kk * 8,
-                   sdesc_sw128(sV + pst * Sh::TILE + (kk % (BN / 16)) * 2048, Sh::KV_ATOM, 1024), id_pv,
+            mma_ts(tO, tbase + Sh::COL_S + pb * BN + kk * 8, sdesc_at(dVs, (kk % (BN / 16)) * 2048), id_pv,
                    npv > 0 || kk > 0);
           tc_commit(v_empty + pst);
           tc_commit(o_ready);
