@@ -750,19 +750,36 @@ __global__ void __launch_bounds__(256) prefill_v_scan_kernel(const uint4* v, con
     contig = __all_sync(0xffffffffu, contig);
     ++tiles;
     if (!contig) ++gathered;
+    // the tile's rows four at a time, each read by the whole warp (coalesced),
+    // all of a group's loads issued before any is examined
     #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      for (int rr = 0; rr < 32; ++rr) {
-        const int row = __shfl_sync(0xffffffffu, r[t], rr);
-        if (row < 0) continue;
-        const uint4* rowp = v + (size_t)row * row_chunks;
-        for (int i = lane; i < row_chunks; i += 32) {
-          const uint4 w = __ldg(rowp + i);
-          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+      for (int rr = 0; rr < 32; rr += 4) {
+        int row[4];
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) row[u] = __shfl_sync(0xffffffffu, r[t], rr + u);
+        for (int i0 = 0; i0 < row_chunks; i0 += 64) {
+          uint4 w[4][2];
           #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t a = wv[u] & 0x7fff7fffu;
-            bad |= __vcmpgeu2(a, 0x47804780u) & __vcmpltu2(a, 0x7f807f80u);
+            #pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int i = i0 + lane + 32 * c;
+              w[u][c] = (row[u] >= 0 && i < row_chunks) ? __ldg(v + (size_t)row[u] * row_chunks + i)
+                                                        : make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            #pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint32_t wv[4] = {w[u][c].x, w[u][c].y, w[u][c].z, w[u][c].w};
+              #pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t a = wv[q] & 0x7fff7fffu;
+                bad |= __vcmpgeu2(a, 0x47804780u) & __vcmpltu2(a, 0x7f807f80u);
+              }
+            }
           }
         }
       }
