@@ -110,7 +110,7 @@ struct DqShape {
   static constexpr int OFF_C = OFF_P + dq::NPB * PBUF;
   // per group: agreement flags [2][4], tile maxima [2][4][QROWS], row sums
   // [4][QROWS], references [2][3][QROWS]; logit scales [QROWS]
-  static constexpr int GRP_FLOATS = 8 + 8 * dq::QROWS + 4 * dq::QROWS + 6 * dq::QROWS;
+  static constexpr int GRP_FLOATS = 8 + 8 * dq::QROWS + 4 * dq::QROWS + 6 * dq::QROWS + 4 * dq::QROWS;
   static constexpr int TAIL = 512 + 64 + NGRP * GRP_FLOATS * 4 + dq::QROWS * 4;
   static constexpr int BUDGET = 227 * 1024 - 1024 - OFF_C - TAIL;
   static constexpr int NC = BUDGET / STAGE < 8 ? BUDGET / STAGE : 8;   // code stages
@@ -120,7 +120,8 @@ struct DqShape {
   static constexpr int NBAR = 1 + 3 * NC + dq::NKT + dq::NS + dq::NPB + NGRP + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base, abort flag, last-CTA flag, final copies [NGRP]
   static constexpr int OFF_GRP = OFF_MISC + 32;         // [NGRP] groups of GRP_FLOATS words
-  static constexpr int G_FLAG = 0, G_RED = 8, G_SUM = 8 + 8 * dq::QROWS, G_REF = 8 + 12 * dq::QROWS;
+  static constexpr int G_FLAG = 0, G_RED = 8, G_SUM = 8 + 8 * dq::QROWS, G_REF = 8 + 12 * dq::QROWS,
+                       G_WSUM = 8 + 18 * dq::QROWS;   // [4][QROWS] sums of the O weights
   static constexpr int OFF_QS = OFF_GRP + NGRP * GRP_FLOATS * 4;   // [QROWS] float
   static constexpr int SMEM_USED = OFF_QS + dq::QROWS * 4;
   static constexpr int SMEM = SMEM_USED + 1024;
@@ -181,6 +182,41 @@ __device__ __forceinline__ void widen_chunk(const uint4& cw, uint32_t* w) {
     for (int t = 0; t < 4; ++t) {
       const uint4 h = widen_i4x8(v[t], false);
       w[4 * t] = h.x; w[4 * t + 1] = h.y; w[4 * t + 2] = h.z; w[4 * t + 3] = h.w;
+    }
+  }
+}
+
+// V codes widened with a constant offset: INT8 code c -> f16 1152 + c (the
+// byte c + 128 under the f16 bits 0x6400), INT4 code c -> 1032 + c, both
+// exact and one subtraction per pair cheaper than the exact widening; FP8
+// codes are widened exactly (offset 0), and so are all codes for more than
+// 16 query vectors (whose registers the weight sums would cost).  The offset
+// is taken back out of O^T at the end with the sum of the O weights (Vᵀ Pᵀ
+// holds offset * that sum).
+template <int KQ, int QVP>
+constexpr float v_offset() { return QVP > 16 ? 0.f : KQ == 1 ? 1152.f : KQ == 2 ? 1032.f : 0.f; }
+template <int KQ, int QVP>
+__device__ __forceinline__ void widen_chunk_off(const uint4& cw, uint32_t* w) {
+  if constexpr (v_offset<KQ, QVP>() == 0.f) {
+    widen_chunk<KQ>(cw, w);
+  } else if constexpr (KQ == 1) {
+    const uint32_t v[4] = {cw.x ^ 0x80808080u, cw.y ^ 0x80808080u, cw.z ^ 0x80808080u, cw.w ^ 0x80808080u};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      w[2 * t] = __byte_perm(v[t], 0x64646464u, 0x4140u);
+      w[2 * t + 1] = __byte_perm(v[t], 0x64646464u, 0x4342u);
+    }
+  } else if constexpr (KQ == 2) {
+    const uint32_t v[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t x = v[t] ^ 0x88888888u;
+      const uint32_t even = x & 0x0F0F0F0Fu, odd = (x >> 4) & 0x0F0F0F0Fu;   // elements 0,2,4,6 / 1,3,5,7
+      const uint32_t p0 = __byte_perm(even, odd, 0x5140u), p1 = __byte_perm(even, odd, 0x7362u);
+      w[4 * t] = __byte_perm(p0, 0x64646464u, 0x4140u);
+      w[4 * t + 1] = __byte_perm(p0, 0x64646464u, 0x4342u);
+      w[4 * t + 2] = __byte_perm(p1, 0x64646464u, 0x4140u);
+      w[4 * t + 3] = __byte_perm(p1, 0x64646464u, 0x4342u);
     }
   }
 }
@@ -547,9 +583,14 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
       ++ph;
       return r;
     };
-    float l[QVP];
+    // l: this thread's partial row sums; wsum: its partial sums of the f16 O
+    // weights, which take the V offset back out of O^T at the end
+    float l[QVP], wsum[QVP];
 #pragma unroll
-    for (int q = 0; q < QVP; ++q) l[q] = 0.f;
+    for (int q = 0; q < QVP; ++q) {
+      l[q] = 0.f;
+      wsum[q] = 0.f;
+    }
     // the logit scales qs[] are read from shared memory once q_full has completed
     if (T > grp && !__all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, wait_ns))) ok = false;
     // this group's tiles are grp, grp + NGRP, ...; this key's list entries three
@@ -612,7 +653,7 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
         for (int a = 0; a < 2; ++a) {
           uint32_t w[32];
 #pragma unroll
-          for (int ch = 0; ch < HC; ++ch) widen_chunk<KQ>(a ? cb[ch] : ca[ch], w + ch * Sh::WPC);
+          for (int ch = 0; ch < HC; ++ch) widen_chunk_off<KQ, QVP>(a ? cb[ch] : ca[ch], w + ch * Sh::WPC);
 #pragma unroll
           for (int t = 0; t < 8; ++t)
             *reinterpret_cast<uint4*>(stg + a * Sh::VATOM + k * 128 + ((t ^ (k & 7)) << 4)) =
@@ -684,6 +725,7 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
             no = mto;
             any_scale = true;
           }
+          if constexpr (v_offset<KQ, QVP>() != 0.f) wsum[q] *= alpha[q];
           if (wq == 0 && lane == q) {
             nref[q] = nl;
             nref[QROWS + q] = no;
@@ -730,9 +772,11 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
       for (int q = 0; q < QVP; ++q) {
         const float pq = x[q] == NEG_INF ? 0.f : fast_ex2(x[q] - mlc[q]);
         l[q] += pq;
-        if (q < QV)
-          *reinterpret_cast<__half*>(Pb + q * 128 + ((((k & 63) >> 3) ^ (q & 7)) << 4)) =
-              __float2half_rn(pq * (sv * cw[q]));
+        if (q < QV) {
+          const __half wq = __float2half_rn(pq * (sv * cw[q]));
+          if constexpr (v_offset<KQ, QVP>() != 0.f) wsum[q] += __half2float(wq);
+          *reinterpret_cast<__half*>(Pb + q * 128 + ((((k & 63) >> 3) ^ (q & 7)) << 4)) = wq;
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -747,6 +791,12 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0) rsum[wq * QROWS + q] = v;
+      if constexpr (v_offset<KQ, QVP>() != 0.f) {
+        float u = wsum[q];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+        if (lane == 0) gw[Sh::G_WSUM + wq * QROWS + q] = u;
+      }
     }
     if (wq == 0 && lane == 0) final_copy[grp] = rp;
     named_barrier(1, NGRP * 4 * 32);   // the softmax warps; every wait before it is bounded
@@ -775,7 +825,15 @@ __global__ void __maxnreg__((DqShape<QVP, KQ>::MAXREG))
 #pragma unroll
         for (int q = 0; q < QVP; ++q) {
           const float mo = fr[QROWS + q];
-          if (mq[q] != NEG_INF && mo != NEG_INF) ov[q] += __uint_as_float(o[q]) * exp2f(mo - mq[q]);
+          if (mq[q] != NEG_INF && mo != NEG_INF) {
+            // the V offset out: O^T holds sum w (offset + v) over the group's keys
+            float oq = __uint_as_float(o[q]);
+            if constexpr (v_offset<KQ, QVP>() != 0.f) {
+              const float* ws = grp_words(gi) + Sh::G_WSUM + q;
+              oq -= v_offset<KQ, QVP>() * (ws[0] + ws[QROWS] + ws[2 * QROWS] + ws[3 * QROWS]);
+            }
+            ov[q] += oq * exp2f(mo - mq[q]);
+          }
         }
       }
 #pragma unroll
