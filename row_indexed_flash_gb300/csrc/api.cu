@@ -113,6 +113,7 @@ struct DecodePlan {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kMaxSplits = far::kDecodeMaxSplits;
+constexpr long long kMergeMaxFloats = 32 * 1024;   // partial floats one merging CTA reads, at most (16-bit tc decode)
 
 // The prefill workspace is the status block alone.
 constexpr size_t kPrefillWorkspace = far::kStatusBytes;
@@ -196,6 +197,21 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
     if (cost < best - 1e-9) {
       best = cost;
       best_ns = (int)ns_eff;
+    }
+  }
+  // The last CTA of a (slice, KV head) merges ns * QV * D fp32 partials with
+  // a few loads in flight per thread; when each CTA streams only a few tiles,
+  // past 32K floats (128 KB) those load rounds outlast what a finer split
+  // saves (measured on the sparse D 256 workload: 32 splits of one tile
+  // 13.7 us in the kernel, 16 splits of two tiles 11.4 us).
+  if (pl->tc && !pl->tcq) {
+    const long long per_split = qv1 * (long long)a->D;
+    while (best_ns > 1 && best_ns * per_split > kMergeMaxFloats &&
+           round_up((L + best_ns - 1) / best_ns, align) <= 4 * (size_t)align) {
+      const int ns_next = (best_ns + 1) / 2;
+      const long long chunk_next = round_up((L + ns_next - 1) / ns_next, align);
+      if (chunk_next > chunk_max) break;
+      best_ns = (int)((L + chunk_next - 1) / chunk_next);
     }
   }
   pl->chunk = (int)round_up((L + best_ns - 1) / best_ns, align);
