@@ -332,6 +332,16 @@ def cpu_leg(p, workload: str, procs: int, min_seconds: float):
 # clocks during the timed region
 
 
+def queue_ahead(torch, steps: int, host_us_per_step: float = 60.0) -> None:
+    """Holds the stream on a device-side sleep long enough for the host to
+    enqueue every timed step behind it, so that the timed region measures the
+    GPU running the steps back to back rather than the host's launch rate (a
+    step of a few microseconds is otherwise timed at the Python loop's pace).
+    The sleep ends before the first timing event, outside the timed region."""
+    seconds = min(20e-3, 0.5e-3 + steps * host_us_per_step * 1e-6)
+    torch.cuda._sleep(int(seconds * 2.1e9))
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -432,7 +442,7 @@ def kernel_kind(workload: str) -> str:
 
 def measure(args, rank, world, p, workload, cpu_baseline):
     """Times one workload on this rank's GPU: warm-up, then args.steps steps
-    (replayed CUDA graphs of the step's launches) with CUDA events on the
+    (one replayed CUDA graph holding the steps' launches) with CUDA events on the
     launching stream, clocks sampled meanwhile; then the same call end to end
     with host inputs.  Returns the result dict on rank 0."""
     import ctypes
@@ -515,50 +525,47 @@ def measure(args, rank, world, p, workload, cpu_baseline):
         step(i)
     torch.cuda.synchronize(dev)
 
-    # Each step's launches are captured once per pool copy in a CUDA graph
-    # and replayed: the small workloads are otherwise bound by host launch
-    # time.  The captured kernels and arguments are exactly those of step(i).
-    graphs = None
+    # The K timed steps are captured, in order, into one CUDA graph that is
+    # replayed once: a graph per step, or a launch per kernel from Python,
+    # leaves gaps of several microseconds between the small steps on the
+    # device.  The captured kernels and arguments are exactly those of step(i).
+    graph = None
     if not args.no_graph:
         try:
-            graphs = []
-            for i in range(len(a_list)):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(args.steps):
                     step(i, torch.cuda.current_stream(dev).cuda_stream)
-                graphs.append(g)
-            for g in graphs:
-                g.replay()
+            graph.replay()   # untimed: the first replay uploads the graph
             torch.cuda.synchronize(dev)
         except Exception as exc:   # fall back to direct launches
             print(f"# CUDA graph capture failed ({exc}); timing direct launches", file=sys.stderr)
-            graphs = None
+            graph = None
 
-    def timed_step(i):
-        if graphs is not None:
-            graphs[i % len(graphs)].replay()
+    def timed_steps():
+        if graph is not None:
+            graph.replay()
         else:
-            step(i)
+            for i in range(args.steps):
+                step(i)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        queue_ahead(torch, args.steps)
         t0.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            timed_step(i)
-            ev[i][1].record(stream)
+        timed_steps()
         t1.record(stream)
         torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
-    mean_launch_ms = sum(launch_ms) / len(launch_ms)
+    # one event pair over the whole region: events between the steps would
+    # each add a device-side gap of about a microsecond to the small steps
+    mean_launch_ms = total_ms / args.steps
     # a wait that ran out would have made every number above meaningless
     if far.fa_rows_status(ws, clear=True) & far.FA_WS_WAIT_EXPIRED:
         raise SystemExit(f"{workload}: a pipeline wait ran out during the timed steps")
@@ -612,8 +619,8 @@ def measure(args, rank, world, p, workload, cpu_baseline):
     step_ms = total_ms / args.steps
     if world > 1:
         step_ms, e2e_ms, mean_launch_ms = max_over_ranks([step_ms, e2e_ms, mean_launch_ms], dist, dev)
-    launch_mode = "cuda_graph" if graphs is not None else "direct"
-    del graphs, pools, a_list, base, pinned, dbuf
+    launch_mode = "cuda_graph of the K timed steps" if graph is not None else "direct"
+    del graph, pools, a_list, base, pinned, dbuf
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
     if rank != 0:
@@ -655,6 +662,7 @@ def measure(args, rank, world, p, workload, cpu_baseline):
                    if not is_prefill else f"inputs larger than L2: pool {pool_bytes / 1e9:.2f} GB"),
             "parallelism": f"replicas x{world}",
             "launch": launch_mode,
+            "queue": "timed steps enqueued behind a device sleep: host launch time is not timed",
         },
         "roofline": {
             "bound": bound,
@@ -758,42 +766,38 @@ def run_append(args, rank, world, cpu_baseline):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
-    graphs = None
+    # the K timed steps captured, in order, into one CUDA graph (see measure)
+    graph = None
     if not args.no_graph:
         try:
-            graphs = []
-            for i in range(n_copies):
-                gr = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gr):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(args.steps):
                     step(i, torch.cuda.current_stream(dev).cuda_stream)
-                graphs.append(gr)
-            for gr in graphs:
-                gr.replay()
+            graph.replay()   # untimed: the first replay uploads the graph
             torch.cuda.synchronize(dev)
         except Exception as exc:
             print(f"# CUDA graph capture failed ({exc}); timing direct launches", file=sys.stderr)
-            graphs = None
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+            graph = None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        queue_ahead(torch, args.steps)
         t0.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            if graphs is not None:
-                graphs[i % n_copies].replay()
-            else:
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
                 step(i)
-            ev[i][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     step_ms = t0.elapsed_time(t1) / args.steps
-    launch_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    launch_ms = step_ms   # one launch per step, timed over the whole region
 
     # end to end: the ubatch and its destinations copied in from pinned host
     # memory, the call, and the written codes and scales copied back
@@ -853,7 +857,8 @@ def run_append(args, rank, world, cpu_baseline):
             "l2": f"inputs larger than L2: {n_copies} ubatch copies of {x_bytes / 1e6:.1f} MB rotated, "
                   f"each to its own pages",
             "parallelism": f"replicas x{world}",
-            "launch": "cuda_graph" if graphs is not None else "direct",
+            "launch": "cuda_graph of the K timed steps" if graph is not None else "direct",
+            "queue": "timed steps enqueued behind a device sleep: host launch time is not timed",
         },
         "roofline": {
             "bound": "hbm",

@@ -224,7 +224,8 @@ fa_status fa_kv_page_table_to_rows(const int32_t* page_table, int32_t max_pages,
  * q = clamp(rint_half_even(x/s), -127, 127) with x/s one fp32 division;
  * s = 0 gives q = 0.
  *   x        [n_rows, Hkv, D] FA_F16 or FA_BF16 (x_dtype)
- *   dst_rows [n_rows] int32 pool rows to write, negative = skip; NULL = row i
+ *   dst_rows [n_rows] int32 pool rows to write, negative or >= R = skip;
+ *            NULL = row i
  *   q        [R, Hkv, D] int8 pool; scale the fp16 layout of fa_rows_args.
  * This is also the KV append of a ubatch into an INT8 pool.
  */

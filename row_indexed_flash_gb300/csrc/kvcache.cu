@@ -5,6 +5,7 @@
 // 1-2.  Negative row = padding: "llama.cpp 0.9.0 inference boundaries",
 // section 1.
 #include <cuda_fp8.h>
+#include <atomic>
 #include <limits.h>
 
 #include "fa_internal.cuh"
@@ -111,92 +112,299 @@ __global__ void quantize_int8_kernel(const uint16_t* __restrict__ x, int x_bf16,
   }
 }
 
-// The same rule for D = 32 * EPL (64, 128, 256) with 16-byte aligned x and q:
-// lane l holds elements EPL*l .. EPL*l + EPL - 1, loaded and stored with one
-// vector access each, and the row's values are loaded together with its
-// destination index rather than after it.
-template <int EPL>
-__global__ void quantize_int8_vec_kernel(const uint16_t* __restrict__ x, int x_bf16, long long n_rows, int Hkv,
-                                         const int32_t* __restrict__ dst_rows, int8_t* __restrict__ q,
-                                         uint16_t* __restrict__ scale, long long R) {
-  constexpr int D = 32 * EPL;
-  const int lane = threadIdx.x & 31;
-  const long long warps = (long long)gridDim.x * (blockDim.x / 32);
-  for (long long w = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5); w < n_rows * Hkv; w += warps) {
-    const long long i = w / Hkv;
-    const int g = (int)(w % Hkv);
-    const uint16_t* src = x + (size_t)w * D + lane * EPL;
-    uint32_t raw[EPL / 2];
-    if constexpr (EPL == 2) {
-      raw[0] = __ldg(reinterpret_cast<const unsigned int*>(src));
-    } else if constexpr (EPL == 4) {
-      const uint2 t = __ldg(reinterpret_cast<const uint2*>(src));
-      raw[0] = t.x;
-      raw[1] = t.y;
-    } else {
-      const uint4 t = __ldg(reinterpret_cast<const uint4*>(src));
-      raw[0] = t.x;
-      raw[1] = t.y;
-      raw[2] = t.z;
-      raw[3] = t.w;
+// x / s rounded to nearest (even) in fp32, for x a bf16 or fp16 value widened
+// to fp32, s a positive finite fp16 scale (or one of the codec tops) and r an
+// approximation of 1/s within a relative 2^-20: one multiply and two fused
+// multiply-adds in place of a division, after the quotient correction of
+// P. Markstein ("IA-64 and Elementary Functions", 2000).  q0 = RN(x*r) lies
+// within 5 ulp of x/s, so the residual x - q0*s is exact in one fma, and the
+// exact q0 + (x - q0*s)*r equals x/s + (x/s - q0)*(s*r - 1): within
+// 5 * 2^-20 ulp of x/s.  Rounding it gives RN(x/s) unless a midpoint of the
+// fp32 grid lies that close.  It cannot: writing x = mx*2^a, s = ms*2^b with
+// mx, ms < 2^11 integers and x/s in [2^e, 2^(e+1)), a - b >= e - 24, so
+// |x/s - M| for a midpoint M = odd * 2^(e-24) is a multiple of 2^(e-24)
+// divided by ms: zero or at least 2^-12 ulp; and zero would make x/s a dyadic
+// number of at most 11 bits equal to a 25-bit one.  The caller handles an
+// infinite x (the residual is NaN; x/s is that infinity).  A zero x gives +0
+// (the sum drops the sign of -0).  A quotient small enough for the residual to
+// underflow is below 2^-76 and codes as a zero either way.
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  return __fmaf_rn(__fmaf_rn(-q0, s, x), r, q0);
+}
+
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));   // within 1 ulp; s is a normal fp32 here
+  return r;
+}
+
+// The per-row codecs for D = 64, 128, 256 with 16-byte aligned x and q, one
+// kernel for all three.  A (row, head) item spans D / 16 lanes, each coding
+// 16 elements: the 8 at 8 * part and the 8 at D/2 + 8 * part, so that every
+// load and every code store is contiguous across the item's lanes.  Each warp
+// streams its own tiles (32 / (D / 16) consecutive items, 1 KB) through
+// shared memory with cp.async, kQuantStages tiles ahead, and each lane copies
+// exactly the pieces and the destination index that it later reads: no
+// barrier, no register held by a load in flight, and a small ubatch is
+// requested whole at the start.  Same results as the one-warp-per-item
+// kernels, with cheaper steps:
+// * amax and the NaN test from the 16-bit patterns: with the sign bit
+//   cleared, bf16 and fp16 values order as their magnitudes do, +Inf above
+//   every finite value, and the NaN-propagating packed max gives the canonical
+//   NaN (above +Inf) when any element is NaN;
+// * the divisions by div_by_scale (the scale's with RN(1/top), the codes'
+//   with an approximate reciprocal of s);
+// * the integer codes by adding 1.5 * 2^23 to the quotient: in [2^23, 2^24)
+//   the fp32 grid step is 1, so the sum's rounding is the round half to even
+//   of the quotient and its low byte is the two's-complement code.  The clamp
+//   to +-top is needed only for a subnormal or saturated scale: otherwise
+//   s >= (amax / top)(1 - 2^-11)(1 - 2^-24), so |x / s| < top + 1/2;
+// * item -> (row, head) by stepping both, since a warp's tiles are a fixed
+//   stride apart.
+enum { kCodecInt8 = 0, kCodecInt4 = 1, kCodecFp8 = 2 };
+
+// Lane-wise max of two bf16x2 (or f16x2) words of non-negative values, any NaN
+// giving the canonical NaN (0x7fff, above +Inf in either format).
+template <bool BF16>
+__device__ __forceinline__ uint32_t hmax2_nan_bits(uint32_t a, uint32_t b) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  } else {
+    const __half2 r = __hmax2_nan(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+// Codes of 16 quotients (8 of the first half row, 8 of the second) packed for
+// the two stores: integer codes from the low bits of q + 1.5 * 2^23 (q already
+// within +-top), E4M3 codes by the saturating conversion with the zero's sign
+// taken from the element.
+template <int CODEC>
+__device__ __forceinline__ void encode_codes(const float (&qv)[16], const float (&vals)[16], uint32_t (&packed)[4]) {
+  constexpr float ROUNDER = 12582912.0f;   // 1.5 * 2^23
+  if constexpr (CODEC == kCodecFp8) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+          make_float2(copysignf(qv[4 * j], vals[4 * j]), copysignf(qv[4 * j + 1], vals[4 * j + 1])), __NV_SATFINITE,
+          __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+          make_float2(copysignf(qv[4 * j + 2], vals[4 * j + 2]), copysignf(qv[4 * j + 3], vals[4 * j + 3])),
+          __NV_SATFINITE, __NV_E4M3);
+      packed[j] = __byte_perm(lo, hi, 0x5410);
     }
-    const long long dst = dst_rows ? (long long)__ldg(dst_rows + i) : i;
-    float vals[EPL];
-    float amax = 0.f;
-    bool nan = false;
+  } else {
+    uint32_t c[16];
 #pragma unroll
-    for (int k = 0; k < EPL / 2; ++k) {
+    for (int e = 0; e < 16; ++e) c[e] = __float_as_uint(qv[e] + ROUNDER);
+    if constexpr (CODEC == kCodecInt4) {
+      uint32_t b[8];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint32_t b = e ? (raw[k] >> 16) : (raw[k] & 0xffffu);
-        const float f = x_bf16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
-        vals[2 * k + e] = f;
-        amax = fmaxf(amax, fabsf(f));   // fmaxf skips NaN: tracked separately
-        nan |= f != f;
+      for (int j = 0; j < 8; ++j) b[j] = (c[2 * j] & 0xfu) | ((c[2 * j + 1] << 4) & 0xf0u);
+      packed[0] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+      packed[1] = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+      packed[2] = packed[3] = 0u;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        packed[j] = __byte_perm(__byte_perm(c[4 * j], c[4 * j + 1], 0x0040),
+                                __byte_perm(c[4 * j + 2], c[4 * j + 3], 0x0040), 0x5410);
+    }
+  }
+}
+constexpr int kQuantStages = 8;   // tiles in flight per warp
+
+template <int CODEC, int D, bool BF16>
+__global__ void __launch_bounds__(256, 3) quantize_rows_staged_kernel(const uint4* __restrict__ x, int n_items,
+                                                                      int Hkv, int rows_step, int heads_step,
+                                                                      const int32_t* __restrict__ dst_rows,
+                                                                      uint8_t* __restrict__ q,
+                                                                      uint16_t* __restrict__ scale, int R) {
+  constexpr int LPI = D / 16;                      // lanes per item
+  constexpr int IPW = 32 / LPI;                    // items per tile
+  constexpr int IC = 2 * D / 16;                   // 16-byte pieces per item
+  constexpr int S = kQuantStages;
+  constexpr int QROW = CODEC == kCodecInt4 ? D / 2 : D;
+  constexpr float TOP = CODEC == kCodecInt8 ? 127.0f : CODEC == kCodecInt4 ? 7.0f : 448.0f;
+  constexpr float RTOP = 1.0f / TOP;              // RN(1/top), folded by the compiler
+  constexpr uint32_t INF_BITS = BF16 ? 0x7f80u : 0x7c00u;
+  extern __shared__ uint4 smem[];                 // per warp: S tiles of 64 pieces, then S x 32 indices
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / LPI, part = lane % LPI;
+  uint4* wtiles = smem + (size_t)warp * S * 64;
+  int32_t* widx = reinterpret_cast<int32_t*>(smem + (size_t)(blockDim.x / 32) * S * 64) + warp * S * 32;
+  const int gw = blockIdx.x * (blockDim.x / 32) + warp;
+  const int item_step = gridDim.x * (blockDim.x / 32) * IPW;   // = rows_step * Hkv + heads_step
+
+  // the lane's item in the tile being issued and in the tile being coded, with
+  // its row and head, stepped by item_step each tile
+  int it_i = gw * IPW + sub, row_i = (int)((unsigned)it_i / (unsigned)Hkv), head_i = it_i - row_i * Hkv;
+  int it_c = it_i, row_c = row_i, head_c = head_i;
+  auto advance = [&](int& it, int& row, int& head) {
+    it += item_step;
+    row += rows_step;
+    head += heads_step;
+    if (head >= Hkv) {
+      head -= Hkv;
+      ++row;
+    }
+  };
+  auto issue = [&](int slot) {
+    const bool ok = it_i < n_items;
+    const uint4* src = ok ? x + (size_t)it_i * IC + part : x;
+    cp_async16(wtiles + slot * 64 + lane, src, ok);
+    cp_async16(wtiles + slot * 64 + 32 + lane, ok ? src + LPI : x, ok);
+    if (dst_rows) cp_async4(widx + slot * 32 + lane, ok ? dst_rows + row_i : dst_rows, ok);
+    cp_async_commit();   // one group per tile, empty or not, so the wait count below holds
+    advance(it_i, row_i, head_i);
+  };
+#pragma unroll
+  for (int st = 0; st < S; ++st) issue(st);
+
+  for (int k = 0; it_c - sub < n_items; ++k) {   // warp-uniform: the tile's first item
+    const int slot = k % S;
+    cp_async_wait<S - 1>();                        // this lane's pieces of tile k have landed
+    const uint4 h0 = wtiles[slot * 64 + lane];
+    const uint4 h1 = wtiles[slot * 64 + 32 + lane];
+    const int d = it_c < n_items ? (dst_rows ? widx[slot * 32 + lane] : row_c) : -1;
+    const uint32_t w[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    uint32_t m2 = w[0] & 0x7fff7fffu;
+#pragma unroll
+    for (int j = 1; j < 8; ++j) m2 = hmax2_nan_bits<BF16>(m2, w[j] & 0x7fff7fffu);
+    uint32_t mag = max(m2 & 0xffffu, m2 >> 16);
+#pragma unroll
+    for (int o = LPI / 2; o >= 1; o >>= 1) mag = max(mag, __shfl_xor_sync(0xffffffffu, mag, o));
+    const bool live = (unsigned)d < (unsigned)R;   // not padding, out of range or past the end
+    const bool has_nan = mag > INF_BITS;
+    const bool row_inf = mag == INF_BITS;
+    const float amax = BF16 ? __uint_as_float(mag << 16) : __half2float(__ushort_as_half((unsigned short)mag));
+    unsigned short sb;
+    if (has_nan) {
+      sb = 0x7E00u;
+    } else {
+      const float sq = row_inf ? amax : div_by_scale(amax, TOP, RTOP);
+      sb = __half_as_ushort(__float2half_rn(fminf(sq, 65504.0f)));
+    }
+    const float sf = __half2float(__ushort_as_half(sb));
+    // no NaN, no Inf, and a scale that needs no clamp (integer codecs) or is not zero
+    const bool plain =
+        !has_nan && !row_inf && (CODEC == kCodecFp8 ? sb != 0u : (sb >= 0x0400u && sb < 0x7bffu));
+    float vals[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if constexpr (BF16) {
+        vals[2 * j] = __uint_as_float(w[j] << 16);
+        vals[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+      } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+        vals[2 * j] = f.x;
+        vals[2 * j + 1] = f.y;
       }
     }
+    const float rs = rcp_approx(sf);
+    float qv[16];
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const bool has_nan = __any_sync(0xffffffffu, nan);
-    if (dst < 0 || dst >= R) continue;   // the same for every lane of the warp
-    const unsigned short sb = row_scale_bits(amax, has_nan, 127.0f);
-    const float sf = __half2float(__ushort_as_half(sb));
-    uint32_t packed[(EPL + 3) / 4] = {};
+    for (int e = 0; e < 16; ++e) qv[e] = div_by_scale(vals[e], sf, rs);
+    uint32_t packed[4];   // codes of the first half row, then of the second
+    if (__all_sync(0xffffffffu, plain || !live)) {
+      encode_codes<CODEC>(qv, vals, packed);
+    } else {   // some item of the warp holds a NaN or an Inf or has a subnormal, saturated or zero scale
+      if (row_inf) {
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      int c = 0;
-      if (sf != 0.f && !has_nan) c = min(max(__float2int_rn(__fdiv_rn(vals[e], sf)), -127), 127);
-      packed[e / 4] |= ((uint32_t)c & 0xffu) << (8 * (e % 4));
+        for (int e = 0; e < 16; ++e)
+          if (isinf(vals[e])) qv[e] = vals[e];
+      }
+      if constexpr (CODEC != kCodecFp8) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qv[e] = fminf(fmaxf(qv[e], -TOP), TOP);
+      }
+      encode_codes<CODEC>(qv, vals, packed);
+      const uint32_t fill = has_nan && CODEC == kCodecFp8 ? 0x7f7f7f7fu : 0u;
+      if (has_nan || sf == 0.f) packed[0] = packed[1] = packed[2] = packed[3] = fill;
     }
-    int8_t* qd = q + ((size_t)dst * Hkv + g) * D + lane * EPL;
-    if constexpr (EPL == 2) {
-      *reinterpret_cast<uint16_t*>(qd) = (uint16_t)packed[0];
-    } else if constexpr (EPL == 4) {
-      *reinterpret_cast<uint32_t*>(qd) = packed[0];
-    } else {
-      *reinterpret_cast<uint2*>(qd) = make_uint2(packed[0], packed[1]);
+    if (live) {
+      uint8_t* qrow = q + ((size_t)d * Hkv + head_c) * QROW;
+      if constexpr (CODEC == kCodecInt4) {
+        *reinterpret_cast<uint32_t*>(qrow + part * 4) = packed[0];
+        *reinterpret_cast<uint32_t*>(qrow + QROW / 2 + part * 4) = packed[1];
+      } else {
+        *reinterpret_cast<uint2*>(qrow + part * 8) = make_uint2(packed[0], packed[1]);
+        *reinterpret_cast<uint2*>(qrow + QROW / 2 + part * 8) = make_uint2(packed[2], packed[3]);
+      }
+      if (part == 0) scale[((size_t)((unsigned)d / kPage) * Hkv + head_c) * kPage + ((unsigned)d % kPage)] = sb;
     }
-    if (lane == 0) scale[((size_t)(dst / kPage) * Hkv + g) * kPage + (dst % kPage)] = sb;
+    issue(slot);   // h0, h1 and d are consumed above, so the slot is free again
+    advance(it_c, row_c, head_c);
   }
+  cp_async_wait<0>();
+}
+
+// Launches the staged kernel when D is 64, 128 or 256, x and q are 16-byte
+// aligned and the item count and pool rows fit an int; returns false (nothing
+// launched) otherwise.  Three blocks of 8 warps per SM (216 KB of stages), at
+// most one warp per tile.
+template <int CODEC, int D, bool BF16>
+void launch_quantize_staged(const uint4* x, int items, int Hkv, const int32_t* dst, uint8_t* q, uint16_t* scale,
+                            int R, cudaStream_t st) {
+  constexpr int smem = 8 * kQuantStages * (64 * 16 + 32 * 4);
+  static std::atomic<bool> attr_set{false};
+  if (!attr_set.load(std::memory_order_relaxed)) {
+    cudaFuncSetAttribute(quantize_rows_staged_kernel<CODEC, D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         smem);
+    attr_set.store(true, std::memory_order_relaxed);
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 1;
+  constexpr int IPW = 32 / (D / 16);
+  const int tiles = (items + IPW - 1) / IPW;
+  int blocks = (tiles + 7) / 8;
+  if (blocks > 3 * sms) blocks = 3 * sms;
+  const int item_step = blocks * 8 * IPW;
+  quantize_rows_staged_kernel<CODEC, D, BF16><<<blocks, 256, smem, st>>>(x, items, Hkv, item_step / Hkv,
+                                                                         item_step % Hkv, dst, q, scale, R);
+}
+
+template <int CODEC, bool BF16>
+bool launch_quantize_staged_d(const uint4* x, int items, int Hkv, int D, const int32_t* dst, uint8_t* q,
+                              uint16_t* scale, int R, cudaStream_t st) {
+  if (D == 64)
+    launch_quantize_staged<CODEC, 64, BF16>(x, items, Hkv, dst, q, scale, R, st);
+  else if (D == 128)
+    launch_quantize_staged<CODEC, 128, BF16>(x, items, Hkv, dst, q, scale, R, st);
+  else if (D == 256)
+    launch_quantize_staged<CODEC, 256, BF16>(x, items, Hkv, dst, q, scale, R, st);
+  else
+    return false;
+  return true;
+}
+
+template <int CODEC>
+bool launch_quantize_v8(const void* x, int x_bf16, long long n_rows, int Hkv, int D, const int32_t* dst, void* q,
+                        uint16_t* scale, long long R, cudaStream_t st) {
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(q) % 16 != 0) return false;
+  const long long items = n_rows * Hkv;
+  if (items >= (1LL << 30) || R >= (1LL << 31)) return false;
+  const uint4* xv = static_cast<const uint4*>(x);
+  uint8_t* qb = static_cast<uint8_t*>(q);
+  return x_bf16 ? launch_quantize_staged_d<CODEC, true>(xv, (int)items, Hkv, D, dst, qb, scale, (int)R, st)
+                : launch_quantize_staged_d<CODEC, false>(xv, (int)items, Hkv, D, dst, qb, scale, (int)R, st);
 }
 
 cudaError_t launch_quantize_int8(const void* x, int x_bf16, long long n_rows, int Hkv, int D, const int32_t* dst,
                                  int8_t* q, uint16_t* scale, long long R, cudaStream_t st) {
   const long long warps = n_rows * Hkv;
   if (warps == 0) return cudaSuccess;
+  if (launch_quantize_v8<kCodecInt8>(x, x_bf16, n_rows, Hkv, D, dst, q, scale, R, st)) return cudaGetLastError();
   const int threads = 256;
   long long blocks = (warps + 7) / 8;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  const uint16_t* xs = static_cast<const uint16_t*>(x);
-  const bool aligned16 = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (reinterpret_cast<uintptr_t>(q) % 16 == 0);
-  if (aligned16 && D == 64)
-    quantize_int8_vec_kernel<2><<<(unsigned)blocks, threads, 0, st>>>(xs, x_bf16, n_rows, Hkv, dst, q, scale, R);
-  else if (aligned16 && D == 128)
-    quantize_int8_vec_kernel<4><<<(unsigned)blocks, threads, 0, st>>>(xs, x_bf16, n_rows, Hkv, dst, q, scale, R);
-  else if (aligned16 && D == 256)
-    quantize_int8_vec_kernel<8><<<(unsigned)blocks, threads, 0, st>>>(xs, x_bf16, n_rows, Hkv, dst, q, scale, R);
-  else
-    quantize_int8_kernel<<<(unsigned)blocks, threads, 0, st>>>(xs, x_bf16, n_rows, Hkv, D, dst, q, scale, R);
+  quantize_int8_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint16_t*>(x), x_bf16, n_rows, Hkv, D,
+                                                             dst, q, scale, R);
   return cudaGetLastError();
 }
 
@@ -261,6 +469,7 @@ cudaError_t launch_quantize_int4(const void* x, int x_bf16, long long n_rows, in
   const int threads = 256;
   long long blocks = (warps + 7) / 8;
   if (blocks > 152 * 64) blocks = 152 * 64;
+  if (launch_quantize_v8<kCodecInt4>(x, x_bf16, n_rows, Hkv, D, dst, q, scale, R, st)) return cudaGetLastError();
   quantize_int4_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint16_t*>(x), x_bf16, n_rows, Hkv, D,
                                                              dst, q, scale, R);
   return cudaGetLastError();
@@ -348,6 +557,7 @@ cudaError_t launch_quantize_fp8(const void* x, int x_bf16, long long n_rows, int
   const int threads = 256;
   long long blocks = (warps + 7) / 8;
   if (blocks > 152 * 64) blocks = 152 * 64;
+  if (launch_quantize_v8<kCodecFp8>(x, x_bf16, n_rows, Hkv, D, dst, q, scale, R, st)) return cudaGetLastError();
   quantize_fp8_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint16_t*>(x), x_bf16, n_rows, Hkv, D,
                                                             dst, q, scale, R);
   return cudaGetLastError();

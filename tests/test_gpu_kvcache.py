@@ -95,6 +95,93 @@ def test_int8_append_scatters_into_named_rows():
     assert np.array_equal(s.cpu().numpy().view(np.uint16), so.view(np.uint16))
 
 
+@pytest.mark.parametrize("codec", ["int8", "int4", "fp8"])
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("bf16", 256)])
+def test_append_codecs_over_many_items_and_a_ragged_tail(codec, dtype, D):
+    """A ubatch large enough that each warp of the 16-byte-load quantiser
+    strides over several groups of items, with a ragged last group, rows named
+    out of order, skipped (-1) and out of range (>= R); then the same ubatch
+    from a source that is not 16-byte aligned (the one-warp-per-item path).
+    Codes and scales bit-exact against the oracle's, untouched rows zero."""
+    g = synth.rng(81 + D)
+    H = 8
+    n = {64: 21_003, 128: 12_003, 256: 6_007}[D]   # above 1,216 blocks x 8 warps x 4 loads of items
+    R = 64 * ((n + 200) // 64 + 1)
+    bits = synth.normal_bits(g, (n, H, D), dtype)
+    dst = g.permutation(R)[:n].astype(np.int32)
+    dst[::11] = -1
+    dst[5::13] = R + 5
+    quant, quant_o = {"int8": (far.fa_kv_quantize_int8, oracle.quantize_int8),
+                      "int4": (far.fa_kv_quantize_int4, oracle.quantize_int4),
+                      "fp8": (far.fa_kv_quantize_fp8, oracle.quantize_fp8)}[codec]
+    qo, so = quant_o(oracle.widen(bits, dtype).astype(np.float32))
+    live = (dst >= 0) & (dst < R)
+    flat = torch.zeros(n * H * D + 8, dtype=torch.int16, device="cuda")
+    for offset in (0, 1):
+        x = flat[offset:offset + n * H * D].view(n, H, D)
+        x.copy_(torch.from_numpy(bits.view(np.int16)).cuda())
+        q, s = quant(x.view(torch.bfloat16 if dtype == "bf16" else torch.float16), R,
+                     dst_rows=torch.from_numpy(dst).cuda())
+        qn = q.cpu().view(torch.uint8).numpy() if codec == "fp8" else q.cpu().numpy()
+        sn = oracle.unpack_scales(s.cpu().numpy()).view(np.uint16)
+        assert np.array_equal(qn[dst[live]].view(np.uint8), qo[live].view(np.uint8))
+        assert np.array_equal(sn[dst[live]], so[live].view(np.uint16))
+        untouched = np.setdiff1d(np.arange(R), dst[live])
+        assert not qn[untouched].any() and not sn[untouched].any()
+
+
+def _e4m3_positive_values():
+    """The finite positive E4M3 values, ascending (bias 7, 3 mantissa bits,
+    largest 448): the grid whose midpoints the FP8 tie case uses."""
+    sub = [m * 2.0 ** -9 for m in range(1, 8)]
+    norm = [(1 + m / 8) * 2.0 ** e for e in range(-6, 9) for m in range(8)]
+    return np.array(sorted(v for v in sub + norm if v <= 448.0))
+
+
+@pytest.mark.parametrize("codec,dtype", [("int8", "f16"), ("int4", "bf16"), ("fp8", "bf16")])
+def test_quantisers_round_exact_ties_to_even(codec, dtype):
+    """Rows whose scale is 0.09375 (3 * 2^-5, no exact reciprocal) and whose
+    other elements make x / s an exact tie: k + 1/2 for the integer codecs, a
+    midpoint of the E4M3 grid for FP8.  The codes must round those ties to
+    even, bit-exact against the oracle; for INT8 and INT4 also against the
+    closed form (k if k is even, else k + 1, with the element's sign).  A few
+    elements are -0 and +0, which E4M3 codes apart."""
+    s_val = 0.09375
+    top = {"int8": 127, "int4": 7, "fp8": 448}[codec]
+    if codec == "fp8":
+        grid = _e4m3_positive_values()
+        q_tie = ((grid[:-1] + grid[1:]) / 2)[-127:]          # 127 midpoints, up to just below 448
+    else:
+        q_tie = np.arange(top) + 0.5                         # 0.5 .. top - 0.5
+    g = synth.rng(83)
+    n, H, D = 64, 2, 128
+    vals = np.empty((n, H, D))
+    vals[:, :, 0] = top * s_val                              # amax: s = fp16(amax / top) = 0.09375 exactly
+    picks = g.integers(0, q_tie.size, size=(n, H, D - 1))
+    signs = np.where(g.random((n, H, D - 1)) < 0.5, -1.0, 1.0)
+    vals[:, :, 1:] = signs * q_tie[picks] * s_val
+    vals[::3, :, 1], vals[::3, :, 2] = -0.0, 0.0              # signed zeros (E4M3 codes them 0x80 and 0x00)
+    wide = vals.astype(np.float32)
+    assert np.array_equal(wide.astype(np.float64), vals)     # every value is exact in fp32
+    bits = synth.f32_to_bf16_bits(wide) if dtype == "bf16" else synth.f32_to_f16_bits(wide)
+    assert np.array_equal(oracle.widen(bits, dtype).astype(np.float64), vals)   # and in the input type
+    quant, quant_o = {"int8": (far.fa_kv_quantize_int8, oracle.quantize_int8),
+                      "int4": (far.fa_kv_quantize_int4, oracle.quantize_int4),
+                      "fp8": (far.fa_kv_quantize_fp8, oracle.quantize_fp8)}[codec]
+    q, s = quant(dev_bits(bits, dtype), n)
+    qo, so = quant_o(oracle.widen(bits, dtype).astype(np.float32))
+    assert np.all(so.astype(np.float64) == s_val)
+    got = q.cpu().view(torch.uint8).numpy() if codec == "fp8" else q.cpu().numpy()
+    assert np.array_equal(got.view(np.uint8), qo.view(np.uint8))
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), oracle.pack_scales(so).view(np.uint16))
+    if codec != "fp8":
+        k = np.floor(q_tie[picks]).astype(np.int64)
+        want = (signs * np.where(k % 2 == 0, k, k + 1)).astype(np.int64)
+        want[::3, :, :2] = 0
+        codes = oracle.dequantize_int8(qo, so) if codec == "int8" else oracle.dequantize_int4(qo, so)
+        assert np.array_equal(np.rint(codes[:, :, 1:] / s_val).astype(np.int64), want)
+
+
 def test_append_16bit_rows():
     g = synth.rng(79)
     R, H, D, n = 300, 8, 128, 50
