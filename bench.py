@@ -64,9 +64,10 @@ KERNEL_SOURCES = {
                  "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
     "prefill": ["row_indexed_flash_gb300/csrc/prefill.cu", "row_indexed_flash_gb300/csrc/tc.cuh",
                 "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
+    "append": ["row_indexed_flash_gb300/csrc/kvcache.cu", "row_indexed_flash_gb300/csrc/fa_internal.cuh"],
 }
 KERNEL_NAMES = {"decode": "fa_rows_decode_tc_kernel", "prefill": "fa_rows_prefill_kernel",
-                "decode_q": "fa_rows_decode_tcq_kernel"}
+                "decode_q": "fa_rows_decode_tcq_kernel", "append": "quantize_rows_staged_kernel"}
 PROFILE_FILES = {
     "decode_bf16": "profiles/decode_bf16_4x16384_ncu.txt",
     "prefill_bf16": "profiles/prefill_bf16_4x2048x99936_ncu.txt",
@@ -74,6 +75,7 @@ PROFILE_FILES = {
     "prefill_bf16_small": "profiles/prefill_bf16_4x2048x16384_ncu.txt",
     "paged_int8": "profiles/paged_int8_32seq_ncu.txt",
     "paged_int8_small": "profiles/paged_int8_16seq_ncu.txt",
+    "kv_append_int8": "profiles/kv_append_int8_4x2048_ncu.txt",
 }
 
 
@@ -867,8 +869,8 @@ def run_append(args, rank, world, cpu_baseline):
             "peak_source": pk_src,
             "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4),
-            "traffic": None,
-            "kernel": "quantize_int8_kernel",
+            "traffic": profiled_traffic("kv_append_int8", "append"),
+            "kernel": KERNEL_NAMES["append"],
             "kernel_ms": round(launch_ms, 5),
             "work_per_launch": work,
         },
