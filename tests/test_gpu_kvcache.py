@@ -96,16 +96,18 @@ def test_int8_append_scatters_into_named_rows():
 
 
 @pytest.mark.parametrize("codec", ["int8", "int4", "fp8"])
-@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f16", 128), ("bf16", 256)])
-def test_append_codecs_over_many_items_and_a_ragged_tail(codec, dtype, D):
-    """A ubatch large enough that each warp of the 16-byte-load quantiser
-    strides over several groups of items, with a ragged last group, rows named
-    out of order, skipped (-1) and out of range (>= R); then the same ubatch
-    from a source that is not 16-byte aligned (the one-warp-per-item path).
-    Codes and scales bit-exact against the oracle's, untouched rows zero."""
-    g = synth.rng(81 + D)
-    H = 8
-    n = {64: 21_003, 128: 12_003, 256: 6_007}[D]   # above 1,216 blocks x 8 warps x 4 loads of items
+@pytest.mark.parametrize("dtype,D,H", [("bf16", 64, 8), ("f16", 128, 8), ("bf16", 256, 8), ("bf16", 128, 3)])
+def test_append_codecs_over_many_items_and_a_ragged_tail(codec, dtype, D, H):
+    """A ubatch large enough that each warp of the staged quantiser strides
+    over several of its tiles (the grid holds 4 blocks x 8 warps per SM), with
+    a ragged last tile, rows named out of order, skipped (-1) and out of range
+    (>= R); with 3 KV heads the warps' item stride is not a multiple of the
+    head count, so the stepped (row, head) of an item carries.  Then the same
+    ubatch from a source that is not 16-byte aligned (the
+    one-warp-per-item path).  Codes and scales bit-exact against the oracle's,
+    untouched rows zero."""
+    g = synth.rng(81 + D + H)
+    n = {64: 21_003, 128: 12_003, 256: 6_007}[D] * (2 if H == 3 else 1)
     R = 64 * ((n + 200) // 64 + 1)
     bits = synth.normal_bits(g, (n, H, D), dtype)
     dst = g.permutation(R)[:n].astype(np.int32)
