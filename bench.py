@@ -521,7 +521,9 @@ def measure(args, rank, world, p, workload, cpu_baseline):
 
     # a bf16 prefill is three kernels: the V-range scan, then the two prefill
     # modes (V to f16, V kept in bf16), one of which exits at once
-    launches_per_step = 1 + (1 if paged else 0) + (8 if select else 0) + (2 if is_prefill and p.dtype == "bf16" else 0)
+    # a decode whose splits are merged by a kernel of their own is two
+    launches_per_step = ((1 if is_prefill else lib.fa_rows_decode_launches(ctypes.byref(a_list[0])))
+                         + (1 if paged else 0) + (8 if select else 0) + (2 if is_prefill and p.dtype == "bf16" else 0))
 
     for i in range(args.warmup):
         step(i)

@@ -136,6 +136,15 @@ size_t fa_rows_workspace_size(const fa_rows_args* a, int is_prefill);
 fa_status fa_rows_workspace_init(void* ws, size_t ws_bytes, fa_stream_t stream);
 
 /*
+ * Kernel launches one fa_rows_decode call with these arguments makes: 1, or 2
+ * when the plan merges the list's splits in a kernel of its own (a
+ * latency-bound 16-bit decode: one wave of CTAs, each over at most four
+ * tiles), 0 when there is nothing to do; -1 (and fa_last_error()) on invalid
+ * arguments.  Host-only: no device work, no stream.
+ */
+int fa_rows_decode_launches(const fa_rows_args* a);
+
+/*
  * Enqueues on `stream` a copy of the workspace's status word into *d_status
  * (a device uint32) and, if `clear` is non-zero, then zeroes the word.  The
  * caller reads d_status once the stream has reached this point; a non-zero

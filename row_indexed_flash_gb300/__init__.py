@@ -68,6 +68,7 @@ _lib_lock = threading.Lock()
 _P = ctypes.c_void_p
 _SIGS = {
     "fa_rows_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(fa_rows_args), ctypes.c_int]),
+    "fa_rows_decode_launches": (ctypes.c_int, [ctypes.POINTER(fa_rows_args)]),
     "fa_rows_workspace_init": (ctypes.c_int, [_P, ctypes.c_size_t, _P]),
     "fa_rows_status": (ctypes.c_int, [_P, ctypes.c_size_t, _P, ctypes.c_int, _P]),
     "fa_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),

@@ -106,6 +106,7 @@ struct DecodePlan {
   bool tc = false;   // tensor-core kernel (either of the two below)
   bool tcq = false;  // the quantised-pool tensor-core kernel
   int qvp = 0, rows = 0, chunk = 0, nsplit = 0;
+  bool merge_kernel = false;   // the splits are merged by a kernel of their own
   size_t ws = 0;     // workspace bytes: status block, counters, partials
   size_t off_cnt = 0, off_ml = 0, off_o = 0;
 };
@@ -216,6 +217,14 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   }
   pl->chunk = (int)round_up((L + best_ns - 1) / best_ns, align);
   pl->nsplit = (L + pl->chunk - 1) / pl->chunk;
+  // A latency-bound 16-bit decode (one wave of CTAs, each streaming at most
+  // four tiles) merges its splits in a kernel of its own: its last CTA per
+  // (slice, KV head) would merge on the critical path with six warps, one
+  // L2 round trip per 16 splits per thread; the merge kernel gives every
+  // (row, 4 dimensions) a thread and costs one launch gap (sparse D 256, 16
+  // splits: 4.9 us of in-kernel merge).
+  pl->merge_kernel = pl->tc && !pl->tcq && pl->nsplit > 1 && units * pl->nsplit <= slots &&
+                     pl->chunk <= 4 * align;
   // [status block][counters][(max, sum) partials][O partials]
   const size_t nunit = (size_t)units;
   const size_t cnt_bytes = round_up(nunit * sizeof(unsigned int), 256);
@@ -262,6 +271,15 @@ size_t fa_rows_workspace_size(const fa_rows_args* a, int is_prefill) {
   DecodePlan pl;
   if (plan_decode(a, &pl) != FA_OK) return 0;
   return pl.ws;
+}
+
+int fa_rows_decode_launches(const fa_rows_args* a) {
+  g_err[0] = 0;
+  if (check_common(a) != FA_OK) return -1;
+  DecodePlan pl;
+  if (plan_decode(a, &pl) != FA_OK) return -1;
+  if ((long long)a->S * a->Nq == 0) return 0;
+  return pl.merge_kernel ? 2 : 1;
 }
 
 fa_status fa_rows_workspace_init(void* ws, size_t ws_bytes, fa_stream_t stream) {
@@ -335,12 +353,14 @@ fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_st
   p.mask_kind = a->mask_kind;
   p.qscale = a->scale * far::kLog2e;
   p.wait_ns = wait_limit();
+  p.merge_kernel = pl.merge_kernel ? 1 : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;
   const int kind = kv_kind(a->kv_dtype);
   if (pl.tc) {
     unsigned int* err = static_cast<unsigned int*>(ws);   // the status word
     e = pl.tcq ? far::decode_tcq_launch(p, kind, err, s) : far::decode_tc_launch(p, a->D, kind, err, s);
+    if (e == cudaSuccess && pl.merge_kernel) e = far::decode_merge_launch(p, a->D, s);
   } else if (kind == far::KV_BF16) {
     e = far::decode_launch_bf16(p, a->D, pl.qvp, s);
   } else if (kind == far::KV_F16) {

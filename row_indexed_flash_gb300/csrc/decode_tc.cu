@@ -718,7 +718,7 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   // on its split counter (marked as aborted) so the counter ends at zero.
   const bool aborted = *abort_flag != 0;
   if (aborted && threadIdx.x == 0 && kp.err) atomicOr(kp.err, FA_WS_WAIT_EXPIRED);
-  if (ns_unit == 1) return;
+  if (ns_unit == 1 || p.merge_kernel) return;
 
   // ---- cross-split merge by the last CTA of this (slice, KV head)
   __threadfence();
@@ -834,6 +834,18 @@ int decode_tc_occupancy(int D, int kind, int qv) {
 }
 
 int decode_tc_tile() { return dk::BN; }
+
+cudaError_t decode_merge_launch(const DecodeParams& a, int D, cudaStream_t st) {
+  const int items = a.QV * (D / 4);
+  const dim3 grid((unsigned)((items + 63) / 64), (unsigned)(a.S * a.Hkv));
+  if (D == 128)
+    merge_splits_kernel<128><<<grid, 64, 0, st>>>(a);
+  else if (D == 256)
+    merge_splits_kernel<256><<<grid, 64, 0, st>>>(a);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
 
 cudaError_t decode_tc_launch(const DecodeParams& a, int D, int kind, unsigned int* err, cudaStream_t st) {
   const int q = qv_pow2(a.QV);

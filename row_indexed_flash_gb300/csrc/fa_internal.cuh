@@ -59,6 +59,7 @@ struct DecodeParams {
   int mask_kind;            // fa_mask_kind
   float qscale;             // scale * log2(e), folded into Q
   unsigned long long wait_ns;   // limit of a pipeline wait (tensor-core kernels)
+  int merge_kernel;         // 1: the splits are merged by decode_merge_launch after the decode, not in it
 };
 
 struct DecodeConfig {
@@ -82,6 +83,10 @@ bool decode_tc_supported(int D, int kind, int qv, int mask_kind);
 int decode_tc_occupancy(int D, int kind, int qv);
 int decode_tc_tile();
 cudaError_t decode_tc_launch(const DecodeParams& p, int D, int kind, unsigned int* err, cudaStream_t st);
+// The cross-split merge as a kernel of its own (one thread per query-vector
+// row and 4 dimensions of every (slice, KV head)), for decodes launched with
+// merge_kernel = 1.  D 128 or 256.
+cudaError_t decode_merge_launch(const DecodeParams& p, int D, cudaStream_t st);
 
 // Tensor-core decode for quantised pools (INT8 / INT4 / FP8 codes + fp16 scales),
 // D 128: one CTA per SM with a deep code ring.  Same workspace as above.

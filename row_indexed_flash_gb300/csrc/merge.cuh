@@ -120,4 +120,70 @@ __device__ __forceinline__ void merge_splits(const DecodeParams& p, size_t unit,
   }
 }
 
+// The same merge as a kernel of its own, for small decodes whose last CTA per
+// (slice, KV head) would otherwise merge on the critical path with a few
+// hundred threads: here every (query-vector row, 4 dimensions) of every unit
+// has a thread, whose (m_k, l_k) and O_k loads for 16 splits at a time go out
+// together, with a running maximum across groups of 16.  Units that one split
+// covers (their output was written by the decode) are skipped.
+template <int D>
+__global__ void __launch_bounds__(64) merge_splits_kernel(const DecodeParams p) {
+  constexpr int D4 = D / 4;
+  const float NEG_INF = __int_as_float(0xff800000);
+  const int unit = blockIdx.y;
+  const int s = unit / p.Hkv, g = unit % p.Hkv;
+  int n_s = p.L;
+  if (p.kv_len) n_s = min(max(__ldg(p.kv_len + s), 0), p.L);
+  const int ns = n_s > 0 && p.chunk > 0 ? (n_s + p.chunk - 1) / p.chunk : 1;
+  const int QV = p.QV;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (ns <= 1 || t >= QV * D4) return;
+  const int r = t / D4, d4 = t % D4;
+  const size_t base = (size_t)unit * p.nsplit;
+  const float2* pml = reinterpret_cast<const float2*>(p.part_ml) + base * QV + r;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + (base * QV + r) * (size_t)D) + d4;
+  const size_t kstride = (size_t)QV * D4;
+  float M = NEG_INF, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < ns; k0 += 16) {
+    float2 ml[16];
+    float4 v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      ml[u] = k0 + u < ns ? __ldcg(pml + (size_t)(k0 + u) * QV) : make_float2(NEG_INF, 0.f);
+      v[u] = k0 + u < ns ? __ldcg(po + (size_t)(k0 + u) * kstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float Mg = M;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) Mg = fmaxf(Mg, ml[u].x);
+    if (Mg == NEG_INF) continue;   // nothing seen yet
+    const float c = M == NEG_INF ? 0.f : fast_ex2(M - Mg);   // rescale of the groups before
+    L *= c;
+    acc.x *= c;
+    acc.y *= c;
+    acc.z *= c;
+    acc.w *= c;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float wk = ml[u].x == NEG_INF ? 0.f : fast_ex2(ml[u].x - Mg);
+      if (wk != 0.f) {   // a zero weight skips its value: an unwritten partial never contributes
+        L = fmaf(ml[u].y, wk, L);
+        acc.x = fmaf(wk, v[u].x, acc.x);
+        acc.y = fmaf(wk, v[u].y, acc.y);
+        acc.z = fmaf(wk, v[u].z, acc.z);
+        acc.w = fmaf(wk, v[u].w, acc.w);
+      }
+    }
+    M = Mg;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int i = r / p.G, h = g * p.G + r % p.G;
+  const size_t oi = ((size_t)s * p.Nq + i) * p.Hq + h;
+  store_out(p.out, oi * D + 4 * d4 + 0, acc.x * inv, p.out_dtype);
+  store_out(p.out, oi * D + 4 * d4 + 1, acc.y * inv, p.out_dtype);
+  store_out(p.out, oi * D + 4 * d4 + 2, acc.z * inv, p.out_dtype);
+  store_out(p.out, oi * D + 4 * d4 + 3, acc.w * inv, p.out_dtype);
+  if (p.lse && d4 == 0) p.lse[oi] = L > 0.f ? (M + __log2f(L)) * kLn2 : NEG_INF;
+}
+
 }  // namespace far

@@ -154,6 +154,34 @@ def test_repeated_calls_are_identical_and_split_plans_agree():
     assert_parity(c, a.double().cpu().numpy())
 
 
+def _decode_launches(p):
+    import ctypes
+    q, k, v = dev_bits(p.q, p.dtype), dev_bits(p.k, p.dtype), dev_bits(p.v, p.dtype)
+    kw = {} if p.kv_len is None else {"kv_len": torch.from_numpy(p.kv_len).cuda()}
+    a, _, _ = far.make_args(q, k, v, torch.from_numpy(p.kv_rows).cuda(), p.scale, causal=p.causal, **kw)
+    return far.lib().fa_rows_decode_launches(ctypes.byref(a))
+
+
+@pytest.mark.parametrize("kw,launches", [
+    (dict(S=1, Hq=16, Hkv=2, D=256, R=4096, L=2048), 2),                      # the sparse shape: 16 splits
+    (dict(S=3, Hq=8, Hkv=2, D=128, R=8192, L=600, kv_len=True), 2),          # short slices write directly
+    (dict(S=2, Hq=32, Hkv=8, D=128, R=9000, L=300, causal=True, Nq=1), 2),
+    (dict(S=4, Hq=32, Hkv=8, D=128, R=40000, L=16000), 1),                    # long chunks: merged in the decode
+])
+def test_split_merge_in_the_decode_and_as_its_own_kernel(kw, launches):
+    """Both places the splits of a (slice, KV head) are merged: by the last
+    CTA of the decode, or (a latency-bound 16-bit decode) by a merge kernel
+    after it.  Parity with the oracle, and a repeated call bit-identical."""
+    p = synth.random_problem(3500 + launches + kw["L"], **kw)
+    assert _decode_launches(p) == launches
+    out, lse = run_decode(p)
+    ref, ref_lse = oracle_for(p)
+    assert_parity(out, ref, f"merge path {launches}")
+    assert_lse(lse, ref_lse)
+    out2, lse2 = run_decode(p)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
 # --- full-size decode workloads ------------------------------------------------
 
 
