@@ -167,7 +167,10 @@ fa_status fa_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
  * Decode: few query rows per slice (Nq * Hq/Hkv <= 32).  Split-KV over the
- * list, online softmax per split, cross-split merge inside the same launch.
+ * list, online softmax per split, cross-split merge inside the same launch
+ * (by the last split of each (slice, KV head) to finish), or, for a
+ * latency-bound 16-bit decode, in a second kernel enqueued right after it on
+ * the same stream (fa_rows_decode_launches tells which).
  * D in {64, 128, 256}; Hq/Hkv a power of two up to 32 (times Nq).
  */
 fa_status fa_rows_decode(const fa_rows_args* a, void* ws, size_t ws_bytes, fa_stream_t stream);
