@@ -450,6 +450,9 @@ __global__ void __launch_bounds__(dk::NWARP * 32, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
+  // a merge kernel launched after this one (programmatic dependent launch)
+  // may be scheduled from here on; it waits for this grid's completion
+  if (p.merge_kernel) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp >= 1 && warp <= NPROD) {
     // ------------------------------------------------------------ producers
@@ -835,16 +838,24 @@ int decode_tc_occupancy(int D, int kind, int qv) {
 
 int decode_tc_tile() { return dk::BN; }
 
+// Launched as a programmatic dependent of the decode: its CTAs may be
+// scheduled while the decode's last CTAs run, and wait (griddepcontrol.wait)
+// for the decode grid to complete and its writes to be visible.
 cudaError_t decode_merge_launch(const DecodeParams& a, int D, cudaStream_t st) {
   const int items = a.QV * (D / 4);
-  const dim3 grid((unsigned)((items + 63) / 64), (unsigned)(a.S * a.Hkv));
-  if (D == 128)
-    merge_splits_kernel<128><<<grid, 64, 0, st>>>(a);
-  else if (D == 256)
-    merge_splits_kernel<256><<<grid, 64, 0, st>>>(a);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)((items + 63) / 64), (unsigned)(a.S * a.Hkv));
+  cfg.blockDim = dim3(64);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (D == 128) return cudaLaunchKernelEx(&cfg, merge_splits_kernel<128>, a);
+  if (D == 256) return cudaLaunchKernelEx(&cfg, merge_splits_kernel<256>, a);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t decode_tc_launch(const DecodeParams& a, int D, int kind, unsigned int* err, cudaStream_t st) {

@@ -128,6 +128,9 @@ __device__ __forceinline__ void merge_splits(const DecodeParams& p, size_t unit,
 // covers (their output was written by the decode) are skipped.
 template <int D>
 __global__ void __launch_bounds__(64) merge_splits_kernel(const DecodeParams p) {
+  // launched as a programmatic dependent of the decode: wait for that grid to
+  // complete and its partials to be visible (a no-op for a plain launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int D4 = D / 4;
   const float NEG_INF = __int_as_float(0xff800000);
   const int unit = blockIdx.y;
