@@ -90,6 +90,9 @@ def test_bad_arguments_are_rejected_on_the_host(lib, kw, status):
 
 def test_null_args_and_empty_batch(lib):
     assert lib.fa_rows_decode(None, None, 0, None) == 1
+    assert lib.fa_rows_decode_launches(None) == -1 and far.fa_last_error()
+    bad = _args(D=100)
+    assert lib.fa_rows_decode_launches(ctypes.byref(bad)) == -1
     a = _args(S=0)
     assert lib.fa_rows_prefill(ctypes.byref(a), None, 0, None) in (0, 2)
 
