@@ -174,7 +174,7 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
   const bool ragged = a->n_valid_hint > 0;
   const double lavg = ragged ? (double)a->n_valid_hint / a->S : (double)L;
   // fixed cost of a CTA (start-up, pipeline fill, merge), in streamed rows
-  const double c_cta = pl->tc ? 256.0 : 64.0, c_split = 2.0, c_empty = 16.0, c_cta_q = 1024.0;
+  const double c_cta = pl->tc ? 256.0 : 64.0, c_split = 2.0, c_empty = 16.0, c_cta_q = 1536.0;
   const int ns_lo = (int)((L + chunk_max - 1) / chunk_max);
   if (ns_lo > kMaxSplits)
     return fail(FA_ERR_UNSUPPORTED, "list length %d needs more than %d splits of %d entries", L, kMaxSplits, chunk_max);
@@ -193,10 +193,12 @@ fa_status plan_decode(const fa_rows_args* a, DecodePlan* pl) {
       // ragged lists on the quantised kernel (one CTA per SM): CTAs of unequal
       // length backfill the SMs, so the step is about the rows streamed plus
       // a fixed cost per busy CTA (pipeline fill, the groups' combine, the
-      // split's share of the merge: about 1 024 rows), over the slots, plus
-      // half a chunk of tail.  Measured on 32 paged sequences of 1k-128k
-      // tokens: 8-16 splits 0.453-0.464 ms, the wave model's 31 splits 0.534.
-      const double per_unit = ceil(lavg / (double)chunk);
+      // split's share of the merge: about 1 536 rows), over the slots, plus
+      // half a chunk of tail; a slice of the mean length holds lavg / chunk
+      // + 1/2 busy splits on average over a spread of lengths.  Measured on
+      // 32 paged sequences of 1k-128k tokens: 6 / 8 / 10 / 13 splits 0.467 /
+      // 0.450 / 0.441 / 0.455 ms, the wave model's 31 splits 0.534.
+      const double per_unit = lavg / (double)chunk + 0.5;
       const double busy = units * per_unit;
       cost = (units * lavg + busy * c_cta_q) / slots + 0.5 * (double)chunk +
              c_empty * ((double)units * ns_eff - busy) / slots + c_split * per_unit;
